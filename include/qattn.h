@@ -1,0 +1,226 @@
+/*
+ * qattn.h -- C ABI of libqattn: attention computed directly over an INT4
+ * KV cache on NVIDIA GB300 (sm_103a).
+ *
+ * Sources of the operations (page title and section):
+ *   [FAQ3]  "Quantized Cross-Attention: Extending FlashAttention-3 with
+ *           In-SRAM Dequantization": §3.1 in-SRAM dequantization fused into
+ *           the attention loop; §3.2 tile of 4-bit codes plus one FP16 scale
+ *           per token; §4.1 kernel signature ([batch, heads, seq, dim]
+ *           ordering, compressed KV, per-token scales, output).
+ *   [TA]    TurboAttention (arXiv 2412.08585): §2.1 prefill and decoding with
+ *           a KV cache (K_t = K_{t-1} | k_t); §2.2 Equation 2 (S = QK^T,
+ *           P = softmax(S), H = PV) and FlashAttention's tiled online
+ *           softmax; §2.3 symmetric quantization (zero point 0).
+ *   [OTQ]   Open-TQ-Metal abstract on the "Attention Quantization" listing:
+ *           int4 KV quantized on the fly, attention on the compressed form.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Memory.   Every pointer is a DEVICE pointer unless marked "host".  The
+ *           caller owns every buffer; the library allocates nothing and
+ *           keeps no state between calls besides immutable kernel handles
+ *           and one device status word (qattn_read_device_flags).
+ * Streams.  Work is enqueued on `stream` (a cudaStream_t; NULL = legacy
+ *           default stream).  No call synchronises, except
+ *           qattn_read_device_flags; results are ready when the stream has run.
+ * Errors.   Arguments are validated on the host before any launch; a
+ *           failed check returns an error code and enqueues nothing.
+ *           QATTN_ERR_CUDA reports a launch failure (cudaGetLastError).
+ *           qattn_last_error() gives a human-readable reason for the most
+ *           recent failure on the calling thread.
+ * Layout.   All tensors are dense row-major in the shapes given, 16-byte
+ *           aligned.  fp16 values travel as uint16_t bit patterns.
+ *
+ * The KV-cache format (bit-exact; [FAQ3] §3.2, [TA] §2.3)
+ * -------------------------------------------------------
+ *   row      one (token, kv-head) vector of D values
+ *   scale    s = fp16(fp32(absmax / 7)), round-to-nearest-even twice; a
+ *            scale that overflows fp16 saturates to 65504
+ *   codes    c_i = clamp(round_half_even(x_i / s), -7, 7) on the exact
+ *            quotient; all codes 0 when s == 0
+ *   packing  D/2 bytes per row; element 2k in the low nibble of byte k,
+ *            element 2k+1 in the high nibble; two's complement nibbles
+ *   value    x^_i = c_i * s
+ *
+ *   contiguous cache: codes [batch, Hkv, capacity, D/2] uint8,
+ *                     scales [batch, Hkv, capacity] fp16
+ *   paged cache:      codes [num_pages, Hkv, page_size, D/2] uint8,
+ *                     scales [num_pages, Hkv, page_size] fp16; token t of
+ *                     sequence b lives in page page_table[b*max_pages + t/page_size]
+ *                     at offset t % page_size.
+ *
+ * Attention semantics ([TA] §2.2 Eq. 2, per head and batch instance)
+ * -------------------------------------------------------------------
+ *   O = softmax(softmax_scale * Q K^T + mask) V over the dequantized cache.
+ *   GQA: query head h reads kv head h / (Hq / Hkv).
+ *   Causal masking is bottom-right aligned: query i of Nq sees key j of Nk
+ *   iff j <= i + Nk - Nq.  A decode query sees all seq_len keys.
+ *   lse = natural-log log-sum-exp of the scaled scores, fp32.
+ *   A query row that sees no key gives O = 0 and lse = -inf.
+ */
+#ifndef QATTN_H
+#define QATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t (struct CUstream_st *). */
+typedef struct CUstream_st *qattn_stream_t;
+
+typedef enum qattn_status {
+  QATTN_OK = 0,
+  QATTN_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer */
+  QATTN_ERR_UNSUPPORTED = 2, /* valid request outside what the kernels cover */
+  QATTN_ERR_WORKSPACE = 3,   /* workspace missing or too small */
+  QATTN_ERR_CUDA = 4         /* a CUDA runtime/driver call failed */
+} qattn_status;
+
+typedef enum qattn_dtype {
+  QATTN_F32 = 0,
+  QATTN_F16 = 1
+} qattn_dtype;
+
+/* Fixed limits (checked by every call). */
+#define QATTN_PAGE_SIZE 64     /* tokens per page of a paged cache */
+#define QATTN_MAX_GROUP 8      /* largest Hq / Hkv */
+#define QATTN_MAX_SPLITS 1024  /* largest num_splits of qattn_decode */
+
+/* Bits of the device status word (qattn_read_device_flags). */
+#define QATTN_FLAG_WAIT_TIMEOUT 1u /* a pipeline wait gave up (kernel returned early) */
+#define QATTN_FLAG_BAD_PAGE 2u     /* a page id or length was out of range; rows skipped */
+#define QATTN_FLAG_TMEM 4u         /* tensor-memory allocation failed */
+
+/*
+ * Where the quantized K and V live.  Passed by host pointer; the struct
+ * itself is read during the call only.
+ *   head_dim         D, 64 or 128
+ *   num_kv_heads     Hkv
+ *   page_table       NULL selects the contiguous layout; otherwise a device
+ *                    int32 array [batch, max_pages_per_seq] of physical page
+ *                    ids (-1 or any id outside [0, num_pages) = no page)
+ *   capacity         contiguous layout: tokens per (sequence, kv-head);
+ *                    must be a positive multiple of 64
+ *   page_size        paged layout: must be QATTN_PAGE_SIZE
+ *   num_pages        paged layout: pages in the pool
+ */
+typedef struct qattn_kv_cache {
+  uint8_t *k_codes;
+  uint16_t *k_scales;
+  uint8_t *v_codes;
+  uint16_t *v_scales;
+  int32_t head_dim;
+  int32_t num_kv_heads;
+  const int32_t *page_table;
+  int32_t max_pages_per_seq;
+  int32_t page_size;
+  int64_t capacity;
+  int64_t num_pages;
+} qattn_kv_cache;
+
+/*
+ * qattn_quantize_kv -- quantize new K and V rows and write them into the
+ * cache (quantize-on-append; [TA] §2.1 K_t = K_{t-1} | k_t, codec above).
+ *
+ *   k, v        [batch, Hkv, n, D] of x_dtype (fp32 or fp16)
+ *   batch, n    sequences, and new rows per (sequence, kv-head); n >= 0
+ *   start_pos   [batch] int32: position of the first new row of each
+ *               sequence; NULL means 0 for every sequence
+ *   cache       destination (contiguous or paged)
+ *
+ * Row i of sequence b goes to token position start_pos[b] + i.  Rows whose
+ * position falls at or past `capacity` (contiguous) or in a missing page
+ * (paged) are not written.  Both K and V are written by one launch.
+ */
+qattn_status qattn_quantize_kv(const void *k, const void *v, qattn_dtype x_dtype,
+                               int32_t batch, int32_t n, const int32_t *start_pos,
+                               const qattn_kv_cache *cache, qattn_stream_t stream);
+
+/*
+ * qattn_decode_workspace_size -- bytes of workspace qattn_decode needs for
+ * `num_splits` key chunks (0 = the automatic choice for these sizes on the
+ * current device).  Host-only; returns 0 for invalid sizes.
+ */
+size_t qattn_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t max_seq_len, int32_t num_splits);
+
+/*
+ * qattn_decode -- one query token per sequence against its whole cache
+ * ([TA] §2.1 decoding; fused in-SRAM dequantization as in [FAQ3] §3.1).
+ *
+ *   q            [batch, Hq, D] fp16
+ *   cache        contiguous or paged INT4 cache
+ *   seq_lens     [batch] int32, 0 <= seq_lens[b] <= max_seq_len; lengths
+ *                beyond the cache (capacity, or max_pages_per_seq * 64) are
+ *                clamped and flagged QATTN_FLAG_BAD_PAGE
+ *   max_seq_len  host int, an upper bound of seq_lens used to size the split
+ *   softmax_scale multiplies Q K^T
+ *   num_splits   key chunks per sequence (split-KV); 0 = automatic.  With
+ *                more than one chunk, partial results go to the workspace and
+ *                are merged by the log-sum-exp combine inside this call.
+ *   workspace    device scratch of at least qattn_decode_workspace_size()
+ *                bytes for the same arguments (may be NULL if that is 0)
+ *   out          [batch, Hq, D] fp16
+ *   lse          [batch, Hq] fp32, or NULL
+ */
+qattn_status qattn_decode(const uint16_t *q, const qattn_kv_cache *cache, const int32_t *seq_lens,
+                          int32_t batch, int32_t num_q_heads, int32_t max_seq_len,
+                          float softmax_scale, int32_t num_splits, void *workspace,
+                          size_t workspace_bytes, uint16_t *out, float *lse,
+                          qattn_stream_t stream);
+
+/*
+ * qattn_prefill -- Nq query rows per sequence against Nk cached keys
+ * ([TA] §2.1 prefill, §2.2 FlashAttention tiling; dense contractions on
+ * the tensor cores with the dequantization fused ahead of the operand
+ * stage, [FAQ3] §3.1).  Contiguous cache only.
+ *
+ *   q        [batch, Hq, Nq, D] fp16
+ *   nq, nk   query rows and keys per sequence, 1 <= nq <= nk <= capacity
+ *   causal   0 or 1 (bottom-right aligned)
+ *   out      [batch, Hq, Nq, D] fp16
+ *   lse      [batch, Hq, Nq] fp32, or NULL
+ */
+qattn_status qattn_prefill(const uint16_t *q, const qattn_kv_cache *cache, int32_t batch,
+                           int32_t num_q_heads, int32_t nq, int32_t nk, float softmax_scale,
+                           int32_t causal, uint16_t *out, float *lse, qattn_stream_t stream);
+
+/*
+ * qattn_combine -- log-sum-exp merge of split-KV partial results.
+ *
+ *   partial_o    [num_splits, rows, D] fp32, each normalised within its split
+ *   partial_lse  [num_splits, rows] fp32 (natural log); a split with
+ *                lse = -inf saw no key and its partial_o is never read
+ *   out          [rows, D] fp16:  O = sum_c exp(lse_c - L) O_c,
+ *   lse          [rows] fp32 or NULL:  L = ln sum_c exp(lse_c)
+ * Rows whose every split is empty get O = 0 and lse = -inf.
+ */
+qattn_status qattn_combine(const float *partial_o, const float *partial_lse, int32_t num_splits,
+                           int64_t rows, int32_t head_dim, uint16_t *out, float *lse,
+                           qattn_stream_t stream);
+
+/*
+ * qattn_read_device_flags -- synchronise the current device, return in
+ * *flags (host) the OR of QATTN_FLAG_* bits the kernels raised since the
+ * last clear, and clear them if `clear` is non-zero.
+ */
+qattn_status qattn_read_device_flags(uint32_t *flags, int32_t clear);
+
+/* Static description of a status code (never NULL). */
+const char *qattn_status_string(qattn_status status);
+
+/* Reason for the most recent non-OK status on the calling thread (host). */
+const char *qattn_last_error(void);
+
+/* Library version, e.g. 0x000100 for 0.1.0. */
+int32_t qattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QATTN_H */

@@ -1,0 +1,63 @@
+// internal.h -- launcher interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qattn {
+
+// Device view of a KV cache (contiguous or paged), passed by value to kernels.
+struct KvView {
+  uint8_t *k_codes;
+  uint16_t *k_scales;
+  uint8_t *v_codes;
+  uint16_t *v_scales;
+  const int32_t *page_table;  // nullptr = contiguous
+  int64_t capacity;           // contiguous: tokens per (sequence, kv-head)
+  int64_t num_pages;          // paged: pool size
+  int32_t max_pages;          // paged: page-table row length
+  int32_t hkv;
+  int32_t head_dim;
+};
+
+constexpr int kPage = 64;  // tokens per page and per decode pipeline stage
+
+// quantize.cu
+cudaError_t launch_quantize(const void *k, const void *v, bool fp16_in, int batch, int n,
+                            const int32_t *start_pos, const KvView &cache, uint32_t *err,
+                            cudaStream_t stream);
+
+// decode.cu: split-KV decode.  With splits == 1 it writes out/lse directly;
+// otherwise it writes fp32 partials (partial_o [splits, B*Hq, D], partial_lse
+// [splits, B*Hq]) that launch_combine merges.
+struct DecodeArgs {
+  const uint16_t *q;
+  const int32_t *seq_lens;
+  uint16_t *out;
+  float *lse;
+  float *partial_o;
+  float *partial_lse;
+  int batch, hq, splits, chunk;  // chunk: tokens per split (multiple of kPage)
+  float scale_log2;              // softmax_scale * log2(e)
+};
+cudaError_t launch_decode(const DecodeArgs &a, const KvView &cache, const CUtensorMap &kmap,
+                          const CUtensorMap &vmap, uint32_t *err, cudaStream_t stream);
+
+// combine.cu (pdl: launched as a programmatic dependent of the previous kernel)
+cudaError_t launch_combine(const float *partial_o, const float *partial_lse, int splits,
+                           int64_t rows, int head_dim, uint16_t *out, float *lse, bool pdl,
+                           cudaStream_t stream);
+
+// prefill.cu
+struct PrefillArgs {
+  const uint16_t *q;
+  uint16_t *out;
+  float *lse;
+  int batch, hq, nq, nk, causal;
+  float scale_log2;
+};
+cudaError_t launch_prefill(const PrefillArgs &a, const KvView &cache, const CUtensorMap &kmap,
+                           const CUtensorMap &vmap, uint32_t *err, cudaStream_t stream);
+
+}  // namespace qattn
