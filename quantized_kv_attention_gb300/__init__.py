@@ -1,0 +1,245 @@
+"""Python binding of libqattn: INT4-KV attention on GB300 (sm_103a).
+
+Argument marshalling only: every step of the attention path runs in the
+library's CUDA kernels.  PyTorch provides device memory and the current
+stream.  The calls mirror the C ABI in include/qattn.h:
+
+    quantize_kv(k, v, cache, start_pos=None)          quantize-on-append
+    decode(q, cache, seq_lens, max_seq_len, scale)    one query per sequence
+    prefill(q, cache, nq, nk, scale, causal)          Nq queries per sequence
+    combine(partial_o, partial_lse)                   log-sum-exp merge
+
+There is no fallback: if libqattn.so is missing or fails to load, every call
+raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libqattn.so")
+
+QATTN_OK, QATTN_ERR_INVALID_ARG, QATTN_ERR_UNSUPPORTED, QATTN_ERR_WORKSPACE, QATTN_ERR_CUDA = range(5)
+QATTN_F32, QATTN_F16 = 0, 1
+PAGE_SIZE = 64
+MAX_GROUP = 8
+MAX_SPLITS = 1024
+FLAG_WAIT_TIMEOUT, FLAG_BAD_PAGE, FLAG_TMEM = 1, 2, 4
+
+# Every symbol include/qattn.h declares.
+EXPORTS = (
+    "qattn_quantize_kv", "qattn_decode_workspace_size", "qattn_decode", "qattn_prefill",
+    "qattn_combine", "qattn_read_device_flags", "qattn_status_string", "qattn_last_error",
+    "qattn_version",
+)
+
+
+class QattnError(RuntimeError):
+    """A non-OK status returned by libqattn."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+class KvCacheStruct(ctypes.Structure):
+    """Layout of ``qattn_kv_cache``."""
+    _fields_ = [
+        ("k_codes", ctypes.c_void_p),
+        ("k_scales", ctypes.c_void_p),
+        ("v_codes", ctypes.c_void_p),
+        ("v_scales", ctypes.c_void_p),
+        ("head_dim", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("page_table", ctypes.c_void_p),
+        ("max_pages_per_seq", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("capacity", ctypes.c_int64),
+        ("num_pages", ctypes.c_int64),
+    ]
+
+
+_lib_handle = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libqattn.so (once) and declare the C signatures."""
+    global _lib_handle
+    if _lib_handle is not None:
+        return _lib_handle
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is not built: run quantized_kv_attention_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, i32, i64, f32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    cache_p = ctypes.POINTER(KvCacheStruct)
+    sig = {
+        "qattn_quantize_kv": (i32, [vp, vp, i32, i32, i32, vp, cache_p, vp]),
+        "qattn_decode_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
+        "qattn_decode": (i32, [vp, cache_p, vp, i32, i32, i32, f32, i32, vp, sz, vp, vp, vp]),
+        "qattn_prefill": (i32, [vp, cache_p, i32, i32, i32, i32, f32, i32, vp, vp, vp]),
+        "qattn_combine": (i32, [vp, vp, i32, i64, i32, vp, vp, vp]),
+        "qattn_read_device_flags": (i32, [ctypes.POINTER(ctypes.c_uint32), i32]),
+        "qattn_status_string": (ctypes.c_char_p, [i32]),
+        "qattn_last_error": (ctypes.c_char_p, []),
+        "qattn_version": (i32, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib_handle = lib
+    return lib
+
+
+def _check(status: int, what: str) -> None:
+    if status != QATTN_OK:
+        lib = load_library()
+        msg = lib.qattn_last_error().decode()
+        raise QattnError(status, f"{what}: {lib.qattn_status_string(status).decode()}: {msg}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+@dataclass
+class KvCache:
+    """Caller-owned INT4 KV cache (contiguous or paged) as torch tensors.
+
+    contiguous: codes [B, Hkv, capacity, D/2] uint8, scales [B, Hkv, capacity] fp16
+    paged:      codes [P, Hkv, 64, D/2] uint8, scales [P, Hkv, 64] fp16,
+                page_table [B, max_pages] int32 (-1 = no page)
+    """
+    k_codes: torch.Tensor
+    k_scales: torch.Tensor
+    v_codes: torch.Tensor
+    v_scales: torch.Tensor
+    head_dim: int
+    num_kv_heads: int
+    capacity: int = 0
+    page_table: Optional[torch.Tensor] = None
+    num_pages: int = 0
+
+    @staticmethod
+    def contiguous(batch, num_kv_heads, capacity, head_dim, device="cuda"):
+        cap = -(-capacity // PAGE_SIZE) * PAGE_SIZE
+        codes = lambda: torch.zeros(batch, num_kv_heads, cap, head_dim // 2, dtype=torch.uint8, device=device)
+        scales = lambda: torch.zeros(batch, num_kv_heads, cap, dtype=torch.float16, device=device)
+        return KvCache(codes(), scales(), codes(), scales(), head_dim, num_kv_heads, capacity=cap)
+
+    @staticmethod
+    def paged(num_pages, num_kv_heads, head_dim, page_table, device="cuda"):
+        codes = lambda: torch.zeros(num_pages, num_kv_heads, PAGE_SIZE, head_dim // 2, dtype=torch.uint8, device=device)
+        scales = lambda: torch.zeros(num_pages, num_kv_heads, PAGE_SIZE, dtype=torch.float16, device=device)
+        pt = page_table.to(device=device, dtype=torch.int32).contiguous()
+        return KvCache(codes(), scales(), codes(), scales(), head_dim, num_kv_heads,
+                       page_table=pt, num_pages=num_pages)
+
+    @property
+    def paged_layout(self) -> bool:
+        return self.page_table is not None
+
+    def struct(self) -> KvCacheStruct:
+        s = KvCacheStruct()
+        s.k_codes, s.k_scales = self.k_codes.data_ptr(), self.k_scales.data_ptr()
+        s.v_codes, s.v_scales = self.v_codes.data_ptr(), self.v_scales.data_ptr()
+        s.head_dim, s.num_kv_heads = self.head_dim, self.num_kv_heads
+        if self.page_table is not None:
+            s.page_table = self.page_table.data_ptr()
+            s.max_pages_per_seq = self.page_table.shape[1]
+            s.page_size = PAGE_SIZE
+            s.num_pages = self.num_pages
+        else:
+            s.page_table = None
+            s.capacity = self.capacity
+        return s
+
+
+def quantize_kv(k: torch.Tensor, v: torch.Tensor, cache: KvCache,
+                start_pos: Optional[torch.Tensor] = None) -> None:
+    """Quantize k, v [B, Hkv, n, D] (fp32 or fp16) into the cache at start_pos[b] + i."""
+    if k.dtype not in (torch.float32, torch.float16) or v.dtype != k.dtype:
+        raise TypeError("k and v must both be float32 or float16")
+    k, v = k.contiguous(), v.contiguous()
+    B, _, n, _ = k.shape
+    sp = None if start_pos is None else start_pos.to(device=k.device, dtype=torch.int32).contiguous()
+    st = cache.struct()
+    dt = QATTN_F16 if k.dtype == torch.float16 else QATTN_F32
+    _check(load_library().qattn_quantize_kv(_ptr(k), _ptr(v), dt, B, n, _ptr(sp), ctypes.byref(st),
+                                            _stream(k.device)), "qattn_quantize_kv")
+
+
+def decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len, num_splits=0) -> int:
+    return int(load_library().qattn_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
+                                                          max_seq_len, num_splits))
+
+
+def decode(q: torch.Tensor, cache: KvCache, seq_lens: torch.Tensor, max_seq_len: int,
+           softmax_scale: float, num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
+           out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+           return_lse: bool = False):
+    """q [B, Hq, D] fp16 -> out [B, Hq, D] fp16 (and lse [B, Hq] fp32)."""
+    q = q.contiguous()
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    need = decode_workspace_size(B, Hq, cache.num_kv_heads, D, max_seq_len, num_splits)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    sl = seq_lens.to(device=q.device, dtype=torch.int32).contiguous()
+    st = cache.struct()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().qattn_decode(_ptr(q), ctypes.byref(st), _ptr(sl), B, Hq, max_seq_len,
+                                       float(softmax_scale), num_splits, _ptr(workspace), ws_bytes,
+                                       _ptr(out), _ptr(lse), _stream(q.device)), "qattn_decode")
+    return (out, lse) if return_lse else out
+
+
+def prefill(q: torch.Tensor, cache: KvCache, nk: int, softmax_scale: float, causal: bool = True,
+            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+            return_lse: bool = False):
+    """q [B, Hq, Nq, D] fp16 against the first nk cached keys -> out [B, Hq, Nq, D] fp16."""
+    q = q.contiguous()
+    B, Hq, Nq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(B, Hq, Nq, dtype=torch.float32, device=q.device)
+    st = cache.struct()
+    _check(load_library().qattn_prefill(_ptr(q), ctypes.byref(st), B, Hq, Nq, nk, float(softmax_scale),
+                                        int(bool(causal)), _ptr(out), _ptr(lse), _stream(q.device)),
+           "qattn_prefill")
+    return (out, lse) if return_lse else out
+
+
+def combine(partial_o: torch.Tensor, partial_lse: torch.Tensor, out: Optional[torch.Tensor] = None,
+            lse: Optional[torch.Tensor] = None, return_lse: bool = False):
+    """partial_o [S, R, D] fp32, partial_lse [S, R] fp32 -> out [R, D] fp16 (and lse [R])."""
+    partial_o, partial_lse = partial_o.contiguous(), partial_lse.contiguous()
+    S, R, D = partial_o.shape
+    if out is None:
+        out = torch.empty(R, D, dtype=torch.float16, device=partial_o.device)
+    if lse is None and return_lse:
+        lse = torch.empty(R, dtype=torch.float32, device=partial_o.device)
+    _check(load_library().qattn_combine(_ptr(partial_o), _ptr(partial_lse), S, R, D, _ptr(out), _ptr(lse),
+                                        _stream(partial_o.device)), "qattn_combine")
+    return (out, lse) if return_lse else out
+
+
+def read_device_flags(clear: bool = True) -> int:
+    """Synchronise the device and return the QATTN_FLAG_* bits raised by the kernels."""
+    f = ctypes.c_uint32(0)
+    _check(load_library().qattn_read_device_flags(ctypes.byref(f), int(clear)), "qattn_read_device_flags")
+    return int(f.value)

@@ -1,0 +1,323 @@
+// api.cu -- the C ABI declared in include/qattn.h: argument validation,
+// TMA descriptor encoding, split-KV sizing and kernel dispatch.  Host code
+// only; no call allocates memory.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/qattn.h"
+#include "internal.h"
+
+namespace qattn {
+
+// The device status word (QATTN_FLAG_* bits), one per device that loads the
+// library; kernels receive its device address.
+__device__ uint32_t g_status_word;
+
+namespace {
+
+thread_local char t_last_error[512] = "";
+
+qattn_status fail(qattn_status st, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+qattn_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(QATTN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  std::once_flag once;
+  uint32_t *status = nullptr;
+  int sms = 0;
+  cudaError_t err = cudaSuccess;
+};
+DeviceState g_dev[kMaxDevices];
+
+// Per-device set-up: the status word's device address and the SM count.
+qattn_status device_state(DeviceState **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(QATTN_ERR_UNSUPPORTED, "device %d", dev);
+  DeviceState &s = g_dev[dev];
+  std::call_once(s.once, [&s, dev]() {
+    s.err = cudaGetSymbolAddress(reinterpret_cast<void **>(&s.status), g_status_word);
+    if (s.err == cudaSuccess) s.err = cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, dev);
+  });
+  if (s.err != cudaSuccess) return cuda_fail(s.err, "device set-up");
+  *out = &s;
+  return QATTN_OK;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+using EncodeFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                              const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                              const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn encode_fn() {
+  static std::once_flag once;
+  static EncodeFn fn = nullptr;
+  std::call_once(once, []() {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  });
+  return fn;
+}
+
+// 2-D view of a code buffer as rows of 128 bytes; one box = one 64-token stage.
+qattn_status code_map(CUtensorMap *map, const void *base, uint64_t bytes, int head_dim) {
+  EncodeFn enc = encode_fn();
+  if (!enc) return fail(QATTN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  const uint64_t rows = bytes / 128;
+  if (rows == 0 || rows > 0x7fffffffull) return fail(QATTN_ERR_UNSUPPORTED, "code buffer of %llu bytes", (unsigned long long)bytes);
+  cuuint64_t dims[2] = {128, rows};
+  cuuint64_t strides[1] = {128};
+  cuuint32_t box[2] = {128, static_cast<cuuint32_t>(kPage * head_dim / 2 / 128)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(QATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return QATTN_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks shared by every call that reads or writes the cache.
+qattn_status check_cache(const qattn_kv_cache *c, int batch, KvView *v, uint64_t *code_bytes) {
+  if (!c) return fail(QATTN_ERR_INVALID_ARG, "cache is NULL");
+  if (!c->k_codes || !c->k_scales || !c->v_codes || !c->v_scales)
+    return fail(QATTN_ERR_INVALID_ARG, "cache has a NULL code or scale pointer");
+  if (!aligned16(c->k_codes) || !aligned16(c->v_codes) || !aligned16(c->k_scales) || !aligned16(c->v_scales))
+    return fail(QATTN_ERR_INVALID_ARG, "cache pointers must be 16-byte aligned");
+  if (c->head_dim != 64 && c->head_dim != 128)
+    return fail(QATTN_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", c->head_dim);
+  if (c->num_kv_heads <= 0) return fail(QATTN_ERR_INVALID_ARG, "num_kv_heads %d", c->num_kv_heads);
+  v->k_codes = c->k_codes, v->k_scales = c->k_scales, v->v_codes = c->v_codes, v->v_scales = c->v_scales;
+  v->page_table = c->page_table;
+  v->hkv = c->num_kv_heads;
+  v->head_dim = c->head_dim;
+  v->capacity = 0, v->num_pages = 0, v->max_pages = 0;
+  if (c->page_table) {
+    if (c->page_size != QATTN_PAGE_SIZE)
+      return fail(QATTN_ERR_UNSUPPORTED, "page_size %d (supported: %d)", c->page_size, QATTN_PAGE_SIZE);
+    if (c->num_pages <= 0 || c->max_pages_per_seq <= 0)
+      return fail(QATTN_ERR_INVALID_ARG, "paged cache needs num_pages > 0 and max_pages_per_seq > 0");
+    v->num_pages = c->num_pages;
+    v->max_pages = c->max_pages_per_seq;
+    *code_bytes = static_cast<uint64_t>(c->num_pages) * c->num_kv_heads * kPage * (c->head_dim / 2);
+  } else {
+    if (c->capacity <= 0 || c->capacity % kPage)
+      return fail(QATTN_ERR_UNSUPPORTED, "capacity %lld must be a positive multiple of %d",
+                  (long long)c->capacity, kPage);
+    v->capacity = c->capacity;
+    *code_bytes = static_cast<uint64_t>(batch) * c->num_kv_heads * c->capacity * (c->head_dim / 2);
+  }
+  return QATTN_OK;
+}
+
+struct SplitPlan {
+  int splits, chunk;
+};
+
+SplitPlan plan_splits(int batch, int hkv, int max_len, int requested, int sms) {
+  const int max_chunks = max_len > 0 ? (max_len + kPage - 1) / kPage : 1;
+  int s = requested;
+  if (s <= 0) {  // about four CTAs per SM in one wave
+    const int units = batch * hkv > 0 ? batch * hkv : 1;
+    s = (4 * sms + units - 1) / units;
+  }
+  if (s > max_chunks) s = max_chunks;
+  if (s > QATTN_MAX_SPLITS) s = QATTN_MAX_SPLITS;
+  if (s < 1) s = 1;
+  int chunk = max_len > 0 ? (max_len + s - 1) / s : kPage;
+  chunk = (chunk + kPage - 1) / kPage * kPage;
+  s = max_len > 0 ? (max_len + chunk - 1) / chunk : 1;
+  return {s, chunk};
+}
+
+size_t workspace_bytes(int splits, int64_t rows, int head_dim) {
+  if (splits <= 1) return 0;
+  const size_t o = static_cast<size_t>(splits) * rows * head_dim * sizeof(float);
+  const size_t o_al = (o + 255) / 256 * 256;
+  return o_al + static_cast<size_t>(splits) * rows * sizeof(float);
+}
+
+}  // namespace
+}  // namespace qattn
+
+using namespace qattn;
+
+extern "C" {
+
+qattn_status qattn_quantize_kv(const void *k, const void *v, qattn_dtype x_dtype, int32_t batch,
+                               int32_t n, const int32_t *start_pos, const qattn_kv_cache *cache,
+                               qattn_stream_t stream) {
+  if (batch < 0 || n < 0) return fail(QATTN_ERR_INVALID_ARG, "batch %d, n %d", batch, n);
+  if (x_dtype != QATTN_F32 && x_dtype != QATTN_F16) return fail(QATTN_ERR_INVALID_ARG, "x_dtype %d", (int)x_dtype);
+  KvView view;
+  uint64_t code_bytes = 0;
+  qattn_status st = check_cache(cache, batch, &view, &code_bytes);
+  if (st != QATTN_OK) return st;
+  if (batch == 0 || n == 0) return QATTN_OK;
+  if (!k || !v) return fail(QATTN_ERR_INVALID_ARG, "k or v is NULL");
+  if (!aligned16(k) || !aligned16(v)) return fail(QATTN_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+  DeviceState *ds;
+  if ((st = device_state(&ds)) != QATTN_OK) return st;
+  cudaError_t e = launch_quantize(k, v, x_dtype == QATTN_F16, batch, n, start_pos, view, ds->status,
+                                  reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "quantize launch");
+}
+
+size_t qattn_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t max_seq_len, int32_t num_splits) {
+  if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_seq_len < 0 || num_splits < 0 ||
+      num_splits > QATTN_MAX_SPLITS || (head_dim != 64 && head_dim != 128))
+    return 0;
+  int sms = 152;
+  int dev = 0;
+  if (num_splits == 0 && cudaGetDevice(&dev) == cudaSuccess) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
+  }
+  cudaGetLastError();
+  const SplitPlan p = plan_splits(batch, num_kv_heads, max_seq_len, num_splits, sms);
+  return workspace_bytes(p.splits, static_cast<int64_t>(batch) * num_q_heads, head_dim);
+}
+
+qattn_status qattn_decode(const uint16_t *q, const qattn_kv_cache *cache, const int32_t *seq_lens,
+                          int32_t batch, int32_t num_q_heads, int32_t max_seq_len,
+                          float softmax_scale, int32_t num_splits, void *workspace,
+                          size_t workspace_size, uint16_t *out, float *lse, qattn_stream_t stream) {
+  if (batch < 0 || num_q_heads <= 0 || max_seq_len < 0)
+    return fail(QATTN_ERR_INVALID_ARG, "batch %d, num_q_heads %d, max_seq_len %d", batch, num_q_heads, max_seq_len);
+  if (num_splits < 0 || num_splits > QATTN_MAX_SPLITS)
+    return fail(QATTN_ERR_INVALID_ARG, "num_splits %d (0..%d)", num_splits, QATTN_MAX_SPLITS);
+  KvView view;
+  uint64_t code_bytes = 0;
+  qattn_status st = check_cache(cache, batch, &view, &code_bytes);
+  if (st != QATTN_OK) return st;
+  if (num_q_heads % view.hkv) return fail(QATTN_ERR_INVALID_ARG, "Hq %d is not a multiple of Hkv %d", num_q_heads, view.hkv);
+  if (num_q_heads / view.hkv > QATTN_MAX_GROUP)
+    return fail(QATTN_ERR_UNSUPPORTED, "group size %d > %d", num_q_heads / view.hkv, QATTN_MAX_GROUP);
+  if (batch == 0) return QATTN_OK;
+  if (!q || !seq_lens || !out) return fail(QATTN_ERR_INVALID_ARG, "q, seq_lens or out is NULL");
+  if (!aligned16(q) || !aligned16(out)) return fail(QATTN_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+  DeviceState *ds;
+  if ((st = device_state(&ds)) != QATTN_OK) return st;
+  const SplitPlan p = plan_splits(batch, view.hkv, max_seq_len, num_splits, ds->sms);
+  const int64_t rows = static_cast<int64_t>(batch) * num_q_heads;
+  const size_t need = workspace_bytes(p.splits, rows, view.head_dim);
+  if (need > 0 && (!workspace || workspace_size < need || !aligned16(workspace)))
+    return fail(QATTN_ERR_WORKSPACE, "workspace of %zu bytes (16-byte aligned) needed, %zu given", need,
+                workspace ? workspace_size : (size_t)0);
+  CUtensorMap kmap, vmap;
+  if ((st = code_map(&kmap, view.k_codes, code_bytes, view.head_dim)) != QATTN_OK) return st;
+  if ((st = code_map(&vmap, view.v_codes, code_bytes, view.head_dim)) != QATTN_OK) return st;
+
+  DecodeArgs a;
+  a.q = q, a.seq_lens = seq_lens, a.out = out, a.lse = lse;
+  a.partial_o = static_cast<float *>(workspace);
+  const size_t o_bytes = static_cast<size_t>(p.splits) * rows * view.head_dim * sizeof(float);
+  a.partial_lse = need ? reinterpret_cast<float *>(static_cast<char *>(workspace) + (o_bytes + 255) / 256 * 256) : nullptr;
+  a.batch = batch, a.hq = num_q_heads, a.splits = p.splits, a.chunk = p.chunk;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_decode(a, view, kmap, vmap, ds->status, s);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  if (p.splits > 1) {
+    e = launch_combine(a.partial_o, a.partial_lse, p.splits, rows, view.head_dim, out, lse, true, s);
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+  }
+  return QATTN_OK;
+}
+
+qattn_status qattn_prefill(const uint16_t *q, const qattn_kv_cache *cache, int32_t batch,
+                           int32_t num_q_heads, int32_t nq, int32_t nk, float softmax_scale,
+                           int32_t causal, uint16_t *out, float *lse, qattn_stream_t stream) {
+  if (batch < 0 || num_q_heads <= 0 || nq < 0 || nk < 0 || (causal != 0 && causal != 1))
+    return fail(QATTN_ERR_INVALID_ARG, "batch %d, Hq %d, nq %d, nk %d, causal %d", batch, num_q_heads, nq, nk, causal);
+  KvView view;
+  uint64_t code_bytes = 0;
+  qattn_status st = check_cache(cache, batch, &view, &code_bytes);
+  if (st != QATTN_OK) return st;
+  if (view.page_table) return fail(QATTN_ERR_UNSUPPORTED, "prefill reads a contiguous cache only");
+  if (num_q_heads % view.hkv) return fail(QATTN_ERR_INVALID_ARG, "Hq %d is not a multiple of Hkv %d", num_q_heads, view.hkv);
+  if (nq > nk) return fail(QATTN_ERR_INVALID_ARG, "nq %d > nk %d", nq, nk);
+  if (nk > view.capacity) return fail(QATTN_ERR_INVALID_ARG, "nk %d > capacity %lld", nk, (long long)view.capacity);
+  if (batch == 0 || nq == 0) return QATTN_OK;
+  if (!q || !out) return fail(QATTN_ERR_INVALID_ARG, "q or out is NULL");
+  if (!aligned16(q) || !aligned16(out)) return fail(QATTN_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+  DeviceState *ds;
+  if ((st = device_state(&ds)) != QATTN_OK) return st;
+  CUtensorMap kmap, vmap;
+  if ((st = code_map(&kmap, view.k_codes, code_bytes, view.head_dim)) != QATTN_OK) return st;
+  if ((st = code_map(&vmap, view.v_codes, code_bytes, view.head_dim)) != QATTN_OK) return st;
+  PrefillArgs a;
+  a.q = q, a.out = out, a.lse = lse;
+  a.batch = batch, a.hq = num_q_heads, a.nq = nq, a.nk = nk, a.causal = causal;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  cudaError_t e = launch_prefill(a, view, kmap, vmap, ds->status, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "prefill launch");
+}
+
+qattn_status qattn_combine(const float *partial_o, const float *partial_lse, int32_t num_splits,
+                           int64_t rows, int32_t head_dim, uint16_t *out, float *lse,
+                           qattn_stream_t stream) {
+  if (num_splits < 1 || num_splits > QATTN_MAX_SPLITS)
+    return fail(QATTN_ERR_INVALID_ARG, "num_splits %d (1..%d)", num_splits, QATTN_MAX_SPLITS);
+  if (rows < 0 || rows > 0x7fffffffLL) return fail(QATTN_ERR_INVALID_ARG, "rows %lld", (long long)rows);
+  if (head_dim != 64 && head_dim != 128) return fail(QATTN_ERR_UNSUPPORTED, "head_dim %d", head_dim);
+  if (rows == 0) return QATTN_OK;
+  if (!partial_o || !partial_lse || !out) return fail(QATTN_ERR_INVALID_ARG, "NULL pointer");
+  if (!aligned16(partial_o) || !aligned16(out)) return fail(QATTN_ERR_INVALID_ARG, "partial_o and out must be 16-byte aligned");
+  cudaError_t e = launch_combine(partial_o, partial_lse, num_splits, rows, head_dim, out, lse, false,
+                                 reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "combine launch");
+}
+
+qattn_status qattn_read_device_flags(uint32_t *flags, int32_t clear) {
+  if (!flags) return fail(QATTN_ERR_INVALID_ARG, "flags is NULL");
+  DeviceState *ds;
+  qattn_status st = device_state(&ds);
+  if (st != QATTN_OK) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  e = cudaMemcpy(flags, ds->status, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && clear) e = cudaMemset(ds->status, 0, sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "status word");
+}
+
+const char *qattn_status_string(qattn_status status) {
+  switch (status) {
+    case QATTN_OK: return "ok";
+    case QATTN_ERR_INVALID_ARG: return "invalid argument";
+    case QATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case QATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case QATTN_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+const char *qattn_last_error(void) { return t_last_error; }
+
+int32_t qattn_version(void) { return 0x000100; }
+
+}  // extern "C"
