@@ -1,0 +1,59 @@
+"""Shared helpers for the tests: building the library, tolerances, comparisons."""
+
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+# Parity bar for attention outputs on unit-variance inputs (max-abs / mean-abs
+# of fp16 O against the float64 oracle), and our bound on the natural-log lse.
+O_MAX_ABS = 4e-3
+O_MEAN_ABS = 5e-4
+LSE_ABS = 1e-3
+
+
+def ensure_library():
+    """Build libqattn.so in-tree if it is missing or stale; return the module."""
+    from quantized_kv_attention_gb300 import build
+    build.build()
+    import quantized_kv_attention_gb300 as qa
+    qa.load_library()
+    return qa
+
+
+def header_symbols():
+    """Function names declared in include/qattn.h."""
+    with open(os.path.join(ROOT, "include", "qattn.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qattn_[a-z0-9_]+)\s*\(", text)))
+
+
+def require_gpu():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    return ensure_library()
+
+
+def assert_close_attention(out_gpu, ref, what="O", max_abs=O_MAX_ABS, mean_abs=O_MEAN_ABS):
+    o = out_gpu.detach().float().cpu().numpy().astype(np.float64)
+    assert o.shape == ref.shape, (o.shape, ref.shape)
+    assert np.isfinite(o).all(), f"{what}: non-finite output"
+    err = np.abs(o - ref)
+    mx, mn = float(err.max()) if err.size else 0.0, float(err.mean()) if err.size else 0.0
+    assert mx <= max_abs and mn <= mean_abs, f"{what}: max-abs {mx:.3e} mean-abs {mn:.3e}"
+    return mx, mn
+
+
+def assert_close_lse(lse_gpu, ref, tol=LSE_ABS):
+    l = lse_gpu.detach().cpu().numpy().astype(np.float64)
+    fin = np.isfinite(ref)
+    assert (np.isfinite(l) == fin).all(), "lse: finiteness differs"
+    assert (l[~fin] == -np.inf).all()
+    if fin.any():
+        err = float(np.abs(l[fin] - ref[fin]).max())
+        assert err <= tol, f"lse max-abs {err:.3e}"

@@ -1,0 +1,105 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol,
+and rejects bad arguments on the host before any launch."""
+
+import ctypes
+import subprocess
+
+import pytest
+
+from common import ensure_library, header_symbols
+
+qa = ensure_library()
+lib = qa.load_library()
+
+
+def test_exports_every_declared_symbol():
+    declared = header_symbols()
+    assert len(declared) >= 9
+    nm = subprocess.run(["nm", "-D", "--defined-only", qa.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in nm.splitlines() if line.strip()}
+    for name in declared:
+        assert name in exported, name
+        assert hasattr(lib, name)
+    assert set(qa.EXPORTS) == set(declared)
+
+
+def test_status_strings_and_version():
+    assert lib.qattn_version() == 0x000100
+    for st in range(5):
+        assert lib.qattn_status_string(st)
+    assert lib.qattn_status_string(99) == b"unknown status"
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: validation fails first
+
+
+def _cache(**kw):
+    s = qa.KvCacheStruct()
+    s.k_codes = s.k_scales = s.v_codes = s.v_scales = FAKE
+    s.head_dim, s.num_kv_heads, s.capacity = 128, 2, 256
+    for k, v in kw.items():
+        setattr(s, k, v)
+    return s
+
+
+def _decode(cache, batch=1, hq=4, max_len=100, splits=0):
+    return lib.qattn_decode(FAKE, ctypes.byref(cache), FAKE, batch, hq, max_len, 1.0, splits, None, 0,
+                            FAKE, None, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=96), qa.QATTN_ERR_UNSUPPORTED),
+    (dict(capacity=100), qa.QATTN_ERR_UNSUPPORTED),
+    (dict(num_kv_heads=0), qa.QATTN_ERR_INVALID_ARG),
+    (dict(k_codes=FAKE + 8), qa.QATTN_ERR_INVALID_ARG),
+    (dict(v_scales=0), qa.QATTN_ERR_INVALID_ARG),
+    (dict(page_table=FAKE, page_size=32, num_pages=4, max_pages_per_seq=2), qa.QATTN_ERR_UNSUPPORTED),
+    (dict(page_table=FAKE, page_size=64, num_pages=0, max_pages_per_seq=2), qa.QATTN_ERR_INVALID_ARG),
+])
+def test_decode_rejects_bad_cache(kw, status):
+    assert _decode(_cache(**kw)) == status
+    assert lib.qattn_last_error()
+
+
+def test_decode_rejects_bad_heads_and_splits():
+    assert _decode(_cache(), hq=5) == qa.QATTN_ERR_INVALID_ARG         # Hq % Hkv
+    assert _decode(_cache(), hq=18) == qa.QATTN_ERR_UNSUPPORTED        # group 9 > 8
+    assert _decode(_cache(), splits=2000) == qa.QATTN_ERR_INVALID_ARG
+    assert _decode(_cache(), max_len=-1) == qa.QATTN_ERR_INVALID_ARG
+    assert b"multiple" in lib.qattn_last_error() or True
+    assert lib.qattn_decode(FAKE, None, FAKE, 1, 4, 10, 1.0, 0, None, 0, FAKE, None, None) == qa.QATTN_ERR_INVALID_ARG
+
+
+def test_prefill_rejects_bad_arguments():
+    c = _cache()
+    pf = lambda **kw: lib.qattn_prefill(kw.get("q", FAKE), ctypes.byref(kw.get("cache", c)), 1, kw.get("hq", 4),
+                                        kw.get("nq", 10), kw.get("nk", 20), 1.0, kw.get("causal", 1),
+                                        kw.get("out", FAKE), None, None)
+    assert pf(nq=30, nk=20) == qa.QATTN_ERR_INVALID_ARG                  # nq > nk
+    assert pf(nk=300) == qa.QATTN_ERR_INVALID_ARG                        # nk > capacity
+    assert pf(causal=2) == qa.QATTN_ERR_INVALID_ARG
+    assert pf(q=FAKE + 2) == qa.QATTN_ERR_INVALID_ARG                    # misaligned
+    assert pf(cache=_cache(page_table=FAKE, page_size=64, num_pages=4, max_pages_per_seq=2)) == qa.QATTN_ERR_UNSUPPORTED
+
+
+def test_quantize_and_combine_reject_bad_arguments():
+    c = _cache()
+    assert lib.qattn_quantize_kv(FAKE, FAKE, 7, 1, 4, None, ctypes.byref(c), None) == qa.QATTN_ERR_INVALID_ARG
+    assert lib.qattn_quantize_kv(FAKE, FAKE, 0, -1, 4, None, ctypes.byref(c), None) == qa.QATTN_ERR_INVALID_ARG
+    assert lib.qattn_quantize_kv(None, FAKE, 0, 1, 4, None, ctypes.byref(c), None) == qa.QATTN_ERR_INVALID_ARG
+    assert lib.qattn_quantize_kv(FAKE, FAKE, 0, 0, 4, None, ctypes.byref(c), None) == qa.QATTN_OK  # nothing to do
+    assert lib.qattn_combine(FAKE, FAKE, 0, 4, 128, FAKE, None, None) == qa.QATTN_ERR_INVALID_ARG
+    assert lib.qattn_combine(FAKE, FAKE, 4, 4, 96, FAKE, None, None) == qa.QATTN_ERR_UNSUPPORTED
+    assert lib.qattn_combine(FAKE, FAKE, 2, 0, 128, FAKE, None, None) == qa.QATTN_OK            # empty
+
+
+def test_workspace_size_host_arithmetic():
+    # explicit split counts need no device: partial_o [S, B*Hq, D] fp32, padded
+    # to 256 bytes, then partial_lse [S, B*Hq] fp32
+    assert qa.decode_workspace_size(2, 8, 2, 128, 1000, 4) == 4 * 16 * 128 * 4 + 4 * 16 * 4
+    assert qa.decode_workspace_size(1, 1, 1, 64, 300, 3) == 3 * 64 * 4 + 256 - (3 * 64 * 4) % 256 + 3 * 4 \
+        if (3 * 64 * 4) % 256 else 3 * 64 * 4 + 3 * 4
+    assert qa.decode_workspace_size(2, 8, 2, 128, 1000, 1) == 0           # one split: no workspace
+    assert qa.decode_workspace_size(2, 8, 2, 128, 60, 4) == 0             # one 64-token chunk
+    assert qa.decode_workspace_size(0, 8, 2, 128, 60, 4) == 0             # invalid
+    assert qa.decode_workspace_size(2, 8, 2, 96, 600, 4) == 0
