@@ -195,3 +195,454 @@ def profiled_traffic(summary_file: str, digest: str, units: float):
     per = float(fields["dram_bytes_per_launch"])
     base = float(fields.get("units_per_launch", units) or units)
     return per * units / base
+
+
+# ----------------------------------------------------------- GPU workloads
+
+def _l2_bytes(torch, device):
+    try:
+        return int(torch.cuda.get_device_properties(device).L2_cache_size)
+    except Exception:
+        return 126 * 2**20
+
+
+def _fill_contiguous(qa, torch, cache, B, Hkv, N, D, seed, device, outliers=None, oscale=10.0):
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    for b in range(B):
+        sub = qa.KvCache(cache.k_codes[b:b + 1], cache.k_scales[b:b + 1], cache.v_codes[b:b + 1],
+                         cache.v_scales[b:b + 1], D, Hkv, capacity=cache.capacity)
+        k = torch.randn(1, Hkv, N, D, device=device, generator=g)
+        if outliers is not None:
+            for h in range(Hkv):
+                k[0, h, :, torch.as_tensor(outliers[h], device=device)] *= oscale
+        v = torch.randn(1, Hkv, N, D, device=device, generator=g)
+        qa.quantize_kv(k, v, sub)
+        del k, v
+
+
+def _graph(torch, fn):
+    """Capture fn() (public-API calls) into a CUDA graph after one eager run."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def _timed_loop(torch, steps, step_fn, inner_a, inner_b, gpu_index, soak_s=1.0):
+    """Run `steps` steps between a barrier + synchronize on both sides; record
+    CUDA events around the dominant kernel's launch (inner) on the stream."""
+    stride = max(1, steps // 4096)
+    pairs = []
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_index)
+    with sampler:
+        t0 = time.time()
+        i = 0
+        while time.time() - t0 < soak_s:          # same step loop, so the clock samples see load
+            step_fn(i, None)
+            i += 1
+            if i % 64 == 0:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        barrier()
+        torch.cuda.synchronize()
+        start.record()
+        for i in range(steps):
+            if i % stride == 0:
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                pairs.append((a, b))
+                step_fn(i, (a, b))
+            else:
+                step_fn(i, None)
+        end.record()
+        torch.cuda.synchronize()
+        barrier()
+    total_ms = start.elapsed_time(end)
+    inner_ms = statistics.mean(a.elapsed_time(b) for a, b in pairs) if pairs else None
+    return total_ms, inner_ms, sampler.summary()
+
+
+def run_decode(name, args, device, gpu_index, rank):
+    import torch
+    import quantized_kv_attention_gb300 as qa
+    from quantized_kv_attention_gb300 import workloads as wl
+    cfg = dict(wl.WORKLOADS[name])
+    B, Hq, Hkv, D = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"]
+    paged = cfg["kind"] == "paged"
+    seed = cfg["seed"] + 1000 * rank
+    splits = args.splits if args.splits >= 0 else (128 if name == "long_decode" else 0)
+    scale = 1.0 / math.sqrt(D)
+    torch.manual_seed(seed)
+    if paged:
+        lens, table, P = wl.paged_layout(cfg["seed"], B, cfg["len_lo"], cfg["len_hi"], cfg["page"])
+        max_len = int(cfg["len_hi"])
+        kv_bytes = int(lens.sum()) * Hkv * (D + 4)
+    else:
+        Nk = cfg["Nk"]
+        lens = [Nk] * B
+        max_len = Nk
+        kv_bytes = B * Hkv * Nk * (D + 4)
+    copies = max(1, math.ceil(4 * _l2_bytes(torch, device) / kv_bytes))
+    caches = []
+    for r in range(copies):
+        if paged:
+            c = qa.KvCache.paged(P, Hkv, D, torch.from_numpy(table), device=device)
+            g = torch.Generator(device=device)
+            g.manual_seed(seed * 31 + r)
+            for b, n in enumerate(lens):
+                sub = qa.KvCache(c.k_codes, c.k_scales, c.v_codes, c.v_scales, D, Hkv,
+                                 page_table=c.page_table[b:b + 1], num_pages=P)
+                k = torch.randn(1, Hkv, int(n), D, device=device, generator=g)
+                v = torch.randn(1, Hkv, int(n), D, device=device, generator=g)
+                qa.quantize_kv(k, v, sub)
+        else:
+            c = qa.KvCache.contiguous(B, Hkv, Nk, D, device=device)
+            oc = wl.outlier_channels(cfg["seed"], Hkv, D, cfg["outliers"]) if cfg.get("outliers") else None
+            _fill_contiguous(qa, torch, c, B, Hkv, Nk, D, seed * 31 + r, device, oc, cfg.get("outlier_scale", 1.0))
+        caches.append(c)
+    torch.cuda.synchronize()
+    sl = torch.tensor([int(x) for x in lens], dtype=torch.int32, device=device)
+    start_pos = (sl - 1).clamp(min=0)
+    q = torch.randn(B, Hq, D, device=device).half()
+    new_k = torch.randn(B, Hkv, 1, D, device=device)
+    new_v = torch.randn(B, Hkv, 1, D, device=device)
+    out = torch.empty(B, Hq, D, dtype=torch.float16, device=device)
+    ws_bytes = qa.decode_workspace_size(B, Hq, Hkv, D, max_len, splits)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
+    launches = 2 + (1 if ws_bytes > 0 else 0)
+
+    def append(r):
+        qa.quantize_kv(new_k, new_v, caches[r], start_pos)
+
+    def attend(r):
+        qa.decode(q, caches[r], sl, max_len, scale, splits, workspace=ws, out=out)
+
+    ga = [_graph(torch, lambda r=r: append(r)) for r in range(copies)]
+    gd = [_graph(torch, lambda r=r: attend(r)) for r in range(copies)]
+    for i in range(args.warmup):
+        ga[i % copies].replay()
+        gd[i % copies].replay()
+    torch.cuda.synchronize()
+
+    def step(i, ev):
+        r = i % copies
+        ga[r].replay()
+        if ev is not None:
+            ev[0].record()
+        gd[r].replay()
+        if ev is not None:
+            ev[1].record()
+
+    total_ms, dec_ms, clocks = _timed_loop(torch, args.steps, step, None, None, gpu_index)
+    value, tmax, world = aggregate(kv_bytes * args.steps / 1e9, total_ms / 1e3, device)
+
+    # e2e: eager public-API calls with pinned host inputs copied in and the
+    # output copied out every step
+    q_h = q.cpu().pin_memory()
+    k_h, v_h = new_k.cpu().pin_memory(), new_v.cpu().pin_memory()
+    out_h = torch.empty(B, Hq, D, dtype=torch.float16).pin_memory()
+    q_d, k_d, v_d = torch.empty_like(q), torch.empty_like(new_k), torch.empty_like(new_v)
+
+    def e2e_step(i):
+        r = i % copies
+        q_d.copy_(q_h, non_blocking=True)
+        k_d.copy_(k_h, non_blocking=True)
+        v_d.copy_(v_h, non_blocking=True)
+        qa.quantize_kv(k_d, v_d, caches[r], start_pos)
+        qa.decode(q_d, caches[r], sl, max_len, scale, splits, workspace=ws, out=out)
+        out_h.copy_(out, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.e2e_steps):
+        e2e_step(i)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_val, _, _ = aggregate(kv_bytes * args.e2e_steps / 1e9, e0.elapsed_time(e1) / 1e3, device)
+    h2d = q.numel() * 2 + new_k.numel() * 4 + new_v.numel() * 4
+    d2h = out.numel() * 2
+
+    peaks, pk_src = measured_peaks()
+    achieved = kv_bytes / (dec_ms / 1e3) / 1e9
+    traffic = profiled_traffic(f"decode_{name}_ncu.txt", source_digest("decode.cu", "ptx.cuh", "combine.cu"),
+                               kv_bytes)
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tmax * 1e3 / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "D": D, "max_seq_len": max_len,
+                   "paged": paged, "splits": "auto" if splits == 0 else splits,
+                   "kv_bytes_per_step": kv_bytes,
+                   "l2": f"rotating {copies} cache copies ({copies * kv_bytes / 2**20:.0f} MiB > 4x L2)",
+                   "softmax_scale": scale, "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": traffic, "kernel": "decode+combine (one qattn_decode call)",
+                     "peak_source": pk_src, "us_per_launch": round(dec_ms * 1e3, 3)},
+        "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
+        "gpu_launches": launches * args.steps,
+        "clocks": clocks,
+    }
+    del caches
+    torch.cuda.empty_cache()
+    return res
+
+
+def prefill_flops(B, Hq, Nq, Nk, D, causal=True):
+    """4 * D flops per visible (query, key) pair (QK^T and PV)."""
+    if causal:
+        shift = Nk - Nq
+        pairs = sum(min(Nk, i + shift + 1) for i in range(Nq))
+    else:
+        pairs = Nq * Nk
+    return 4.0 * D * B * Hq * pairs
+
+
+def run_prefill(name, args, device, gpu_index, rank, steps=None):
+    import torch
+    import quantized_kv_attention_gb300 as qa
+    from quantized_kv_attention_gb300 import workloads as wl
+    cfg = dict(wl.WORKLOADS[name])
+    B, Hq, Hkv, D, Nq, Nk = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["Nq"], cfg["Nk"]
+    steps = steps or args.steps
+    scale = 1.0 / math.sqrt(D)
+    g = torch.Generator(device=device)
+    g.manual_seed(cfg["seed"] + 1000 * rank)
+    k = torch.randn(B, Hkv, Nk, D, device=device, generator=g)
+    v = torch.randn(B, Hkv, Nk, D, device=device, generator=g)
+    q = torch.randn(B, Hq, Nq, D, device=device, generator=g).half()
+    out = torch.empty_like(q)
+    cache = qa.KvCache.contiguous(B, Hkv, Nk, D, device=device)
+    flops = prefill_flops(B, Hq, Nq, Nk, D, True)
+
+    ga = _graph(torch, lambda: qa.quantize_kv(k, v, cache))
+    gp = _graph(torch, lambda: qa.prefill(q, cache, Nk, scale, True, out=out))
+    for _ in range(args.warmup):
+        ga.replay()
+        gp.replay()
+    torch.cuda.synchronize()
+
+    def step(i, ev):
+        ga.replay()
+        if ev is not None:
+            ev[0].record()
+        gp.replay()
+        if ev is not None:
+            ev[1].record()
+
+    total_ms, pf_ms, clocks = _timed_loop(torch, steps, step, None, None, gpu_index)
+    value, tmax, world = aggregate(flops * steps / 1e12, total_ms / 1e3, device)
+
+    # e2e through the public API with pinned host buffers
+    q_h, k_h, v_h = q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory()
+    out_h = torch.empty(q.shape, dtype=torch.float16).pin_memory()
+    e2e_steps = max(3, min(args.e2e_steps, 10))
+
+    def e2e_step():
+        q.copy_(q_h, non_blocking=True)
+        k.copy_(k_h, non_blocking=True)
+        v.copy_(v_h, non_blocking=True)
+        qa.quantize_kv(k, v, cache)
+        qa.prefill(q, cache, Nk, scale, True, out=out)
+        out_h.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_val, _, _ = aggregate(flops * e2e_steps / 1e12, e0.elapsed_time(e1) / 1e3, device)
+
+    peaks, pk_src = measured_peaks()
+    achieved = flops / (pf_ms / 1e3) / 1e12
+    peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    traffic = profiled_traffic(f"prefill_{name}_ncu.txt", source_digest("prefill.cu", "ptx.cuh"), flops)
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(tmax * 1e3 / steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "D": D, "Nq": Nq, "Nk": Nk,
+                   "causal": True, "flops_per_step": flops, "softmax_scale": scale,
+                   "l2": "Q and O (134 MB each) exceed L2 every step",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "prefill", "peak_source": pk_src + " bf16 sustained (fp16 runs at the bf16 rate)",
+                     "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4),
+                     "ms_per_launch": round(pf_ms, 4)},
+        "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": q.numel() * 2 + k.numel() * 4 + v.numel() * 4,
+                "d2h_bytes_per_step": out.numel() * 2, "steps": e2e_steps},
+        "gpu_launches": 2 * steps,
+        "clocks": clocks,
+    }
+    del k, v, q, out, cache
+    torch.cuda.empty_cache()
+    return res
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def _cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_step_factory(name, units=None):
+    """An oracle step over a bounded sample of `name`; returns (step_fn,
+    units of the metric per step, unit, description)."""
+    import numpy as np
+    from oracle import attention as att
+    from oracle import codec
+    from quantized_kv_attention_gb300 import workloads as wl
+    cfg = dict(wl.WORKLOADS[name])
+    D, Hq, Hkv = cfg["D"], cfg["Hq"], cfg["Hkv"]
+    G = Hq // Hkv
+    scale = 1.0 / math.sqrt(D)
+    if cfg["kind"] == "prefill":
+        Nq, Nk = cfg["Nq"], cfg["Nk"]
+        rows = units or 256
+        k = wl.kv_slice(cfg["seed"], "k", 0, 0, Nk, D).numpy()[None, None]
+        v = wl.kv_slice(cfg["seed"], "v", 0, 0, Nk, D).numpy()[None, None]
+        q = wl.queries(cfg["seed"], 1, 1, Nq, D).numpy()[:, :, Nq - rows:]
+        flops = prefill_flops(1, 1, rows, Nk, D, True)
+
+        def step():
+            pk, sk = codec.quantize_pack(k)
+            pv, sv = codec.quantize_pack(v)
+            att.attention_quantized(q, pk, sk, pv, sv, scale, True)
+        desc = f"one head, the last {rows} causal query rows of Nq=Nk={Nk} (append of that head's K/V included)"
+        return step, flops / 1e12, "TFLOP/s", desc
+    if cfg["kind"] == "paged":
+        lens, _, _ = wl.paged_layout(cfg["seed"], cfg["B"], cfg["len_lo"], cfg["len_hi"], cfg["page"])
+        N = int(lens[0])
+    else:
+        N = cfg["Nk"]
+    heads = units or Hkv
+    oc = wl.outlier_channels(cfg["seed"], Hkv, D, cfg["outliers"]) if cfg.get("outliers") else None
+    k = np.stack([wl.kv_slice(cfg["seed"], "k", 0, h, N, D, oc, cfg.get("outlier_scale", 1.0)).numpy()
+                  for h in range(heads)])[None]
+    v = np.stack([wl.kv_slice(cfg["seed"], "v", 0, h, N, D).numpy() for h in range(heads)])[None]
+    pk, sk = codec.quantize_pack(k)
+    pv, sv = codec.quantize_pack(v)
+    q = wl.queries(cfg["seed"], 1, heads * G, D).numpy()[:, :, None]
+    new = k[:, :, -1:].copy()
+
+    def step():
+        codec.quantize_pack(new)
+        codec.quantize_pack(new)
+        att.attention_quantized(q, pk, sk, pv, sv, scale)
+    desc = f"sequence 0, {heads} of {Hkv} kv-heads x {N} tokens (append of one row + decode)"
+    return step, heads * N * (D + 4) / 1e9, "GB/s", desc
+
+
+def cpu_baseline(name, budget_s):
+    step, units, unit, desc = oracle_step_factory(name)
+    step()
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        step()
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(units * n / dt, 4), "unit": unit, "cores": _cores(), "kind": "oracle",
+            "sample": f"{desc}; {n} steps in {dt:.1f} s; numpy float64, BLAS threads = all cores"}
+
+
+def run_reference(args):
+    """The float64 oracle on the host cores, as the reference arm."""
+    name = args.workload
+    kind_prefill = name == "causal_prefill"
+    budget = min(2.0, 150.0 / max(1, args.steps + args.warmup))   # seconds per step
+    probe, _, _, _ = oracle_step_factory(name, units=1 if not kind_prefill else 64)
+    t0 = time.perf_counter()
+    probe()
+    t1 = time.perf_counter() - t0
+    base = 64 if kind_prefill else 1
+    units = max(base, min((8192 if kind_prefill else 8), int(base * budget / max(t1, 1e-6))))
+    if kind_prefill:
+        units = max(64, units // 64 * 64)
+    step, per_step, unit, desc = oracle_step_factory(name, units=units)
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = per_step * args.steps / dt
+    return {"metric": METRIC, "value": round(value, 4), "unit": unit, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": name},
+            "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": _cores(), "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def compact(res):
+    keep = ("value", "unit", "ms_per_step", "steps", "config", "roofline", "e2e", "clocks")
+    return {k: res[k] for k in keep if k in res}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return 0
+    import torch
+    from quantized_kv_attention_gb300 import build as qbuild
+    from quantized_kv_attention_gb300 import workloads as wl
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    rank, world = dist_init("nccl")
+    if rank == 0:
+        qbuild.build()
+    barrier()
+    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
+        if os.environ.get("CUDA_VISIBLE_DEVICES") else local
+    kind = wl.WORKLOADS[args.workload]["kind"]
+    runner = run_prefill if kind == "prefill" else run_decode
+    res = runner(args.workload, args, device, gpu_index, rank)
+    if args.secondary and world == 1 and args.workload == "gqa_decode":
+        res["secondary"] = {
+            "long_decode": compact(run_decode("long_decode", args, device, gpu_index, rank)),
+            "causal_prefill": compact(run_prefill("causal_prefill", args, device, gpu_index, rank,
+                                                  steps=min(args.steps, 50))),
+        }
+    if rank == 0 and world == 1:
+        res["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    import torch.distributed as dist
+    if dist.is_initialized():
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
