@@ -210,6 +210,32 @@ qattn_status qattn_combine(const float *partial_o, const float *partial_lse, int
  */
 qattn_status qattn_read_device_flags(uint32_t *flags, int32_t clear);
 
+/* Bytes of the library-owned scratch behind qattn_decode_noalloc (8 MiB per device). */
+#define QATTN_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+/*
+ * qattn_decode_noalloc -- qattn_decode without a workspace argument, for
+ * callers that cannot allocate device memory (for example a plugin that is
+ * handed only its input and output buffers, or code on a device whose memory
+ * a caching allocator has already reserved).  The source pages have no
+ * counterpart; this is a convenience of the library.
+ *
+ * Same arguments and results as qattn_decode, except that the split partials
+ * live in a fixed device array owned by the library
+ * (QATTN_NOALLOC_SCRATCH_BYTES on every GPU that loads it, kept until exit).
+ *   - Sizes whose partials exceed that array are refused with
+ *     QATTN_ERR_UNSUPPORTED before any work (use fewer splits, or qattn_decode).
+ *   - The first call on a device, with that device current, looks up the
+ *     array's address (cudaGetSymbolAddress); make it before any stream capture.
+ *   - All calls on a device share the array: calls that overlap on the GPU
+ *     race.  Nothing in it needs clearing between calls.
+ *   - The call allocates nothing.
+ */
+qattn_status qattn_decode_noalloc(const uint16_t *q, const qattn_kv_cache *cache,
+                                  const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                                  int32_t max_seq_len, float softmax_scale, int32_t num_splits,
+                                  uint16_t *out, float *lse, qattn_stream_t stream);
+
 /* Static description of a status code (never NULL). */
 const char *qattn_status_string(qattn_status status);
 

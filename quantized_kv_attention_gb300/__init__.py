@@ -36,7 +36,7 @@ FLAG_WAIT_TIMEOUT, FLAG_BAD_PAGE, FLAG_TMEM = 1, 2, 4
 EXPORTS = (
     "qattn_quantize_kv", "qattn_decode_workspace_size", "qattn_decode", "qattn_prefill",
     "qattn_combine", "qattn_read_device_flags", "qattn_status_string", "qattn_last_error",
-    "qattn_version",
+    "qattn_version", "qattn_decode_noalloc",
 )
 
 
@@ -88,6 +88,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qattn_status_string": (ctypes.c_char_p, [i32]),
         "qattn_last_error": (ctypes.c_char_p, []),
         "qattn_version": (i32, []),
+        "qattn_decode_noalloc": (i32, [vp, cache_p, vp, i32, i32, i32, f32, i32, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

@@ -160,6 +160,11 @@ size_t workspace_bytes(int splits, int64_t rows, int head_dim) {
 }
 
 }  // namespace
+
+// Lets other translation units of the library report a failure through
+// qattn_last_error().
+void record_error(const char *msg) { snprintf(t_last_error, sizeof(t_last_error), "%s", msg); }
+
 }  // namespace qattn
 
 using namespace qattn;

@@ -60,4 +60,7 @@ struct PrefillArgs {
 cudaError_t launch_prefill(const PrefillArgs &a, const KvView &cache, const CUtensorMap &kmap,
                            const CUtensorMap &vmap, uint32_t *err, cudaStream_t stream);
 
+// api.cu: sets the message returned by qattn_last_error() on this thread.
+void record_error(const char *msg);
+
 }  // namespace qattn
