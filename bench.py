@@ -50,6 +50,7 @@ def parse_args(argv=None):
     p.add_argument("--secondary", type=int, default=1, help="also time long_decode and causal_prefill")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU budget of the oracle baseline")
     p.add_argument("--e2e-steps", type=int, default=50)
+    p.add_argument("--soak", type=float, default=1.0, help="seconds of the step loop before timing (clock samples)")
     return p.parse_args(argv)
 
 
@@ -234,38 +235,78 @@ def _graph(torch, fn):
     return g
 
 
-def _timed_loop(torch, steps, step_fn, inner_a, inner_b, gpu_index, soak_s=1.0):
-    """Run `steps` steps between a barrier + synchronize on both sides; record
-    CUDA events around the dominant kernel's launch (inner) on the stream."""
-    stride = max(1, steps // 4096)
-    pairs = []
+def _timed_graphs(torch, steps, enqueue_steps, enqueue_inner, inner_count, gpu_index,
+                  period=1, soak_s=1.0, chunk=256):
+    """Time exactly `steps` steps, replayed from CUDA graphs of the public-API
+    calls (so the host never starves the GPU), between a barrier and a
+    synchronize on both sides, with CUDA events on the launching stream.
+
+    enqueue_steps(n) enqueues n consecutive steps starting from rotation slot
+    0 (period = rotation length); enqueue_inner(n) enqueues n back-to-back
+    launches of the dominant kernel alone, timed the same way to give its mean
+    launch duration.  Clocks are sampled over a soak of the same graphs right
+    before the timed region and over the region itself."""
+    S = min(steps, max(period, chunk // period * period))
+    g_main = _graph(torch, lambda: enqueue_steps(S))
+    rem = steps % S
+    g_rem = _graph(torch, lambda: enqueue_steps(rem)) if rem else None
+    g_inner = _graph(torch, lambda: enqueue_inner(inner_count))
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    i0, i1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(gpu_index)
     with sampler:
         t0 = time.time()
-        i = 0
-        while time.time() - t0 < soak_s:          # same step loop, so the clock samples see load
-            step_fn(i, None)
-            i += 1
-            if i % 64 == 0:
-                torch.cuda.synchronize()
-        torch.cuda.synchronize()
+        while time.time() - t0 < soak_s:
+            g_main.replay()
+            torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()
         start.record()
-        for i in range(steps):
-            if i % stride == 0:
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                pairs.append((a, b))
-                step_fn(i, (a, b))
-            else:
-                step_fn(i, None)
+        for _ in range(steps // S):
+            g_main.replay()
+        if g_rem is not None:
+            g_rem.replay()
         end.record()
         torch.cuda.synchronize()
         barrier()
-    total_ms = start.elapsed_time(end)
-    inner_ms = statistics.mean(a.elapsed_time(b) for a, b in pairs) if pairs else None
-    return total_ms, inner_ms, sampler.summary()
+        reps = max(1, int(math.ceil(2 * steps / max(1, inner_count))))
+        g_inner.replay()
+        torch.cuda.synchronize()
+        i0.record()
+        for _ in range(reps):
+            g_inner.replay()
+        i1.record()
+        torch.cuda.synchronize()
+    return start.elapsed_time(end), i0.elapsed_time(i1) / (reps * inner_count), sampler.summary()
+
+
+def workload_config(name, splits=None):
+    """The `config` object both arms print for a workload."""
+    from quantized_kv_attention_gb300 import workloads as wl
+    cfg = dict(wl.WORKLOADS[name])
+    D = cfg["D"]
+    out = {"workload": name}
+    for key in ("B", "Hq", "Hkv", "D", "Nq", "Nk", "len_lo", "len_hi", "page", "outliers", "seed"):
+        if key in cfg:
+            out[key] = cfg[key]
+    out["softmax_scale"] = 1.0 / math.sqrt(D)
+    if cfg["kind"] == "prefill":
+        out["causal"] = True
+        out["flops_per_step"] = prefill_flops(cfg["B"], cfg["Hq"], cfg["Nq"], cfg["Nk"], D, True)
+        out["l2"] = "inputs larger than L2: Q and O are 134 MB each per step"
+    else:
+        if splits is None:
+            splits = 128 if name == "long_decode" else 0
+        out["splits"] = "auto" if splits == 0 else splits
+        out["l2"] = "rotating KV-cache copies totalling more than 4x L2"
+        if cfg["kind"] == "paged":
+            lens, _, _ = wl.paged_layout(cfg["seed"], cfg["B"], cfg["len_lo"], cfg["len_hi"], cfg["page"])
+            out["kv_bytes_per_step"] = int(lens.sum()) * cfg["Hkv"] * (D + 4)
+        else:
+            out["kv_bytes_per_step"] = cfg["B"] * cfg["Hkv"] * cfg["Nk"] * (D + 4)
+    out["step"] = ("append all K/V rows (quantize) + causal prefill" if cfg["kind"] == "prefill"
+                   else "append one K/V row per sequence (quantize) + split-KV decode + combine")
+    return out
 
 
 def run_decode(name, args, device, gpu_index, rank):
@@ -323,23 +364,20 @@ def run_decode(name, args, device, gpu_index, rank):
     def attend(r):
         qa.decode(q, caches[r], sl, max_len, scale, splits, workspace=ws, out=out)
 
-    ga = [_graph(torch, lambda r=r: append(r)) for r in range(copies)]
-    gd = [_graph(torch, lambda r=r: attend(r)) for r in range(copies)]
-    for i in range(args.warmup):
-        ga[i % copies].replay()
-        gd[i % copies].replay()
+    def enqueue_steps(n):
+        for i in range(n):
+            append(i % copies)
+            attend(i % copies)
+
+    def enqueue_inner(n):
+        for i in range(n):
+            attend(i % copies)
+
+    enqueue_steps(max(args.warmup, 1))
     torch.cuda.synchronize()
-
-    def step(i, ev):
-        r = i % copies
-        ga[r].replay()
-        if ev is not None:
-            ev[0].record()
-        gd[r].replay()
-        if ev is not None:
-            ev[1].record()
-
-    total_ms, dec_ms, clocks = _timed_loop(torch, args.steps, step, None, None, gpu_index)
+    inner_count = max(copies, 64 // copies * copies)
+    total_ms, dec_ms, clocks = _timed_graphs(torch, args.steps, enqueue_steps, enqueue_inner, inner_count,
+                                             gpu_index, period=copies, soak_s=args.soak)
     value, tmax, world = aggregate(kv_bytes * args.steps / 1e9, total_ms / 1e3, device)
 
     # e2e: eager public-API calls with pinned host inputs copied in and the
@@ -358,17 +396,20 @@ def run_decode(name, args, device, gpu_index, rank):
         qa.decode(q_d, caches[r], sl, max_len, scale, splits, workspace=ws, out=out)
         out_h.copy_(out, non_blocking=True)
 
-    for i in range(3):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(args.e2e_steps):
-        e2e_step(i)
-    e1.record()
-    torch.cuda.synchronize()
-    e2e_val, _, _ = aggregate(kv_bytes * args.e2e_steps / 1e9, e0.elapsed_time(e1) / 1e3, device)
+    e2e_val = None
+    if args.e2e_steps > 0:
+        for i in range(3):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(args.e2e_steps):
+            e2e_step(i)
+        e1.record()
+        torch.cuda.synchronize()
+        e2e_val, _, _ = aggregate(kv_bytes * args.e2e_steps / 1e9, e0.elapsed_time(e1) / 1e3, device)
+        e2e_val = round(e2e_val, 2)
     h2d = q.numel() * 2 + new_k.numel() * 4 + new_v.numel() * 4
     d2h = out.numel() * 2
 
@@ -381,16 +422,14 @@ def run_decode(name, args, device, gpu_index, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tmax * 1e3 / args.steps, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic",
-        "config": {"workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "D": D, "max_seq_len": max_len,
-                   "paged": paged, "splits": "auto" if splits == 0 else splits,
-                   "kv_bytes_per_step": kv_bytes,
-                   "l2": f"rotating {copies} cache copies ({copies * kv_bytes / 2**20:.0f} MiB > 4x L2)",
-                   "softmax_scale": scale, "parallelism": f"replicas x{world}"},
+        "config": workload_config(name, splits),
+        "setup": {"cache_copies": copies, "rotation_mib": round(copies * kv_bytes / 2**20),
+                  "parallelism": f"replicas x{world}", "timing": "CUDA graphs of the API calls"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "traffic": traffic, "kernel": "decode+combine (one qattn_decode call)",
                      "peak_source": pk_src, "us_per_launch": round(dec_ms * 1e3, 3)},
-        "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
         "gpu_launches": launches * args.steps,
         "clocks": clocks,
@@ -427,28 +466,25 @@ def run_prefill(name, args, device, gpu_index, rank, steps=None):
     cache = qa.KvCache.contiguous(B, Hkv, Nk, D, device=device)
     flops = prefill_flops(B, Hq, Nq, Nk, D, True)
 
-    ga = _graph(torch, lambda: qa.quantize_kv(k, v, cache))
-    gp = _graph(torch, lambda: qa.prefill(q, cache, Nk, scale, True, out=out))
-    for _ in range(args.warmup):
-        ga.replay()
-        gp.replay()
+    def enqueue_steps(n):
+        for _ in range(n):
+            qa.quantize_kv(k, v, cache)
+            qa.prefill(q, cache, Nk, scale, True, out=out)
+
+    def enqueue_inner(n):
+        for _ in range(n):
+            qa.prefill(q, cache, Nk, scale, True, out=out)
+
+    enqueue_steps(max(args.warmup, 1))
     torch.cuda.synchronize()
-
-    def step(i, ev):
-        ga.replay()
-        if ev is not None:
-            ev[0].record()
-        gp.replay()
-        if ev is not None:
-            ev[1].record()
-
-    total_ms, pf_ms, clocks = _timed_loop(torch, steps, step, None, None, gpu_index)
+    total_ms, pf_ms, clocks = _timed_graphs(torch, steps, enqueue_steps, enqueue_inner, 2, gpu_index,
+                                            chunk=8, soak_s=args.soak)
     value, tmax, world = aggregate(flops * steps / 1e12, total_ms / 1e3, device)
 
     # e2e through the public API with pinned host buffers
     q_h, k_h, v_h = q.cpu().pin_memory(), k.cpu().pin_memory(), v.cpu().pin_memory()
     out_h = torch.empty(q.shape, dtype=torch.float16).pin_memory()
-    e2e_steps = max(3, min(args.e2e_steps, 10))
+    e2e_steps = min(args.e2e_steps, 10)
 
     def e2e_step():
         q.copy_(q_h, non_blocking=True)
@@ -458,16 +494,19 @@ def run_prefill(name, args, device, gpu_index, rank, steps=None):
         qa.prefill(q, cache, Nk, scale, True, out=out)
         out_h.copy_(out, non_blocking=True)
 
-    e2e_step()
-    torch.cuda.synchronize()
-    barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(e2e_steps):
+    e2e_val = None
+    if e2e_steps > 0:
         e2e_step()
-    e1.record()
-    torch.cuda.synchronize()
-    e2e_val, _, _ = aggregate(flops * e2e_steps / 1e12, e0.elapsed_time(e1) / 1e3, device)
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record()
+        torch.cuda.synchronize()
+        e2e_val, _, _ = aggregate(flops * e2e_steps / 1e12, e0.elapsed_time(e1) / 1e3, device)
+        e2e_val = round(e2e_val, 2)
 
     peaks, pk_src = measured_peaks()
     achieved = flops / (pf_ms / 1e3) / 1e12
@@ -478,16 +517,14 @@ def run_prefill(name, args, device, gpu_index, rank, steps=None):
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(tmax * 1e3 / steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic",
-        "config": {"workload": name, "B": B, "Hq": Hq, "Hkv": Hkv, "D": D, "Nq": Nq, "Nk": Nk,
-                   "causal": True, "flops_per_step": flops, "softmax_scale": scale,
-                   "l2": "Q and O (134 MB each) exceed L2 every step",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(name),
+        "setup": {"parallelism": f"replicas x{world}", "timing": "CUDA graphs of the API calls"},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "prefill", "peak_source": pk_src + " bf16 sustained (fp16 runs at the bf16 rate)",
                      "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4),
                      "ms_per_launch": round(pf_ms, 4)},
-        "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s",
+        "e2e": {"value": e2e_val, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": q.numel() * 2 + k.numel() * 4 + v.numel() * 4,
                 "d2h_bytes_per_step": out.numel() * 2, "steps": e2e_steps},
         "gpu_launches": 2 * steps,
@@ -595,7 +632,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": name},
+            "config": workload_config(name, None if args.splits < 0 else args.splits),
             "cpu_baseline": {"value": round(value, 4), "unit": unit, "cores": _cores(), "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -603,7 +640,7 @@ def run_reference(args):
 
 
 def compact(res):
-    keep = ("value", "unit", "ms_per_step", "steps", "config", "roofline", "e2e", "clocks")
+    keep = ("value", "unit", "ms_per_step", "steps", "config", "setup", "roofline", "e2e", "clocks")
     return {k: res[k] for k in keep if k in res}
 
 
@@ -634,7 +671,7 @@ def main(argv=None):
             "causal_prefill": compact(run_prefill("causal_prefill", args, device, gpu_index, rank,
                                                   steps=min(args.steps, 50))),
         }
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
         res["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
     if rank == 0:
         print(json.dumps(res), flush=True)
