@@ -89,6 +89,7 @@ typedef enum qattn_dtype {
 #define QATTN_PAGE_SIZE 64     /* tokens per page of a paged cache */
 #define QATTN_MAX_GROUP 8      /* largest Hq / Hkv */
 #define QATTN_MAX_SPLITS 1024  /* largest num_splits of qattn_decode */
+#define QATTN_MAX_BATCH 2048   /* largest batch of qattn_decode */
 
 /* Bits of the device status word (qattn_read_device_flags). */
 #define QATTN_FLAG_WAIT_TIMEOUT 1u /* a pipeline wait gave up (kernel returned early) */
@@ -142,7 +143,7 @@ qattn_status qattn_quantize_kv(const void *k, const void *v, qattn_dtype x_dtype
 
 /*
  * qattn_decode_workspace_size -- bytes of workspace qattn_decode needs for
- * `num_splits` key chunks (0 = the automatic choice for these sizes on the
+ * `num_splits` key ranges (0 = the automatic choice for these sizes on the
  * current device).  Host-only; returns 0 for invalid sizes.
  */
 size_t qattn_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
@@ -159,11 +160,14 @@ size_t qattn_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t n
  *                clamped and flagged QATTN_FLAG_BAD_PAGE
  *   max_seq_len  host int, an upper bound of seq_lens used to size the split
  *   softmax_scale multiplies Q K^T
- *   num_splits   key chunks per sequence (split-KV); 0 = automatic.  With
- *                more than one chunk, partial results go to the workspace and
- *                are merged by the log-sum-exp combine inside this call.
+ *   num_splits   number of balanced key ranges the whole batch is cut into
+ *                (split-KV; one persistent CTA per range); 0 = one per SM.
+ *                Every range holds the same number of 64-token stages, so
+ *                ranges cut sequences wherever needed; a (sequence, kv-head)
+ *                cut by ranges leaves one fp32 partial per range, merged by
+ *                the log-sum-exp combine inside this call.
  *   workspace    device scratch of at least qattn_decode_workspace_size()
- *                bytes for the same arguments (may be NULL if that is 0)
+ *                bytes for the same arguments (two partial slots per range)
  *   out          [batch, Hq, D] fp16
  *   lse          [batch, Hq] fp32, or NULL
  */

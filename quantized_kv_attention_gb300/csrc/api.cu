@@ -132,31 +132,21 @@ qattn_status check_cache(const qattn_kv_cache *c, int batch, KvView *v, uint64_t
   return QATTN_OK;
 }
 
-struct SplitPlan {
-  int splits, chunk;
-};
-
-SplitPlan plan_splits(int batch, int hkv, int max_len, int requested, int sms) {
-  const int max_chunks = max_len > 0 ? (max_len + kPage - 1) / kPage : 1;
-  int s = requested;
-  if (s <= 0) {  // about four CTAs per SM in one wave
-    const int units = batch * hkv > 0 ? batch * hkv : 1;
-    s = (4 * sms + units - 1) / units;
-  }
-  if (s > max_chunks) s = max_chunks;
-  if (s > QATTN_MAX_SPLITS) s = QATTN_MAX_SPLITS;
-  if (s < 1) s = 1;
-  int chunk = max_len > 0 ? (max_len + s - 1) / s : kPage;
-  chunk = (chunk + kPage - 1) / kPage * kPage;
-  s = max_len > 0 ? (max_len + chunk - 1) / chunk : 1;
-  return {s, chunk};
+// Number of balanced key ranges (one persistent CTA each) for a decode call:
+// one per SM by default, never more than there are 64-token stages.
+int plan_ctas(int batch, int hkv, int max_len, int requested, int sms) {
+  const int64_t stages = static_cast<int64_t>(batch) * hkv * ((static_cast<int64_t>(max_len) + kPage - 1) / kPage);
+  int64_t n = requested > 0 ? requested : sms;
+  if (n > stages) n = stages;
+  if (n > QATTN_MAX_SPLITS) n = QATTN_MAX_SPLITS;
+  if (n < 1) n = 1;
+  return static_cast<int>(n);
 }
 
-size_t workspace_bytes(int splits, int64_t rows, int head_dim) {
-  if (splits <= 1) return 0;
-  const size_t o = static_cast<size_t>(splits) * rows * head_dim * sizeof(float);
-  const size_t o_al = (o + 255) / 256 * 256;
-  return o_al + static_cast<size_t>(splits) * rows * sizeof(float);
+// partial_o [2*ctas, G, D] fp32, padded to 256 bytes, then partial_lse [2*ctas, G].
+size_t workspace_bytes(int ctas, int group, int head_dim) {
+  const size_t o = static_cast<size_t>(2) * ctas * group * head_dim * sizeof(float);
+  return (o + 255) / 256 * 256 + static_cast<size_t>(2) * ctas * group * sizeof(float);
 }
 
 }  // namespace
@@ -192,8 +182,9 @@ qattn_status qattn_quantize_kv(const void *k, const void *v, qattn_dtype x_dtype
 
 size_t qattn_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                    int32_t head_dim, int32_t max_seq_len, int32_t num_splits) {
-  if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || max_seq_len < 0 || num_splits < 0 ||
-      num_splits > QATTN_MAX_SPLITS || (head_dim != 64 && head_dim != 128))
+  if (batch <= 0 || batch > QATTN_MAX_BATCH || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      num_q_heads % num_kv_heads || num_q_heads / num_kv_heads > QATTN_MAX_GROUP || max_seq_len < 0 ||
+      num_splits < 0 || num_splits > QATTN_MAX_SPLITS || (head_dim != 64 && head_dim != 128))
     return 0;
   int sms = 152;
   int dev = 0;
@@ -202,8 +193,8 @@ size_t qattn_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t n
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
   }
   cudaGetLastError();
-  const SplitPlan p = plan_splits(batch, num_kv_heads, max_seq_len, num_splits, sms);
-  return workspace_bytes(p.splits, static_cast<int64_t>(batch) * num_q_heads, head_dim);
+  const int ctas = plan_ctas(batch, num_kv_heads, max_seq_len, num_splits, sms);
+  return workspace_bytes(ctas, num_q_heads / num_kv_heads, head_dim);
 }
 
 qattn_status qattn_decode(const uint16_t *q, const qattn_kv_cache *cache, const int32_t *seq_lens,
@@ -212,6 +203,7 @@ qattn_status qattn_decode(const uint16_t *q, const qattn_kv_cache *cache, const 
                           size_t workspace_size, uint16_t *out, float *lse, qattn_stream_t stream) {
   if (batch < 0 || num_q_heads <= 0 || max_seq_len < 0)
     return fail(QATTN_ERR_INVALID_ARG, "batch %d, num_q_heads %d, max_seq_len %d", batch, num_q_heads, max_seq_len);
+  if (batch > QATTN_MAX_BATCH) return fail(QATTN_ERR_UNSUPPORTED, "batch %d > %d", batch, QATTN_MAX_BATCH);
   if (num_splits < 0 || num_splits > QATTN_MAX_SPLITS)
     return fail(QATTN_ERR_INVALID_ARG, "num_splits %d (0..%d)", num_splits, QATTN_MAX_SPLITS);
   KvView view;
@@ -226,10 +218,13 @@ qattn_status qattn_decode(const uint16_t *q, const qattn_kv_cache *cache, const 
   if (!aligned16(q) || !aligned16(out)) return fail(QATTN_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
   DeviceState *ds;
   if ((st = device_state(&ds)) != QATTN_OK) return st;
-  const SplitPlan p = plan_splits(batch, view.hkv, max_seq_len, num_splits, ds->sms);
-  const int64_t rows = static_cast<int64_t>(batch) * num_q_heads;
-  const size_t need = workspace_bytes(p.splits, rows, view.head_dim);
-  if (need > 0 && (!workspace || workspace_size < need || !aligned16(workspace)))
+  const int G = num_q_heads / view.hkv;
+  const int64_t stage_limit = view.page_table ? view.max_pages : view.capacity / kPage;
+  if (static_cast<int64_t>(batch) * view.hkv * stage_limit >= (int64_t(1) << 31))
+    return fail(QATTN_ERR_UNSUPPORTED, "batch * Hkv * cached stages exceeds 2^31");
+  const int ctas = plan_ctas(batch, view.hkv, max_seq_len, num_splits, ds->sms);
+  const size_t need = workspace_bytes(ctas, G, view.head_dim);
+  if (!workspace || workspace_size < need || !aligned16(workspace))
     return fail(QATTN_ERR_WORKSPACE, "workspace of %zu bytes (16-byte aligned) needed, %zu given", need,
                 workspace ? workspace_size : (size_t)0);
   CUtensorMap kmap, vmap;
@@ -239,18 +234,12 @@ qattn_status qattn_decode(const uint16_t *q, const qattn_kv_cache *cache, const 
   DecodeArgs a;
   a.q = q, a.seq_lens = seq_lens, a.out = out, a.lse = lse;
   a.partial_o = static_cast<float *>(workspace);
-  const size_t o_bytes = static_cast<size_t>(p.splits) * rows * view.head_dim * sizeof(float);
-  a.partial_lse = need ? reinterpret_cast<float *>(static_cast<char *>(workspace) + (o_bytes + 255) / 256 * 256) : nullptr;
-  a.batch = batch, a.hq = num_q_heads, a.splits = p.splits, a.chunk = p.chunk;
+  const size_t o_bytes = static_cast<size_t>(2) * ctas * G * view.head_dim * sizeof(float);
+  a.partial_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + (o_bytes + 255) / 256 * 256);
+  a.batch = batch, a.hq = num_q_heads, a.ctas = ctas;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_decode(a, view, kmap, vmap, ds->status, s);
-  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
-  if (p.splits > 1) {
-    e = launch_combine(a.partial_o, a.partial_lse, p.splits, rows, view.head_dim, out, lse, true, s);
-    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
-  }
-  return QATTN_OK;
+  cudaError_t e = launch_decode(a, view, kmap, vmap, ds->status, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "decode launch");
 }
 
 qattn_status qattn_prefill(const uint16_t *q, const qattn_kv_cache *cache, int32_t batch,

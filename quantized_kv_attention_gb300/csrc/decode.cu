@@ -3,127 +3,224 @@
 // TurboAttention (arXiv 2412.08585) §2.1: a decode step attends the new query
 // q_t against the whole cache; §2.2: FlashAttention's tiling with the online
 // softmax of Milakov & Gimelshein (running max and sum, rescaling, final
-// normalisation).  "Quantized Cross-Attention ... In-SRAM Dequantization"
-// §3.1-§3.2: the 4-bit tile is brought from HBM into shared memory and
-// dequantized inline, never written back as fp16; a quantized tile is 4x
-// smaller, so a deeper ring of tiles fits on chip.
+// normalisation), here split along the keys with a log-sum-exp merge.
+// "Quantized Cross-Attention ... In-SRAM Dequantization" §3.1-§3.2: the 4-bit
+// tile goes from HBM into shared memory and is dequantized inline, never
+// written back as fp16; a quantized tile is 4x smaller, so a deep ring of
+// tiles fits on chip.
 //
-// Grid (splits, Hkv, B); a CTA owns the keys [split*chunk, (split+1)*chunk)
-// of one (sequence, kv-head) and all G = Hq/Hkv query heads that read it.
-//   warp 4       producer: per 64-token stage, two 2-D TMA loads of the K/V
-//                codes (128-byte rows, 128B swizzle) and two bulk copies of
-//                the K/V scales, completion tracked by an mbarrier ring.
-//   warps 0-3    consumers: 16 tokens each per stage.
-//     S^T (16 tokens x 8 heads) = codes_K (16 x D) . Q^T on mma.sync
-//       m16n8k16 with tokens on M, the nibbles decoded to exact fp16
-//       integers in registers; the fp32 result is multiplied by the
-//       per-token K scale (exact scale folding, no fp16 rounding of c*s).
-//     online softmax in the log2 domain, warp-uniform lazy rescale.
-//     P' = P * s_V (per-token V scale folded into the probabilities), moved
-//       to the B-operand layout with movmatrix.
-//     O^T (D x 8 heads) += codes_V^T (D x 16 tokens) . P'^T, the V codes
-//       transposed by ldmatrix.trans (pairs of tokens per register) and
-//       decoded in registers.
-//   end: the four consumer warps merge their (m, l, O) in shared memory; the
-//   CTA writes the final fp16 O and lse (one split) or fp32 partials.
+// Work split.  The keys of all (sequence, kv-head) pairs form one list of
+// 64-token stages (pair-major).  A persistent grid of one CTA per SM cuts the
+// list into equal contiguous ranges, so every SM streams the same number of
+// bytes whatever the sequence lengths.  A pair that lies inside one range is
+// finished by its CTA (final fp16 O and lse); a pair cut by range boundaries
+// leaves one fp32 partial per CTA it touches, merged by decode_merge_kernel.
+//
+// CTA roles.
+//   warp 8      producer: for each stage, two 2-D TMA loads of the K/V codes
+//               (128-byte rows, 128B swizzle) and two bulk copies of the K/V
+//               scales into a 16-deep mbarrier ring.
+//   warps 0-7   consumers: warp w takes 32 tokens (half) of every fourth stage.
+//     S^T (16 tokens x 8 heads) = codes_K . Q^T on mma.sync m16n8k16, tokens on
+//       M.  Each nibble becomes an fp16 subnormal u * 2^-24 with u = c + 8 in
+//       one LOP3 (the high nibble of a byte gives 16 u * 2^-24; Q carries the
+//       1/16 for those columns), so S = 2^24 * acc - 8 * sum(q) exactly.
+//     online softmax in the log2 domain, per-token K scale in fp32, one max
+//       reduction per 32 tokens, warp-uniform rescale when the max grows.
+//     P' = P * s_V[token] in fp16, moved into the B-operand layout by movmatrix.
+//     O^T (D x 8 heads) += V codes^T . P'^T, the V codes transposed by
+//       ldmatrix.trans and decoded the same way; O = 2^24 / f * acc - 8 * sum(P').
+//   Segment end: the eight consumer warps merge (m, l, O) in shared memory.
 #include <math.h>
 
+#include "../../include/qattn.h"
 #include "internal.h"
 #include "ptx.cuh"
 
 namespace qattn {
 namespace {
 
-constexpr int kConsumerWarps = 4;
+constexpr int kConsumerWarps = 8;
+constexpr int kWarpsPerStage = 2;                           // 32 tokens each
+constexpr int kGroups = kConsumerWarps / kWarpsPerStage;    // stage it goes to group it % 4
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 4;
+constexpr int kStages = 16;                                 // multiple of kGroups
+constexpr float kTwo24 = 16777216.0f;
+static_assert(kStages % kGroups == 0, "each group owns fixed ring slots");
 
 template <int D>
 struct Cfg {
-  static constexpr int kCodeBytes = kPage * D / 2;                          // per tensor
+  static constexpr int kCodeBytes = kPage * D / 2;  // per tensor per stage
   static constexpr int kStageBytes = (2 * kCodeBytes + 4 * kPage + 1023) / 1024 * 1024;
-  static constexpr int kKBytes = D / 8;  // K code bytes per lane per token
+  static constexpr int kKBytes = D / 8;             // K code bytes per lane per token
   static constexpr int kWords = kKBytes / 4;
-  static constexpr int kMt = D / 16;     // m-tiles of O^T (and k-steps of S)
-  static constexpr int kSmem = kStages * kStageBytes + 1024 + 128;
-  static_assert(kConsumerWarps * (8 * D + 16) * 4 <= kStages * kStageBytes, "merge scratch");
+  static constexpr int kMt = D / 16;                // m-tiles of O^T, k-steps of S
+  static constexpr int kRing = kStages * kStageBytes;
 };
+
+// Dynamic shared memory: ring | merge (O per warp and head) | m, l | prefix | barriers.
+template <int D>
+__host__ __device__ constexpr int merge_bytes(int G) { return kConsumerWarps * G * D * 4; }
+template <int D>
+__host__ __device__ constexpr int smem_bytes(int G, int batch) {
+  return Cfg<D>::kRing + merge_bytes<D>(G) + 2 * kConsumerWarps * 8 * 4 + (batch + 1) * 4 +
+         2 * kStages * 8 + kStages * 4 + 8 + 1024;
+}
 
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
+// Nibbles -> fp16 subnormals: out[k] = (u_lo, u_hi) * 2^-24 for nibble k of
+// each 16-bit half, u = code + 8 (the XOR maps two's complement to offset
+// binary); odd k come out 16x larger (nibble sits four bits higher).
+__device__ __forceinline__ void decode_sub(uint32_t w, uint32_t (&out)[4]) {
+  const uint32_t w8 = w >> 8;
+  out[0] = lop3_and_xor(w, 0x000F000Fu, 0x00080008u);
+  out[1] = lop3_and_xor(w, 0x00F000F0u, 0x00800080u);
+  out[2] = lop3_and_xor(w8, 0x000F000Fu, 0x00080008u);
+  out[3] = lop3_and_xor(w8, 0x00F000F0u, 0x00800080u);
+}
+
+// Range of the flattened stage list owned by CTA i of n: [i*T/n, (i+1)*T/n).
+__device__ __forceinline__ int64_t range_start(int64_t i, int64_t T, int64_t n) { return i * T / n; }
+// CTA owning global stage gs (inverse of range_start).
+__host__ __device__ __forceinline__ int64_t owner_cta(int64_t gs, int64_t T, int64_t n) {
+  return ((gs + 1) * n + T - 1) / T - 1;
+}
+
+struct Loc {
+  int b, kvh, s, n;  // sequence, kv-head, stage within the pair, stages of the pair
+};
+
+// prefix[b] = Hkv * (stages of sequences 0..b-1); locate the pair of stage gs.
+__device__ __forceinline__ Loc locate(int64_t gs, const int *prefix, int batch, int hkv) {
+  int lo = 0, hi = batch - 1;  // largest b with prefix[b] <= gs (and a non-empty b)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (prefix[mid] <= gs) lo = mid; else hi = mid - 1;
+  }
+  Loc l;
+  l.b = lo;
+  l.n = (prefix[lo + 1] - prefix[lo]) / hkv;
+  const int r = static_cast<int>(gs - prefix[lo]);
+  l.kvh = r / l.n;
+  l.s = r - l.kvh * l.n;
+  return l;
+}
+
 template <int D>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(DecodeArgs a, KvView cache, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap vmap, uint32_t *err) {
   using C = Cfg<D>;
+  const int G = a.hq / cache.hkv;
+  const int B = a.batch, hkv = cache.hkv;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * C::kStageBytes);
+  float *smo = reinterpret_cast<float *>(smem + C::kRing);           // [warp][G][D]
+  float *smm = smo + kConsumerWarps * G * D;                          // [warp][8]
+  float *sml = smm + kConsumerWarps * 8;                              // [warp][8]
+  int *prefix = reinterpret_cast<int *>(sml + kConsumerWarps * 8);    // [B + 1]
+  uint64_t *full = reinterpret_cast<uint64_t *>(
+      (reinterpret_cast<uintptr_t>(prefix + B + 1) + 7) & ~static_cast<uintptr_t>(7));
   uint64_t *empty = full + kStages;
-  int *valid = reinterpret_cast<int *>(empty + kStages);
+  int *valid = reinterpret_cast<int *>(empty + kStages);  // [kStages]: 0 = missing page
+  volatile int *abort_flag = valid + kStages;               // set after a timed-out wait
 
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-  const int G = a.hq / cache.hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool paged = cache.page_table != nullptr;
-
-  int len = __ldg(a.seq_lens + b);
   const int64_t limit = paged ? static_cast<int64_t>(cache.max_pages) * kPage : cache.capacity;
-  if (len > limit) {
-    len = static_cast<int>(limit);
-    if (threadIdx.x == 0 && split == 0 && kvh == 0) atomicOr(err, kFlagBadPage);
-  }
-  if (len < 0) len = 0;
-  const int t_begin = split * a.chunk;
-  const int t_end = min(t_begin + a.chunk, len);
-  const int nst = t_end > t_begin ? (t_end - t_begin + kPage - 1) / kPage : 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(smem_u32(full + s), 1);
-      mbar_init(smem_u32(empty + s), kConsumerWarps);
+      mbar_init(smem_u32(empty + s), kWarpsPerStage);
     }
+    *abort_flag = 0;
     fence_mbar_init();
+  }
+  pdl_wait();  // inputs may come from the preceding kernel on the stream
+
+  // prefix[b]: first global stage of sequence b (all its kv-heads, pair-major)
+  for (int b = threadIdx.x; b < B; b += kThreads) {
+    int len = __ldg(a.seq_lens + b);
+    if (len > limit) {
+      len = static_cast<int>(limit);
+      atomicOr(err, kFlagBadPage);
+    }
+    prefix[b + 1] = len > 0 ? hkv * ((len + kPage - 1) / kPage) : 0;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    int carry = 0;
+    for (int base = 0; base < B; base += 32) {
+      int v = base + lane < B ? prefix[base + lane + 1] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+      }
+      if (base + lane < B) prefix[base + lane + 1] = carry + v;
+      carry += __shfl_sync(0xffffffffu, v, 31);
+    }
+    if (lane == 0) prefix[0] = 0;
   }
   __syncthreads();
 
+  const int64_t T = prefix[B];
+  const int64_t gs0 = range_start(blockIdx.x, T, gridDim.x);
+  const int64_t gs1 = range_start(blockIdx.x + 1, T, gridDim.x);
+  const int nst = static_cast<int>(gs1 - gs0);
+  if (nst <= 0) return;
+
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && nst > 0) {
+    if (lane == 0) {
       prefetch_tmap(&kmap);
       prefetch_tmap(&vmap);
-      for (int it = 0; it < nst; ++it) {
-        const int s = it % kStages;
-        const uint32_t ph = (it / kStages) & 1;
-        if (it >= kStages && !mbar_wait(smem_u32(empty + s), ph ^ 1, err)) break;
-        const int tok = t_begin + it * kPage;
-        int64_t row_tok;  // cache row of the stage's first token
-        bool ok = true;
-        if (paged) {
-          const int page = __ldg(cache.page_table + static_cast<int64_t>(b) * cache.max_pages + tok / kPage);
-          ok = page >= 0 && page < cache.num_pages;
-          if (!ok) atomicOr(err, kFlagBadPage);
-          row_tok = (static_cast<int64_t>(ok ? page : 0) * cache.hkv + kvh) * kPage;
-        } else {
-          row_tok = (static_cast<int64_t>(b) * cache.hkv + kvh) * cache.capacity + tok;
+      int it = 0;
+      for (int64_t gs = gs0; gs < gs1;) {
+        const Loc l = locate(gs, prefix, B, hkv);
+        const int cnt = static_cast<int>(min(static_cast<int64_t>(l.n - l.s), gs1 - gs));
+        for (int j = 0; j < cnt; ++j, ++it) {
+          const int s = it % kStages;
+          const uint32_t ph = (it / kStages) & 1;
+          if (it >= kStages &&
+              !mbar_wait(smem_u32(empty + s), ph ^ 1, err, *abort_flag ? kDrainCycles : kWaitCycles)) {
+            *abort_flag = 1;  // stop issuing; the consumers drain with short waits
+            return;
+          }
+          const int stage = l.s + j;
+          int64_t row_tok;
+          bool ok = true;
+          if (paged) {
+            const int page =
+                __ldg(cache.page_table + static_cast<int64_t>(l.b) * cache.max_pages + stage);
+            ok = page >= 0 && page < cache.num_pages;
+            if (!ok) atomicOr(err, kFlagBadPage);
+            row_tok = (static_cast<int64_t>(ok ? page : 0) * hkv + l.kvh) * kPage;
+          } else {
+            row_tok = (static_cast<int64_t>(l.b) * hkv + l.kvh) * cache.capacity +
+                      static_cast<int64_t>(stage) * kPage;
+          }
+          const uint32_t full_s = smem_u32(full + s);
+          valid[s] = ok;
+          if (ok) {
+            uint8_t *st = smem + s * C::kStageBytes;
+            const int row128 = static_cast<int>(row_tok * (D / 2) / 128);
+            mbar_arrive_expect_tx(full_s, 2 * C::kCodeBytes + 4 * kPage);
+            tma_load_2d(smem_u32(st), &kmap, 0, row128, full_s);
+            tma_load_2d(smem_u32(st + C::kCodeBytes), &vmap, 0, row128, full_s);
+            bulk_g2s(smem_u32(st + 2 * C::kCodeBytes), cache.k_scales + row_tok, 2 * kPage, full_s);
+            bulk_g2s(smem_u32(st + 2 * C::kCodeBytes + 2 * kPage), cache.v_scales + row_tok,
+                     2 * kPage, full_s);
+          } else {
+            mbar_arrive(full_s);  // a missing page: its tokens are masked
+          }
         }
-        valid[s] = ok;
-        const uint32_t full_s = smem_u32(full + s);
-        if (ok) {
-          uint8_t *st = smem + s * C::kStageBytes;
-          const int row128 = static_cast<int>(row_tok * (D / 2) / 128);
-          mbar_arrive_expect_tx(full_s, 2 * C::kCodeBytes + 4 * kPage);
-          tma_load_2d(smem_u32(st), &kmap, 0, row128, full_s);
-          tma_load_2d(smem_u32(st + C::kCodeBytes), &vmap, 0, row128, full_s);
-          bulk_g2s(smem_u32(st + 2 * C::kCodeBytes), cache.k_scales + row_tok, 2 * kPage, full_s);
-          bulk_g2s(smem_u32(st + 2 * C::kCodeBytes + 2 * kPage), cache.v_scales + row_tok,
-                   2 * kPage, full_s);
-        } else {
-          mbar_arrive(full_s);
-        }
+        gs += cnt;
       }
     }
     return;
@@ -131,195 +228,364 @@ __global__ void __launch_bounds__(kThreads)
 
   // -------------------------------------------------------------- consumers
   const int g = lane >> 2, c = lane & 3;
-  // Q as the B operand (k = head dim, n = head g).  The head-dim order inside
-  // a k-step follows the nibble decoder: word i of lane c's code bytes covers
-  // d = dbase + 8i + {0..7} and decode_nibbles yields the pairs (e, e + 4).
-  uint32_t qb[C::kMt][2];
-  {
-    const int dbase = c * (D / 4);
-    const __half *qrow =
-        reinterpret_cast<const __half *>(a.q) + (static_cast<int64_t>(b) * a.hq + kvh * G + g) * D;
-#pragma unroll
-    for (int i = 0; i < C::kWords; ++i)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        __half lo = __float2half(0.f), hi = __float2half(0.f);
-        if (g < G) {
-          lo = qrow[dbase + 8 * i + e];
-          hi = qrow[dbase + 8 * i + e + 4];
-        }
-        __half2 h2 = __halves2half2(lo, hi);
-        qb[2 * i + (e >> 1)][e & 1] = *reinterpret_cast<uint32_t *>(&h2);
-      }
-  }
+  const int grp = warp / kWarpsPerStage, sub = warp % kWarpsPerStage;
+  const float kf = a.scale_log2 * kTwo24;  // folds the 2^-24 of the subnormal codes
+  int it = 0;                              // CTA-local stage index, as in the producer
+  for (int64_t gs = gs0; gs < gs1;) {
+    const Loc l = locate(gs, prefix, B, hkv);
+    const int cnt = static_cast<int>(min(static_cast<int64_t>(l.n - l.s), gs1 - gs));
+    const int len = static_cast<int>(min(static_cast<int64_t>(__ldg(a.seq_lens + l.b)), limit));
 
-  float m0 = -1e30f, m1 = -1e30f, l0 = 0.f, l1 = 0.f;  // heads 2c, 2c+1 (log2 domain)
-  float o[C::kMt][4];
-#pragma unroll
-  for (int mt = 0; mt < C::kMt; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-
-  for (int it = 0; it < nst; ++it) {
-    const int s = it % kStages;
-    const uint32_t ph = (it / kStages) & 1;
-    if (!mbar_wait(smem_u32(full + s), ph, err)) break;
-    const int nvalid = t_end - (t_begin + it * kPage + warp * 16);
-    if (valid[s] && nvalid > 0) {
-      const uint32_t kb = smem_u32(smem + s * C::kStageBytes);
-      const uint32_t vb = kb + C::kCodeBytes;
-      const __half *sks = reinterpret_cast<const __half *>(smem + s * C::kStageBytes + 2 * C::kCodeBytes);
-      const __half *svs = sks + kPage;
-      const int lt = warp * 16 + g;  // stage-local token of fragment row g
-
-      // S^T = codes_K . Q^T  (rows g and g+8 = tokens lt, lt+8)
-      uint32_t kw0[C::kWords], kw1[C::kWords];
-      if constexpr (C::kWords == 4) {
-        uint4 u0 = lds128(kb + swz128(lt * (D / 2) + c * C::kKBytes));
-        uint4 u1 = lds128(kb + swz128((lt + 8) * (D / 2) + c * C::kKBytes));
-        kw0[0] = u0.x, kw0[1] = u0.y, kw0[2] = u0.z, kw0[3] = u0.w;
-        kw1[0] = u1.x, kw1[1] = u1.y, kw1[2] = u1.z, kw1[3] = u1.w;
-      } else {
-        uint2 u0 = lds64(kb + swz128(lt * (D / 2) + c * C::kKBytes));
-        uint2 u1 = lds64(kb + swz128((lt + 8) * (D / 2) + c * C::kKBytes));
-        kw0[0] = u0.x, kw0[1] = u0.y;
-        kw1[0] = u1.x, kw1[1] = u1.y;
-      }
-      float sacc[4] = {0.f, 0.f, 0.f, 0.f};
+    // Q of head g as the B operand.  Lane c covers d = c*D/4 + 8i + {0..7}
+    // (word i of its K code bytes); the decoder pairs (e, e+4) and nibble
+    // positions 1 and 3 come out 16x larger, so those columns carry q / 16.
+    uint32_t qb[C::kMt][2];
+    float qsum = 0.f;
+    {
+      const int dbase = c * (D / 4);
+      const uint4 *qv = reinterpret_cast<const uint4 *>(
+          a.q + (static_cast<int64_t>(l.b) * a.hq + l.kvh * G + min(g, G - 1)) * D + dbase);
+      const __half2 sixteenth = __float2half2_rn(0.0625f);
 #pragma unroll
       for (int i = 0; i < C::kWords; ++i) {
-        uint32_t x0[4], x1[4];
-        decode_nibbles(kw0[i], x0);
-        decode_nibbles(kw1[i], x1);
-        mma_16816(sacc, x0[0], x1[0], x0[1], x1[1], qb[2 * i][0], qb[2 * i][1]);
-        mma_16816(sacc, x0[2], x1[2], x0[3], x1[3], qb[2 * i + 1][0], qb[2 * i + 1][1]);
+        uint4 u = g < G ? __ldg(qv + i) : make_uint4(0, 0, 0, 0);
+        const uint32_t p0 = __byte_perm(u.x, u.z, 0x5410), p1 = __byte_perm(u.x, u.z, 0x7632);
+        const uint32_t p2 = __byte_perm(u.y, u.w, 0x5410), p3 = __byte_perm(u.y, u.w, 0x7632);
+        __half2 h1 = __hmul2(*reinterpret_cast<const __half2 *>(&p1), sixteenth);
+        __half2 h3 = __hmul2(*reinterpret_cast<const __half2 *>(&p3), sixteenth);
+        qb[2 * i][0] = p0;
+        qb[2 * i][1] = *reinterpret_cast<uint32_t *>(&h1);
+        qb[2 * i + 1][0] = p2;
+        qb[2 * i + 1][1] = *reinterpret_cast<uint32_t *>(&h3);
+        // the bias must use exactly the values the MMA multiplies
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&p0));
+        const float2 f2 = __half22float2(*reinterpret_cast<const __half2 *>(&p2));
+        const float2 f1 = __half22float2(h1), f3 = __half22float2(h3);
+        qsum += f0.x + f0.y + f2.x + f2.y + 16.f * (f1.x + f1.y + f3.x + f3.y);
       }
-      const bool v0 = g < nvalid, v1 = g + 8 < nvalid;
-      const float fk0 = __half2float(sks[lt]) * a.scale_log2;
-      const float fk1 = __half2float(sks[lt + 8]) * a.scale_log2;
-      const float t0 = v0 ? sacc[0] * fk0 : -INFINITY, t1 = v0 ? sacc[1] * fk0 : -INFINITY;
-      const float t2 = v1 ? sacc[2] * fk1 : -INFINITY, t3 = v1 ? sacc[3] * fk1 : -INFINITY;
+    }
+    qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
+    qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
+    // raw-unit bias 8 * sum(q) * 2^-24 for the thread's heads 2c and 2c+1
+    const float bq0 = 8.f / kTwo24 * __shfl_sync(0xffffffffu, qsum, (2 * c) << 2);
+    const float bq1 = 8.f / kTwo24 * __shfl_sync(0xffffffffu, qsum, (2 * c + 1) << 2);
 
-      // online softmax: the running max changes rarely, so the rescale is a
-      // warp-uniform branch taken only when some head's max grows.
-      float mx0 = fmaxf(t0, t2), mx1 = fmaxf(t1, t3);
+    float m0 = -1e30f, m1 = -1e30f, l0 = 0.f, l1 = 0.f, ps0 = 0.f, ps1 = 0.f;
+    float o[C::kMt][4];
 #pragma unroll
-      for (int off = 4; off < 32; off <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    for (int mt = 0; mt < C::kMt; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+
+    for (int j = 0; j < cnt; ++j, ++it) {
+      if (it % kGroups != grp) continue;
+      const int s = it % kStages;
+      const uint32_t ph = (it / kStages) & 1;
+      const bool got = mbar_wait(smem_u32(full + s), ph, err, *abort_flag ? kDrainCycles : kWaitCycles);
+      if (!got) *abort_flag = 1;
+      const int nvalid = min(kPage, len - (l.s + j) * kPage) - sub * 32;
+      if (got && valid[s] && nvalid > 0) {
+        const uint32_t kb = smem_u32(smem + s * C::kStageBytes);
+        const uint32_t vb = kb + C::kCodeBytes;
+        const __half *sks = reinterpret_cast<const __half *>(smem + s * C::kStageBytes + 2 * C::kCodeBytes);
+        const __half *svs = sks + kPage;
+
+        // S^T for two 16-token tiles (independent MMA chains)
+        float sacc[2][4];
+        uint32_t kw[2][2][C::kWords];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          sacc[t][0] = sacc[t][1] = sacc[t][2] = sacc[t][3] = 0.f;
+          const int lt = sub * 32 + t * 16 + g;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t addr = kb + swz128((lt + 8 * h) * (D / 2) + c * C::kKBytes);
+            if constexpr (C::kWords == 4) {
+              const uint4 u = lds128(addr);
+              kw[t][h][0] = u.x, kw[t][h][1] = u.y, kw[t][h][2] = u.z, kw[t][h][3] = u.w;
+            } else {
+              const uint2 u = lds64(addr);
+              kw[t][h][0] = u.x, kw[t][h][1] = u.y;
+            }
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < C::kWords; ++i)
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            uint32_t x0[4], x1[4];
+            decode_sub(kw[t][0][i], x0);
+            decode_sub(kw[t][1][i], x1);
+            mma_16816(sacc[t], x0[0], x1[0], x0[1], x1[1], qb[2 * i][0], qb[2 * i][1]);
+            mma_16816(sacc[t], x0[2], x1[2], x0[3], x1[3], qb[2 * i + 1][0], qb[2 * i + 1][1]);
+          }
+
+        float ts[2][4], fv[2][2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int lt = sub * 32 + t * 16 + g;
+          const bool v0 = t * 16 + g < nvalid, v1 = t * 16 + g + 8 < nvalid;
+          const float f0 = __half2float(sks[lt]) * kf, f1 = __half2float(sks[lt + 8]) * kf;
+          ts[t][0] = v0 ? (sacc[t][0] - bq0) * f0 : -INFINITY;
+          ts[t][1] = v0 ? (sacc[t][1] - bq1) * f0 : -INFINITY;
+          ts[t][2] = v1 ? (sacc[t][2] - bq0) * f1 : -INFINITY;
+          ts[t][3] = v1 ? (sacc[t][3] - bq1) * f1 : -INFINITY;
+          fv[t][0] = v0 ? __half2float(svs[lt]) : 0.f;
+          fv[t][1] = v1 ? __half2float(svs[lt + 8]) : 0.f;
+        }
+        float mx0 = fmaxf(fmaxf(ts[0][0], ts[0][2]), fmaxf(ts[1][0], ts[1][2]));
+        float mx1 = fmaxf(fmaxf(ts[0][1], ts[0][3]), fmaxf(ts[1][1], ts[1][3]));
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        if (__any_sync(0xffffffffu, mx0 > m0 || mx1 > m1)) {
+          const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+          const float al0 = ex2(m0 - n0), al1 = ex2(m1 - n1);
+          m0 = n0, m1 = n1;
+          l0 *= al0, l1 *= al1, ps0 *= al0, ps1 *= al1;
+#pragma unroll
+          for (int mt = 0; mt < C::kMt; ++mt) {
+            o[mt][0] *= al0, o[mt][1] *= al1, o[mt][2] *= al0, o[mt][3] *= al1;
+          }
+        }
+        uint32_t pb[2][2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const float p0 = ex2(ts[t][0] - m0), p1 = ex2(ts[t][1] - m1);
+          const float p2 = ex2(ts[t][2] - m0), p3 = ex2(ts[t][3] - m1);
+          l0 += p0 + p2;
+          l1 += p1 + p3;
+          const uint32_t r0 = pack_half2(p0 * fv[t][0], p1 * fv[t][0]);
+          const uint32_t r1 = pack_half2(p2 * fv[t][1], p3 * fv[t][1]);
+          const float2 q0 = __half22float2(*reinterpret_cast<const __half2 *>(&r0));
+          const float2 q1 = __half22float2(*reinterpret_cast<const __half2 *>(&r1));
+          ps0 += q0.x + q1.x;  // sum of the fp16 P' the MMA sees (bias of the V codes)
+          ps1 += q0.y + q1.y;
+          pb[t][0] = movmatrix_trans(r0);
+          pb[t][1] = movmatrix_trans(r1);
+        }
+        // O^T += V codes^T . P'^T; ldmatrix.x4.trans matrix q holds tokens
+        // (q & 2 ? 8 : 0) + 0..7 of the tile at 16-byte chunk 2 jp + (q & 1).
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int jp = 0; jp < D / 64; ++jp) {
+            const int q = lane >> 3;
+            const int vt = sub * 32 + t * 16 + ((q & 2) ? 8 : 0) + (lane & 7);
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4_trans(vb + swz128(vt * (D / 2) + (2 * jp + (q & 1)) * 16), r0, r1, r2, r3);
+            uint32_t d0[4], d1[4], d2[4], d3[4];
+            decode_sub(r0, d0);
+            decode_sub(r1, d1);
+            decode_sub(r2, d2);
+            decode_sub(r3, d3);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_16816(o[jp * 4 + k], d0[k], d1[k], d2[k], d3[k], pb[t][0], pb[t][1]);
+          }
       }
-      if (__any_sync(0xffffffffu, mx0 > m0 || mx1 > m1)) {
-        const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
-        const float al0 = ex2(m0 - n0), al1 = ex2(m1 - n1);
-        m0 = n0, m1 = n1, l0 *= al0, l1 *= al1;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(empty + s));
+    }
+
+    // --------------------------------------------- segment end: merge warps
 #pragma unroll
-        for (int mt = 0; mt < C::kMt; ++mt) {
-          o[mt][0] *= al0, o[mt][1] *= al1, o[mt][2] *= al0, o[mt][3] *= al1;
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+      ps0 += __shfl_xor_sync(0xffffffffu, ps0, off);
+      ps1 += __shfl_xor_sync(0xffffffffu, ps1, off);
+    }
+#pragma unroll
+    for (int jp = 0; jp < D / 64; ++jp)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int mt = jp * 4 + k;
+        const float fac = (k & 1) ? kTwo24 / 16.f : kTwo24;
+        const int dlo = 64 * jp + 4 * g + k, dhi = dlo + 32;
+        if (2 * c < G) {
+          float *w0 = smo + (warp * G + 2 * c) * D;
+          w0[dlo] = o[mt][0] * fac - 8.f * ps0;
+          w0[dhi] = o[mt][2] * fac - 8.f * ps0;
+        }
+        if (2 * c + 1 < G) {
+          float *w1 = smo + (warp * G + 2 * c + 1) * D;
+          w1[dlo] = o[mt][1] * fac - 8.f * ps1;
+          w1[dhi] = o[mt][3] * fac - 8.f * ps1;
         }
       }
-      const float p0 = ex2(t0 - m0), p1 = ex2(t1 - m1), p2 = ex2(t2 - m0), p3 = ex2(t3 - m1);
-      l0 += p0 + p2;
-      l1 += p1 + p3;
-      const float fv0 = v0 ? __half2float(svs[lt]) : 0.f;
-      const float fv1 = v1 ? __half2float(svs[lt + 8]) : 0.f;
-      const uint32_t pb0 = movmatrix_trans(pack_half2(p0 * fv0, p1 * fv0));
-      const uint32_t pb1 = movmatrix_trans(pack_half2(p2 * fv1, p3 * fv1));
-
-      // O^T += codes_V^T . P'^T: matrix q of ldmatrix.x4.trans holds tokens
-      // (q & 2 ? 8 : 0) + 0..7 of this warp's slice at 16-byte chunk 2 jp + (q & 1).
+    if (g == 0) {
+      smm[warp * 8 + 2 * c] = m0, smm[warp * 8 + 2 * c + 1] = m1;
+      sml[warp * 8 + 2 * c] = l0, sml[warp * 8 + 2 * c + 1] = l1;
+    }
+    consumer_sync();
+    const bool complete = l.s == 0 && cnt == l.n;
+    const int64_t slot = l.s > 0 ? 2 * static_cast<int64_t>(blockIdx.x) : 2 * static_cast<int64_t>(blockIdx.x) + 1;
+    for (int idx = threadIdx.x; idx < G * D; idx += kConsumerWarps * 32) {
+      const int h = idx / D, d = idx - h * D;
+      float M = smm[h];
 #pragma unroll
-      for (int jp = 0; jp < D / 64; ++jp) {
-        const int q = lane >> 3;
-        const int vt = warp * 16 + ((q & 2) ? 8 : 0) + (lane & 7);
-        uint32_t r0, r1, r2, r3;
-        ldsm_x4_trans(vb + swz128(vt * (D / 2) + (2 * jp + (q & 1)) * 16), r0, r1, r2, r3);
-        uint32_t d0[4], d1[4], d2[4], d3[4];
-        decode_nibbles(r0, d0);
-        decode_nibbles(r1, d1);
-        decode_nibbles(r2, d2);
-        decode_nibbles(r3, d3);
+      for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, smm[w * 8 + h]);
+      float L = 0.f, acc = 0.f;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) mma_16816(o[jp * 4 + k], d0[k], d1[k], d2[k], d3[k], pb0, pb1);
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float sc = ex2(smm[w * 8 + h] - M);
+        L += sc * sml[w * 8 + h];
+        acc += sc * smo[(w * G + h) * D + d];
+      }
+      const bool live = L > 0.f;
+      const float ov = live ? acc / L : 0.f;
+      const float lse_v = live ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+      if (complete) {
+        const int64_t row = static_cast<int64_t>(l.b) * a.hq + l.kvh * G + h;
+        a.out[row * D + d] = __half_as_ushort(__float2half_rn(ov));
+        if (d == 0 && a.lse) a.lse[row] = lse_v;
+      } else {
+        const int64_t prow = slot * G + h;
+        a.partial_o[prow * D + d] = ov;
+        if (d == 0) a.partial_lse[prow] = lse_v;
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(empty + s));
+    consumer_sync();  // the merge buffer is free again
+    gs += cnt;
   }
+}
 
-#pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+// Merges the partials of every (sequence, kv-head) pair that the balanced
+// ranges cut: pair p spanning CTAs c0 < c1 has partials in slot 2*c0 + 1
+// (its start, in c0's last segment) and slots 2*c for c0 < c <= c1.  Pairs of
+// empty sequences get O = 0, lse = -inf.  One CTA per pair, warp h per head.
+template <int D>
+__global__ void __launch_bounds__(256)
+    decode_merge_kernel(const int32_t *__restrict__ seq_lens, int batch, int hkv, int G, int ctas,
+                        int64_t limit, const float *__restrict__ po, const float *__restrict__ pl,
+                        uint16_t *__restrict__ out, float *__restrict__ lse) {
+  constexpr int VPL = D / 32;
+  __shared__ float wsh[8][QATTN_MAX_SPLITS + 1];
+  __shared__ int red[2][8];
+  pdl_wait();
+  const int b = blockIdx.x / hkv, kvh = blockIdx.x % hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto stages = [&](int bb) {
+    const int64_t len = min(static_cast<int64_t>(__ldg(seq_lens + bb)), limit);
+    return len > 0 ? static_cast<int>((len + kPage - 1) / kPage) : 0;
+  };
+  int tot = 0, pre = 0;
+  for (int bb = threadIdx.x; bb < batch; bb += 256) {
+    const int n = stages(bb);
+    tot += n;
+    if (bb < b) pre += n;
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    pre += __shfl_xor_sync(0xffffffffu, pre, o);
+  }
+  if (lane == 0) red[0][warp] = tot, red[1][warp] = pre;
+  __syncthreads();
+  tot = pre = 0;
+  for (int w = 0; w < 8; ++w) tot += red[0][w], pre += red[1][w];
+  const int n = stages(b);
+  const int64_t hq = static_cast<int64_t>(hkv) * G;
+  if (warp >= G) return;
+  const int64_t row = static_cast<int64_t>(b) * hq + kvh * G + warp;
+  if (n == 0) {
+    for (int d = lane; d < D; d += 32) out[row * D + d] = 0;
+    if (lane == 0 && lse) lse[row] = -INFINITY;
+    return;
+  }
+  const int64_t T = static_cast<int64_t>(hkv) * tot;
+  const int64_t first = static_cast<int64_t>(hkv) * pre + static_cast<int64_t>(kvh) * n;
+  const int64_t c0 = owner_cta(first, T, ctas), c1 = owner_cta(first + n - 1, T, ctas);
+  if (c0 == c1) return;  // finished inside one CTA
+  const int np = static_cast<int>(c1 - c0 + 1);
+  auto slot_of = [&](int k) { return k == 0 ? 2 * c0 + 1 : 2 * (c0 + k); };
+  float M = -INFINITY;
+  for (int k = lane; k < np; k += 32) M = fmaxf(M, pl[slot_of(k) * G + warp]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float z = 0.f;
+  for (int k = lane; k < np; k += 32) {
+    const float lv = pl[slot_of(k) * G + warp];
+    const float e = lv == -INFINITY ? 0.f : expf(lv - M);
+    wsh[warp][k] = e;
+    z += e;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  __syncwarp();
+  float acc[VPL];
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) acc[j] = 0.f;
+  for (int k = 0; k < np; ++k) {
+    const float wk = wsh[warp][k];
+    if (wk > 0.f) {
+      const float *src = po + (slot_of(k) * G + warp) * D + lane * VPL;
+      if constexpr (VPL == 4) {
+        const float4 x = __ldg(reinterpret_cast<const float4 *>(src));
+        acc[0] += wk * x.x, acc[1] += wk * x.y, acc[2] += wk * x.z, acc[3] += wk * x.w;
+      } else {
+        const float2 x = __ldg(reinterpret_cast<const float2 *>(src));
+        acc[0] += wk * x.x, acc[1] += wk * x.y;
+      }
+    }
+  }
+  const float inv = M == -INFINITY ? 0.f : 1.f / z;
+#pragma unroll
+  for (int j = 0; j < VPL; ++j)
+    out[row * D + lane * VPL + j] = __half_as_ushort(__float2half_rn(acc[j] * inv));
+  if (lane == 0 && lse) lse[row] = M == -INFINITY ? -INFINITY : M + logf(z);
+}
 
-  // ------------------------------------------- merge the consumer warps
-  consumer_sync();  // every warp is done with the stage buffers
-  float *smo = reinterpret_cast<float *>(smem);  // [warp][head 8][D]
-  float *smm = smo + kConsumerWarps * 8 * D;    // [warp][head 8]
-  float *sml = smm + kConsumerWarps * 8;
-#pragma unroll
-  for (int jp = 0; jp < D / 64; ++jp)
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int mt = jp * 4 + k;
-      const int dlo = 64 * jp + 4 * g + k, dhi = dlo + 32;
-      float *w0 = smo + (warp * 8 + 2 * c) * D;
-      w0[dlo] = o[mt][0];
-      w0[D + dlo] = o[mt][1];
-      w0[dhi] = o[mt][2];
-      w0[D + dhi] = o[mt][3];
-    }
-  if (g == 0) {
-    smm[warp * 8 + 2 * c] = m0, smm[warp * 8 + 2 * c + 1] = m1;
-    sml[warp * 8 + 2 * c] = l0, sml[warp * 8 + 2 * c + 1] = l1;
-  }
-  consumer_sync();
-  const int tid = threadIdx.x;
-  for (int idx = tid; idx < G * D; idx += kConsumerWarps * 32) {
-    const int h = idx / D, d = idx % D;
-    float M = smm[h];
-#pragma unroll
-    for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, smm[w * 8 + h]);
-    float L = 0.f, acc = 0.f;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) {
-      const float sc = ex2(smm[w * 8 + h] - M);
-      L += sc * sml[w * 8 + h];
-      acc += sc * smo[(w * 8 + h) * D + d];
-    }
-    const int64_t row = static_cast<int64_t>(b) * a.hq + kvh * G + h;
-    const bool live = L > 0.f;
-    const float lse_v = live ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
-    if (a.splits == 1) {
-      a.out[row * D + d] = __half_as_ushort(__float2half_rn(live ? acc / L : 0.f));
-      if (d == 0 && a.lse) a.lse[row] = lse_v;
-    } else {
-      const int64_t prow = static_cast<int64_t>(split) * a.batch * a.hq + row;
-      a.partial_o[prow * D + d] = live ? acc / L : 0.f;
-      if (d == 0) a.partial_lse[prow] = lse_v;
-    }
-  }
+cudaLaunchAttribute pdl_attr() {
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  return attr;
 }
 
 template <int D>
 cudaError_t launch_d(const DecodeArgs &a, const KvView &cache, const CUtensorMap &kmap,
                      const CUtensorMap &vmap, uint32_t *err, cudaStream_t stream) {
-  using C = Cfg<D>;
-  static bool configured = false;  // attribute is per-function, set once per process
+  static bool configured = false;  // per-function attribute, set once per process
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmem);
+                                         smem_bytes<D>(QATTN_MAX_GROUP, QATTN_MAX_BATCH));
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid(a.splits, cache.hkv, a.batch);
-  decode_kernel<D><<<grid, kThreads, C::kSmem, stream>>>(a, cache, kmap, vmap, err);
-  return cudaGetLastError();
+  const int G = a.hq / cache.hkv;
+  cudaLaunchAttribute attr[1] = {pdl_attr()};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.ctas);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem_bytes<D>(G, a.batch);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<D>, a, cache, kmap, vmap, err);
+  if (e != cudaSuccess) return e;
+  const int64_t limit = cache.page_table ? static_cast<int64_t>(cache.max_pages) * kPage : cache.capacity;
+  cudaLaunchConfig_t mc = {};
+  mc.gridDim = dim3(a.batch * cache.hkv);
+  mc.blockDim = dim3(256);
+  mc.stream = stream;
+  mc.attrs = attr;
+  mc.numAttrs = 1;
+  return cudaLaunchKernelEx(&mc, decode_merge_kernel<D>, a.seq_lens, a.batch, cache.hkv, G, a.ctas, limit,
+                            static_cast<const float *>(a.partial_o), static_cast<const float *>(a.partial_lse),
+                            a.out, a.lse);
 }
 
 }  // namespace
 
+int decode_smem_bytes(int head_dim, int group, int batch) {
+  return head_dim == 128 ? smem_bytes<128>(group, batch) : smem_bytes<64>(group, batch);
+}
+
 cudaError_t launch_decode(const DecodeArgs &a, const KvView &cache, const CUtensorMap &kmap,
                           const CUtensorMap &vmap, uint32_t *err, cudaStream_t stream) {
-  if (a.batch == 0) return cudaSuccess;
+  if (a.batch == 0 || a.ctas <= 0) return cudaSuccess;
   return cache.head_dim == 128 ? launch_d<128>(a, cache, kmap, vmap, err, stream)
                                : launch_d<64>(a, cache, kmap, vmap, err, stream);
 }

@@ -28,9 +28,9 @@ cudaError_t launch_quantize(const void *k, const void *v, bool fp16_in, int batc
                             const int32_t *start_pos, const KvView &cache, uint32_t *err,
                             cudaStream_t stream);
 
-// decode.cu: split-KV decode.  With splits == 1 it writes out/lse directly;
-// otherwise it writes fp32 partials (partial_o [splits, B*Hq, D], partial_lse
-// [splits, B*Hq]) that launch_combine merges.
+// decode.cu: persistent split-KV decode over `ctas` balanced key ranges plus
+// the merge of pairs the ranges cut.  Workspace: partial_o [2*ctas, G, D] and
+// partial_lse [2*ctas, G] fp32 (two slots per CTA).
 struct DecodeArgs {
   const uint16_t *q;
   const int32_t *seq_lens;
@@ -38,9 +38,10 @@ struct DecodeArgs {
   float *lse;
   float *partial_o;
   float *partial_lse;
-  int batch, hq, splits, chunk;  // chunk: tokens per split (multiple of kPage)
-  float scale_log2;              // softmax_scale * log2(e)
+  int batch, hq, ctas;
+  float scale_log2;  // softmax_scale * log2(e)
 };
+int decode_smem_bytes(int head_dim, int group, int batch);
 cudaError_t launch_decode(const DecodeArgs &a, const KvView &cache, const CUtensorMap &kmap,
                           const CUtensorMap &vmap, uint32_t *err, cudaStream_t stream);
 

@@ -21,6 +21,8 @@ enum : uint32_t {
 
 // ~2 s at 2 GHz: far above any legitimate wait, far below a watchdog.
 constexpr long long kWaitCycles = 4000000000LL;
+// After a first timeout a kernel drains with waits this short (~1 ms).
+constexpr long long kDrainCycles = 2000000LL;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -61,11 +63,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *err) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t *err,
+                                          long long limit = kWaitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       if (err) atomicOr(err, kFlagWaitTimeout);
       return false;
     }

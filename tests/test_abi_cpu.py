@@ -94,12 +94,13 @@ def test_quantize_and_combine_reject_bad_arguments():
 
 
 def test_workspace_size_host_arithmetic():
-    # explicit split counts need no device: partial_o [S, B*Hq, D] fp32, padded
-    # to 256 bytes, then partial_lse [S, B*Hq] fp32
-    assert qa.decode_workspace_size(2, 8, 2, 128, 1000, 4) == 4 * 16 * 128 * 4 + 4 * 16 * 4
-    assert qa.decode_workspace_size(1, 1, 1, 64, 300, 3) == 3 * 64 * 4 + 256 - (3 * 64 * 4) % 256 + 3 * 4 \
-        if (3 * 64 * 4) % 256 else 3 * 64 * 4 + 3 * 4
-    assert qa.decode_workspace_size(2, 8, 2, 128, 1000, 1) == 0           # one split: no workspace
-    assert qa.decode_workspace_size(2, 8, 2, 128, 60, 4) == 0             # one 64-token chunk
-    assert qa.decode_workspace_size(0, 8, 2, 128, 60, 4) == 0             # invalid
+    # explicit range counts need no device: two partial slots per range,
+    # partial_o [2 * ranges, G, D] fp32 padded to 256 bytes, then partial_lse [2 * ranges, G]
+    assert qa.decode_workspace_size(2, 8, 2, 128, 1000, 4) == 2 * 4 * 4 * 128 * 4 + 2 * 4 * 4 * 4
+    # ranges are capped by the number of 64-token stages: 1 * 1 * ceil(300 / 64) = 5
+    assert qa.decode_workspace_size(1, 1, 1, 64, 300, 9) == 2 * 5 * 64 * 4 + 2 * 5 * 4
+    assert qa.decode_workspace_size(1, 3, 1, 64, 64, 1) == 2 * 3 * 64 * 4 + 2 * 3 * 4       # one range, G = 3
+    assert qa.decode_workspace_size(0, 8, 2, 128, 60, 4) == 0             # invalid sizes
     assert qa.decode_workspace_size(2, 8, 2, 96, 600, 4) == 0
+    assert qa.decode_workspace_size(2, 8, 3, 128, 600, 4) == 0
+    assert qa.decode_workspace_size(4096, 8, 2, 128, 600, 4) == 0         # batch above the limit
