@@ -500,13 +500,19 @@ __global__ void __launch_bounds__(256)
   if (c0 == c1) return;  // finished inside one CTA
   const int np = static_cast<int>(c1 - c0 + 1);
   auto slot_of = [&](int k) { return k == 0 ? 2 * c0 + 1 : 2 * (c0 + k); };
+  // CTAs between c0 and c1 whose range is empty (more CTAs than stages) wrote nothing
+  auto used = [&](int k) {
+    const int64_t c = c0 + k;
+    return k == 0 || c * T / ctas < (c + 1) * T / ctas;
+  };
   float M = -INFINITY;
-  for (int k = lane; k < np; k += 32) M = fmaxf(M, pl[slot_of(k) * G + warp]);
+  for (int k = lane; k < np; k += 32)
+    if (used(k)) M = fmaxf(M, pl[slot_of(k) * G + warp]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float z = 0.f;
   for (int k = lane; k < np; k += 32) {
-    const float lv = pl[slot_of(k) * G + warp];
+    const float lv = used(k) ? pl[slot_of(k) * G + warp] : -INFINITY;
     const float e = lv == -INFINITY ? 0.f : expf(lv - M);
     wsh[warp][k] = e;
     z += e;
