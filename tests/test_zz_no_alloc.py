@@ -70,7 +70,7 @@ def test_noalloc_matches_decode_on_consecutive_calls():
 def test_noalloc_refuses_sizes_beyond_its_scratch():
     qa = require_gpu()
     lib = qa.load_library()
-    B, Hq, Hkv, D, L, splits = 64, 64, 8, 128, 32768, 256
+    B, Hq, Hkv, D, L, splits = 1, 64, 8, 128, 131072, 1024
     assert qa.decode_workspace_size(B, Hq, Hkv, D, L, splits) > SCRATCH_BYTES
     fake = 0x10000  # never dereferenced: the size check comes first
     st = qa.KvCacheStruct()
