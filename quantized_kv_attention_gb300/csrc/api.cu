@@ -97,6 +97,43 @@ qattn_status code_map(CUtensorMap *map, const void *base, uint64_t bytes, int he
   return QATTN_OK;
 }
 
+// Decode maps: codes as 3-D [heads][rows_per_head][128 B] (128B swizzle),
+// scales as 2-D [heads][tokens_per_head] fp16; boxes from decode_geometry().
+qattn_status decode_maps(DecodeMaps *m, const KvView &v, int batch) {
+  EncodeFn enc = encode_fn();
+  if (!enc) return fail(QATTN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  const bool paged = v.page_table != nullptr;
+  const DecodeGeometry geo = decode_geometry(v.head_dim, v.hkv, paged);
+  const uint64_t heads = paged ? static_cast<uint64_t>(v.num_pages) * v.hkv : static_cast<uint64_t>(batch) * v.hkv;
+  const uint64_t tokens = paged ? kPage : static_cast<uint64_t>(v.capacity);
+  const uint64_t rows = tokens * v.head_dim / 256;
+  if (heads > 0x7fffffffull || rows > 0x7fffffffull) return fail(QATTN_ERR_UNSUPPORTED, "cache too large");
+  const void *bases[4] = {v.k_codes, v.v_codes, v.k_scales, v.v_scales};
+  CUtensorMap *outs[4] = {&m->k, &m->v, &m->ks, &m->vs};
+  for (int i = 0; i < 4; ++i) {
+    CUresult r;
+    if (i < 2) {
+      cuuint64_t dims[3] = {128, rows, heads};
+      cuuint64_t strides[2] = {128, rows * 128};
+      cuuint32_t box[3] = {128, static_cast<cuuint32_t>(geo.box_rows), static_cast<cuuint32_t>(geo.box_heads)};
+      cuuint32_t es[3] = {1, 1, 1};
+      r = enc(outs[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(bases[i]), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+      cuuint64_t dims[2] = {tokens, heads};
+      cuuint64_t strides[1] = {tokens * 2};
+      cuuint32_t box[2] = {static_cast<cuuint32_t>(geo.box_tokens), static_cast<cuuint32_t>(geo.box_heads)};
+      cuuint32_t es[2] = {1, 1};
+      r = enc(outs[i], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(bases[i]), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
+    if (r != CUDA_SUCCESS) return fail(QATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for decode map %d", (int)r, i);
+  }
+  return QATTN_OK;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Checks shared by every call that reads or writes the cache.
@@ -133,9 +170,11 @@ qattn_status check_cache(const qattn_kv_cache *c, int batch, KvView *v, uint64_t
 }
 
 // Number of balanced key ranges (one persistent CTA each) for a decode call:
-// one per SM by default, never more than there are 64-token stages.
-int plan_ctas(int batch, int hkv, int max_len, int requested, int sms) {
-  const int64_t stages = static_cast<int64_t>(batch) * hkv * ((static_cast<int64_t>(max_len) + kPage - 1) / kPage);
+// one per SM by default, never more than there can be stages.
+int plan_ctas(int batch, int hkv, int head_dim, int max_len, int requested, int sms) {
+  const DecodeGeometry geo = decode_geometry(head_dim, hkv, false);
+  const int64_t stages = static_cast<int64_t>(batch) * geo.groups *
+                         ((static_cast<int64_t>(max_len) + geo.tokens_per_stage - 1) / geo.tokens_per_stage);
   int64_t n = requested > 0 ? requested : sms;
   if (n > stages) n = stages;
   if (n > QATTN_MAX_SPLITS) n = QATTN_MAX_SPLITS;
@@ -143,11 +182,14 @@ int plan_ctas(int batch, int hkv, int max_len, int requested, int sms) {
   return static_cast<int>(n);
 }
 
-// partial_o [2*ctas, G, D] fp32, padded to 256 bytes, then partial_lse [2*ctas, G].
-size_t workspace_bytes(int ctas, int group, int head_dim) {
-  const size_t o = static_cast<size_t>(2) * ctas * group * head_dim * sizeof(float);
-  return (o + 255) / 256 * 256 + static_cast<size_t>(2) * ctas * group * sizeof(float);
+// partial_o [2*ctas, rows, D] fp32, padded to 256 bytes, then partial_lse
+// [2*ctas, rows]; rows = kv-heads per stage * G.
+size_t workspace_bytes(int ctas, int rows, int head_dim) {
+  const size_t o = static_cast<size_t>(2) * ctas * rows * head_dim * sizeof(float);
+  return (o + 255) / 256 * 256 + static_cast<size_t>(2) * ctas * rows * sizeof(float);
 }
+
+bool hkv_supported(int hkv) { return hkv == 1 || hkv == 2 || hkv == 4 || (hkv > 0 && hkv % 8 == 0); }
 
 }  // namespace
 
@@ -184,6 +226,7 @@ size_t qattn_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t n
                                    int32_t head_dim, int32_t max_seq_len, int32_t num_splits) {
   if (batch <= 0 || batch > QATTN_MAX_BATCH || num_q_heads <= 0 || num_kv_heads <= 0 ||
       num_q_heads % num_kv_heads || num_q_heads / num_kv_heads > QATTN_MAX_GROUP || max_seq_len < 0 ||
+      !hkv_supported(num_kv_heads) ||
       num_splits < 0 || num_splits > QATTN_MAX_SPLITS || (head_dim != 64 && head_dim != 128))
     return 0;
   int sms = 152;
@@ -193,8 +236,9 @@ size_t qattn_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t n
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
   }
   cudaGetLastError();
-  const int ctas = plan_ctas(batch, num_kv_heads, max_seq_len, num_splits, sms);
-  return workspace_bytes(ctas, num_q_heads / num_kv_heads, head_dim);
+  const int ctas = plan_ctas(batch, num_kv_heads, head_dim, max_seq_len, num_splits, sms);
+  const DecodeGeometry geo = decode_geometry(head_dim, num_kv_heads, false);
+  return workspace_bytes(ctas, geo.heads_per_stage * (num_q_heads / num_kv_heads), head_dim);
 }
 
 qattn_status qattn_decode(const uint16_t *q, const qattn_kv_cache *cache, const int32_t *seq_lens,
@@ -213,6 +257,8 @@ qattn_status qattn_decode(const uint16_t *q, const qattn_kv_cache *cache, const 
   if (num_q_heads % view.hkv) return fail(QATTN_ERR_INVALID_ARG, "Hq %d is not a multiple of Hkv %d", num_q_heads, view.hkv);
   if (num_q_heads / view.hkv > QATTN_MAX_GROUP)
     return fail(QATTN_ERR_UNSUPPORTED, "group size %d > %d", num_q_heads / view.hkv, QATTN_MAX_GROUP);
+  if (!hkv_supported(view.hkv))
+    return fail(QATTN_ERR_UNSUPPORTED, "num_kv_heads %d (supported: 1, 2, 4 or a multiple of 8)", view.hkv);
   if (batch == 0) return QATTN_OK;
   if (!q || !seq_lens || !out) return fail(QATTN_ERR_INVALID_ARG, "q, seq_lens or out is NULL");
   if (!aligned16(q) || !aligned16(out)) return fail(QATTN_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
@@ -222,23 +268,24 @@ qattn_status qattn_decode(const uint16_t *q, const qattn_kv_cache *cache, const 
   const int64_t stage_limit = view.page_table ? view.max_pages : view.capacity / kPage;
   if (static_cast<int64_t>(batch) * view.hkv * stage_limit >= (int64_t(1) << 31))
     return fail(QATTN_ERR_UNSUPPORTED, "batch * Hkv * cached stages exceeds 2^31");
-  const int ctas = plan_ctas(batch, view.hkv, max_seq_len, num_splits, ds->sms);
-  const size_t need = workspace_bytes(ctas, G, view.head_dim);
+  const int ctas = plan_ctas(batch, view.hkv, view.head_dim, max_seq_len, num_splits, ds->sms);
+  const DecodeGeometry geo = decode_geometry(view.head_dim, view.hkv, view.page_table != nullptr);
+  const int slot_rows = geo.heads_per_stage * G;
+  const size_t need = workspace_bytes(ctas, slot_rows, view.head_dim);
   if (!workspace || workspace_size < need || !aligned16(workspace))
     return fail(QATTN_ERR_WORKSPACE, "workspace of %zu bytes (16-byte aligned) needed, %zu given", need,
                 workspace ? workspace_size : (size_t)0);
-  CUtensorMap kmap, vmap;
-  if ((st = code_map(&kmap, view.k_codes, code_bytes, view.head_dim)) != QATTN_OK) return st;
-  if ((st = code_map(&vmap, view.v_codes, code_bytes, view.head_dim)) != QATTN_OK) return st;
+  DecodeMaps maps;
+  if ((st = decode_maps(&maps, view, batch)) != QATTN_OK) return st;
 
   DecodeArgs a;
   a.q = q, a.seq_lens = seq_lens, a.out = out, a.lse = lse;
   a.partial_o = static_cast<float *>(workspace);
-  const size_t o_bytes = static_cast<size_t>(2) * ctas * G * view.head_dim * sizeof(float);
+  const size_t o_bytes = static_cast<size_t>(2) * ctas * slot_rows * view.head_dim * sizeof(float);
   a.partial_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + (o_bytes + 255) / 256 * 256);
   a.batch = batch, a.hq = num_q_heads, a.ctas = ctas;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
-  cudaError_t e = launch_decode(a, view, kmap, vmap, ds->status, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_decode(a, view, maps, ds->status, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "decode launch");
 }
 

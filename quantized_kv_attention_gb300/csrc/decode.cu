@@ -9,28 +9,33 @@
 // written back as fp16; a quantized tile is 4x smaller, so a deep ring of
 // tiles fits on chip.
 //
-// Work split.  The keys of all (sequence, kv-head) pairs form one list of
-// 64-token stages (pair-major).  A persistent grid of one CTA per SM cuts the
-// list into equal contiguous ranges, so every SM streams the same number of
-// bytes whatever the sequence lengths.  A pair that lies inside one range is
-// finished by its CTA (final fp16 O and lse); a pair cut by range boundaries
-// leaves one fp32 partial per CTA it touches, merged by decode_merge_kernel.
+// Stage.  One pipeline stage holds 256 (token, kv-head) rows: 32 tokens of 8
+// kv-heads (Hkv >= 8, heads in groups of 8) or 256/Hkv tokens of every head
+// (Hkv = 1, 2, 4).  It arrives as four TMA requests -- K codes, V codes, K
+// scales, V scales -- of 16 KB, 16 KB, 512 B and 512 B at D = 128: few large
+// requests are what lets one CTA per SM stream at HBM speed.
+//
+// Work split.  Stages of all (sequence, head-group) segments form one list;
+// a persistent grid of one CTA per SM cuts it into equal contiguous ranges,
+// so every SM streams the same number of bytes whatever the lengths.  A
+// segment inside one range is finished by its CTA (fp16 O and lse); a segment
+// cut by range boundaries leaves one fp32 partial per CTA it touches, merged
+// by decode_merge_kernel (launched as a programmatic dependent).
 //
 // CTA roles.
-//   warp 8      producer: for each stage, two 2-D TMA loads of the K/V codes
-//               (128-byte rows, 128B swizzle) and two bulk copies of the K/V
-//               scales into a 16-deep mbarrier ring.
-//   warps 0-7   consumers: warp w takes 32 tokens (half) of every fourth stage.
-//     S^T (16 tokens x 8 heads) = codes_K . Q^T on mma.sync m16n8k16, tokens on
-//       M.  Each nibble becomes an fp16 subnormal u * 2^-24 with u = c + 8 in
-//       one LOP3 (the high nibble of a byte gives 16 u * 2^-24; Q carries the
-//       1/16 for those columns), so S = 2^24 * acc - 8 * sum(q) exactly.
-//     online softmax in the log2 domain, per-token K scale in fp32, one max
+//   warp 8      producer: one elected thread issues the stage's TMA loads
+//               into a 5-deep mbarrier ring.
+//   warps 0-7   consumers: warp w owns kv-head w / (8 / HB) of the group and
+//               32 tokens of it per stage (HB = heads per stage).
+//     S^T (16 tokens x 8 q-heads) = codes_K . Q^T on mma.sync m16n8k16 with
+//       tokens on M.  A nibble becomes the fp16 subnormal u * 2^-24,
+//       u = code + 8, in one LOP3 (a high nibble gives 16 u * 2^-24 and Q
+//       carries 1/16 for those columns); S = 2^24 acc - 8 sum(q), exact.
+//     online softmax in the log2 domain, K scale per token in fp32, one max
 //       reduction per 32 tokens, warp-uniform rescale when the max grows.
-//     P' = P * s_V[token] in fp16, moved into the B-operand layout by movmatrix.
-//     O^T (D x 8 heads) += V codes^T . P'^T, the V codes transposed by
-//       ldmatrix.trans and decoded the same way; O = 2^24 / f * acc - 8 * sum(P').
-//   Segment end: the eight consumer warps merge (m, l, O) in shared memory.
+//     P' = P * s_V[token] in fp16, moved to the B-operand layout by movmatrix.
+//     O^T (D x 8 q-heads) += V codes^T . P'^T, V transposed by ldmatrix.trans
+//       and decoded the same way; O = 2^24 / f acc - 8 sum(P').
 #include <math.h>
 
 #include "../../include/qattn.h"
@@ -41,30 +46,27 @@ namespace qattn {
 namespace {
 
 constexpr int kConsumerWarps = 8;
-constexpr int kWarpsPerStage = 2;                           // 32 tokens each
-constexpr int kGroups = kConsumerWarps / kWarpsPerStage;    // stage it goes to group it % 4
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kStages = 16;                                 // multiple of kGroups
+constexpr int kRowsPerStage = 256;  // (token, kv-head) rows per stage
 constexpr float kTwo24 = 16777216.0f;
-static_assert(kStages % kGroups == 0, "each group owns fixed ring slots");
 
 template <int D>
 struct Cfg {
-  static constexpr int kCodeBytes = kPage * D / 2;  // per tensor per stage
-  static constexpr int kStageBytes = (2 * kCodeBytes + 4 * kPage + 1023) / 1024 * 1024;
-  static constexpr int kKBytes = D / 8;             // K code bytes per lane per token
-  static constexpr int kWords = kKBytes / 4;
-  static constexpr int kMt = D / 16;                // m-tiles of O^T, k-steps of S
+  static constexpr int kCodeBytes = kRowsPerStage * D / 2;  // per tensor per stage
+  static constexpr int kScaleBytes = kRowsPerStage * 2;
+  static constexpr int kStageBytes = (2 * kCodeBytes + 2 * kScaleBytes + 1023) / 1024 * 1024;
+  static constexpr int kStages = D == 128 ? 5 : 8;
   static constexpr int kRing = kStages * kStageBytes;
+  static constexpr int kKBytes = D / 8;  // K code bytes per lane per token
+  static constexpr int kWords = kKBytes / 4;
+  static constexpr int kMt = D / 16;     // m-tiles of O^T, k-steps of S
 };
 
-// Dynamic shared memory: ring | merge (O per warp and head) | m, l | prefix | barriers.
-template <int D>
-__host__ __device__ constexpr int merge_bytes(int G) { return kConsumerWarps * G * D * 4; }
+// Dynamic shared memory: ring | merge (O per warp, q-head) | m, l | prefix | barriers, flags.
 template <int D>
 __host__ __device__ constexpr int smem_bytes(int G, int batch) {
-  return Cfg<D>::kRing + merge_bytes<D>(G) + 2 * kConsumerWarps * 8 * 4 + (batch + 1) * 4 +
-         2 * kStages * 8 + kStages * 4 + 8 + 1024;
+  return Cfg<D>::kRing + kConsumerWarps * G * D * 4 + 2 * kConsumerWarps * 8 * 4 + (batch + 1) * 4 +
+         2 * Cfg<D>::kStages * 8 + Cfg<D>::kStages * 4 + 16 + 1024;
 }
 
 __device__ __forceinline__ void consumer_sync() {
@@ -73,7 +75,7 @@ __device__ __forceinline__ void consumer_sync() {
 
 // Nibbles -> fp16 subnormals: out[k] = (u_lo, u_hi) * 2^-24 for nibble k of
 // each 16-bit half, u = code + 8 (the XOR maps two's complement to offset
-// binary); odd k come out 16x larger (nibble sits four bits higher).
+// binary); odd k come out 16x larger (the nibble sits four bits higher).
 __device__ __forceinline__ void decode_sub(uint32_t w, uint32_t (&out)[4]) {
   const uint32_t w8 = w >> 8;
   out[0] = lop3_and_xor(w, 0x000F000Fu, 0x00080008u);
@@ -83,39 +85,66 @@ __device__ __forceinline__ void decode_sub(uint32_t w, uint32_t (&out)[4]) {
 }
 
 // Range of the flattened stage list owned by CTA i of n: [i*T/n, (i+1)*T/n).
-__device__ __forceinline__ int64_t range_start(int64_t i, int64_t T, int64_t n) { return i * T / n; }
+__host__ __device__ __forceinline__ int64_t range_start(int64_t i, int64_t T, int64_t n) {
+  return i * T / n;
+}
 // CTA owning global stage gs (inverse of range_start).
 __host__ __device__ __forceinline__ int64_t owner_cta(int64_t gs, int64_t T, int64_t n) {
   return ((gs + 1) * n + T - 1) / T - 1;
 }
 
 struct Loc {
-  int b, kvh, s, n;  // sequence, kv-head, stage within the pair, stages of the pair
+  int b, hg, s, n;  // sequence, head group, stage within the segment, stages of the segment
 };
 
-// prefix[b] = Hkv * (stages of sequences 0..b-1); locate the pair of stage gs.
-__device__ __forceinline__ Loc locate(int64_t gs, const int *prefix, int batch, int hkv) {
-  int lo = 0, hi = batch - 1;  // largest b with prefix[b] <= gs (and a non-empty b)
+// prefix[b] = groups * (stages of sequences 0..b-1); locate the segment of gs.
+__device__ __forceinline__ Loc locate(int64_t gs, const int *prefix, int batch, int groups) {
+  int lo = 0, hi = batch - 1;  // largest b with prefix[b] <= gs: always a non-empty sequence
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
     if (prefix[mid] <= gs) lo = mid; else hi = mid - 1;
   }
   Loc l;
   l.b = lo;
-  l.n = (prefix[lo + 1] - prefix[lo]) / hkv;
+  l.n = (prefix[lo + 1] - prefix[lo]) / groups;
   const int r = static_cast<int>(gs - prefix[lo]);
-  l.kvh = r / l.n;
-  l.s = r - l.kvh * l.n;
+  l.hg = r / l.n;
+  l.s = r - l.hg * l.n;
   return l;
 }
 
+// Geometry of one stage, from the number of kv-heads HB it carries.
+struct StageGeo {
+  int hb;      // kv-heads per stage (8, 4, 2 or 1)
+  int tokens;  // tokens per head per stage = 256 / hb
+  int groups;  // head groups = Hkv / hb
+  int wph;     // consumer warps per head = 8 / hb
+};
+__host__ __device__ __forceinline__ StageGeo stage_geo(int hkv) {
+  StageGeo g;
+  g.hb = hkv >= 8 ? 8 : hkv;
+  g.tokens = kRowsPerStage / g.hb;
+  g.groups = hkv / g.hb;
+  g.wph = kConsumerWarps / g.hb;
+  return g;
+}
+
+// Tensor maps of one cache (built on the host, passed by value):
+//   codes  3-D [heads_total][rows_per_head][128 B]; box [box_heads][box_rows][128 B], 128B swizzle
+//   scales 2-D [heads_total][tokens_per_head] fp16; box [box_heads][box_tokens]
+// heads_total = B*Hkv (contiguous) or P*Hkv (paged); a paged stage of more
+// than one page is loaded page by page and head by head (box_heads = 1).
+struct Maps {
+  CUtensorMap k, v, ks, vs;
+};
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_kernel(DecodeArgs a, KvView cache, const __grid_constant__ CUtensorMap kmap,
-                  const __grid_constant__ CUtensorMap vmap, uint32_t *err) {
+    decode_kernel(DecodeArgs a, KvView cache, const __grid_constant__ Maps maps, uint32_t *err) {
   using C = Cfg<D>;
   const int G = a.hq / cache.hkv;
   const int B = a.batch, hkv = cache.hkv;
+  const StageGeo geo = stage_geo(hkv);
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -125,32 +154,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   int *prefix = reinterpret_cast<int *>(sml + kConsumerWarps * 8);    // [B + 1]
   uint64_t *full = reinterpret_cast<uint64_t *>(
       (reinterpret_cast<uintptr_t>(prefix + B + 1) + 7) & ~static_cast<uintptr_t>(7));
-  uint64_t *empty = full + kStages;
-  int *valid = reinterpret_cast<int *>(empty + kStages);  // [kStages]: 0 = missing page
-  volatile int *abort_flag = valid + kStages;               // set after a timed-out wait
+  uint64_t *empty = full + C::kStages;
+  int *valid = reinterpret_cast<int *>(empty + C::kStages);          // [kStages]: 0 = missing page
+  volatile int *abort_flag = valid + C::kStages;                     // set after a timed-out wait
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool paged = cache.page_table != nullptr;
   const int64_t limit = paged ? static_cast<int64_t>(cache.max_pages) * kPage : cache.capacity;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < C::kStages; ++s) {
       mbar_init(smem_u32(full + s), 1);
-      mbar_init(smem_u32(empty + s), kWarpsPerStage);
+      mbar_init(smem_u32(empty + s), kConsumerWarps);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
-  pdl_wait();  // inputs may come from the preceding kernel on the stream
+  pdl_wait();                // inputs may come from the preceding kernel on the stream
+  pdl_launch_dependents();   // the merge kernel may be scheduled as SMs free up
 
-  // prefix[b]: first global stage of sequence b (all its kv-heads, pair-major)
+  // prefix[b]: first global stage of sequence b (all its head groups)
   for (int b = threadIdx.x; b < B; b += kThreads) {
     int len = __ldg(a.seq_lens + b);
     if (len > limit) {
       len = static_cast<int>(limit);
       atomicOr(err, kFlagBadPage);
     }
-    prefix[b + 1] = len > 0 ? hkv * ((len + kPage - 1) / kPage) : 0;
+    prefix[b + 1] = len > 0 ? geo.groups * ((len + geo.tokens - 1) / geo.tokens) : 0;
   }
   __syncthreads();
   if (warp == 0) {
@@ -172,52 +202,79 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t T = prefix[B];
   const int64_t gs0 = range_start(blockIdx.x, T, gridDim.x);
   const int64_t gs1 = range_start(blockIdx.x + 1, T, gridDim.x);
-  const int nst = static_cast<int>(gs1 - gs0);
-  if (nst <= 0) return;
+  if (gs1 <= gs0) return;
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      prefetch_tmap(&kmap);
-      prefetch_tmap(&vmap);
+      prefetch_tmap(&maps.k);
+      prefetch_tmap(&maps.v);
+      prefetch_tmap(&maps.ks);
+      prefetch_tmap(&maps.vs);
+      const int rows_per_tok = D / 2;  // code bytes per token
       int it = 0;
       for (int64_t gs = gs0; gs < gs1;) {
-        const Loc l = locate(gs, prefix, B, hkv);
+        const Loc l = locate(gs, prefix, B, geo.groups);
         const int cnt = static_cast<int>(min(static_cast<int64_t>(l.n - l.s), gs1 - gs));
         for (int j = 0; j < cnt; ++j, ++it) {
-          const int s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1;
-          if (it >= kStages &&
+          const int s = it % C::kStages;
+          const uint32_t ph = (it / C::kStages) & 1;
+          if (it >= C::kStages &&
               !mbar_wait(smem_u32(empty + s), ph ^ 1, err, *abort_flag ? kDrainCycles : kWaitCycles)) {
             *abort_flag = 1;  // stop issuing; the consumers drain with short waits
             return;
           }
-          const int stage = l.s + j;
-          int64_t row_tok;
-          bool ok = true;
-          if (paged) {
-            const int page =
-                __ldg(cache.page_table + static_cast<int64_t>(l.b) * cache.max_pages + stage);
-            ok = page >= 0 && page < cache.num_pages;
-            if (!ok) atomicOr(err, kFlagBadPage);
-            row_tok = (static_cast<int64_t>(ok ? page : 0) * hkv + l.kvh) * kPage;
-          } else {
-            row_tok = (static_cast<int64_t>(l.b) * hkv + l.kvh) * cache.capacity +
-                      static_cast<int64_t>(stage) * kPage;
-          }
+          const int tok0 = (l.s + j) * geo.tokens;  // first token of the stage in the sequence
           const uint32_t full_s = smem_u32(full + s);
-          valid[s] = ok;
-          if (ok) {
-            uint8_t *st = smem + s * C::kStageBytes;
-            const int row128 = static_cast<int>(row_tok * (D / 2) / 128);
-            mbar_arrive_expect_tx(full_s, 2 * C::kCodeBytes + 4 * kPage);
-            tma_load_2d(smem_u32(st), &kmap, 0, row128, full_s);
-            tma_load_2d(smem_u32(st + C::kCodeBytes), &vmap, 0, row128, full_s);
-            bulk_g2s(smem_u32(st + 2 * C::kCodeBytes), cache.k_scales + row_tok, 2 * kPage, full_s);
-            bulk_g2s(smem_u32(st + 2 * C::kCodeBytes + 2 * kPage), cache.v_scales + row_tok,
-                     2 * kPage, full_s);
+          const uint32_t st = smem_u32(smem + s * C::kStageBytes);
+          const uint32_t stv = st + C::kCodeBytes, sks = st + 2 * C::kCodeBytes, svs = sks + C::kScaleBytes;
+          const int head_base = l.hg * geo.hb;
+          if (!paged) {
+            const int head0 = l.b * hkv + head_base;
+            const int row0 = tok0 * rows_per_tok / 128;
+            valid[s] = 1;
+            mbar_arrive_expect_tx(full_s, 2 * C::kCodeBytes + 2 * C::kScaleBytes);
+            tma_load_3d(st, &maps.k, 0, row0, head0, full_s);
+            tma_load_3d(stv, &maps.v, 0, row0, head0, full_s);
+            tma_load_2d(sks, &maps.ks, tok0, head0, full_s);
+            tma_load_2d(svs, &maps.vs, tok0, head0, full_s);
           } else {
-            mbar_arrive(full_s);  // a missing page: its tokens are masked
+            const int npages = geo.tokens > kPage ? geo.tokens / kPage : 1;
+            bool ok = true;
+            for (int pi = 0; pi < npages; ++pi) {
+              const int page = __ldg(cache.page_table + static_cast<int64_t>(l.b) * cache.max_pages +
+                                     (tok0 + pi * kPage) / kPage);
+              ok = ok && page >= 0 && page < cache.num_pages;
+            }
+            valid[s] = ok;
+            if (!ok) {
+              atomicOr(err, kFlagBadPage);
+              mbar_arrive(full_s);  // a missing page: the stage's tokens are masked
+              continue;
+            }
+            mbar_arrive_expect_tx(full_s, 2 * C::kCodeBytes + 2 * C::kScaleBytes);
+            for (int pi = 0; pi < npages; ++pi) {
+              const int ptok = tok0 + pi * kPage;
+              const int page = __ldg(cache.page_table + static_cast<int64_t>(l.b) * cache.max_pages + ptok / kPage);
+              const int inner = ptok % kPage;  // token offset inside the page
+              if (npages == 1) {               // every head of the stage in one box
+                const int head0 = page * hkv + head_base;
+                tma_load_3d(st, &maps.k, 0, inner * rows_per_tok / 128, head0, full_s);
+                tma_load_3d(stv, &maps.v, 0, inner * rows_per_tok / 128, head0, full_s);
+                tma_load_2d(sks, &maps.ks, inner, head0, full_s);
+                tma_load_2d(svs, &maps.vs, inner, head0, full_s);
+              } else {                         // one page of one head per box
+                for (int h = 0; h < geo.hb; ++h) {
+                  const int head = page * hkv + head_base + h;
+                  const uint32_t cofs = (h * geo.tokens + pi * kPage) * rows_per_tok;
+                  const uint32_t sofs = (h * geo.tokens + pi * kPage) * 2;
+                  tma_load_3d(st + cofs, &maps.k, 0, 0, head, full_s);
+                  tma_load_3d(stv + cofs, &maps.v, 0, 0, head, full_s);
+                  tma_load_2d(sks + sofs, &maps.ks, 0, head, full_s);
+                  tma_load_2d(svs + sofs, &maps.vs, 0, head, full_s);
+                }
+              }
+            }
           }
         }
         gs += cnt;
@@ -228,27 +285,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // -------------------------------------------------------------- consumers
   const int g = lane >> 2, c = lane & 3;
-  const int grp = warp / kWarpsPerStage, sub = warp % kWarpsPerStage;
-  const float kf = a.scale_log2 * kTwo24;  // folds the 2^-24 of the subnormal codes
-  int it = 0;                              // CTA-local stage index, as in the producer
+  const int hbw = warp / geo.wph;              // this warp's kv-head within the stage
+  const int tok_w = (warp % geo.wph) * 32;     // its 32 tokens within that head's stage tokens
+  const int kofs = hbw * geo.tokens * (D / 2); // byte offset of the head's codes in a stage
+  const int sofs = hbw * geo.tokens;           // element offset of the head's scales
+  const float kf = a.scale_log2 * kTwo24;      // folds the 2^-24 of the subnormal codes
+  int it = 0;                                  // CTA-local stage index, as in the producer
   for (int64_t gs = gs0; gs < gs1;) {
-    const Loc l = locate(gs, prefix, B, hkv);
+    const Loc l = locate(gs, prefix, B, geo.groups);
     const int cnt = static_cast<int>(min(static_cast<int64_t>(l.n - l.s), gs1 - gs));
     const int len = static_cast<int>(min(static_cast<int64_t>(__ldg(a.seq_lens + l.b)), limit));
+    const int kvh = l.hg * geo.hb + hbw;
 
-    // Q of head g as the B operand.  Lane c covers d = c*D/4 + 8i + {0..7}
-    // (word i of its K code bytes); the decoder pairs (e, e+4) and nibble
+    // Q of q-head g as the B operand.  Lane c covers d = c*D/4 + 8i + {0..7}
+    // (word i of its K code bytes); the decoder pairs (e, e+4), and nibble
     // positions 1 and 3 come out 16x larger, so those columns carry q / 16.
     uint32_t qb[C::kMt][2];
     float qsum = 0.f;
     {
       const int dbase = c * (D / 4);
       const uint4 *qv = reinterpret_cast<const uint4 *>(
-          a.q + (static_cast<int64_t>(l.b) * a.hq + l.kvh * G + min(g, G - 1)) * D + dbase);
+          a.q + (static_cast<int64_t>(l.b) * a.hq + kvh * G + min(g, G - 1)) * D + dbase);
       const __half2 sixteenth = __float2half2_rn(0.0625f);
 #pragma unroll
       for (int i = 0; i < C::kWords; ++i) {
-        uint4 u = g < G ? __ldg(qv + i) : make_uint4(0, 0, 0, 0);
+        const uint4 u = g < G ? __ldg(qv + i) : make_uint4(0, 0, 0, 0);
         const uint32_t p0 = __byte_perm(u.x, u.z, 0x5410), p1 = __byte_perm(u.x, u.z, 0x7632);
         const uint32_t p2 = __byte_perm(u.y, u.w, 0x5410), p3 = __byte_perm(u.y, u.w, 0x7632);
         __half2 h1 = __hmul2(*reinterpret_cast<const __half2 *>(&p1), sixteenth);
@@ -266,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
     qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
-    // raw-unit bias 8 * sum(q) * 2^-24 for the thread's heads 2c and 2c+1
+    // raw-unit bias 8 * sum(q) * 2^-24 for the lane's q-heads 2c and 2c+1
     const float bq0 = 8.f / kTwo24 * __shfl_sync(0xffffffffu, qsum, (2 * c) << 2);
     const float bq1 = 8.f / kTwo24 * __shfl_sync(0xffffffffu, qsum, (2 * c + 1) << 2);
 
@@ -276,17 +337,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int mt = 0; mt < C::kMt; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
     for (int j = 0; j < cnt; ++j, ++it) {
-      if (it % kGroups != grp) continue;
-      const int s = it % kStages;
-      const uint32_t ph = (it / kStages) & 1;
+      const int s = it % C::kStages;
+      const uint32_t ph = (it / C::kStages) & 1;
       const bool got = mbar_wait(smem_u32(full + s), ph, err, *abort_flag ? kDrainCycles : kWaitCycles);
       if (!got) *abort_flag = 1;
-      const int nvalid = min(kPage, len - (l.s + j) * kPage) - sub * 32;
+      const int nvalid = len - (l.s + j) * geo.tokens - tok_w;
       if (got && valid[s] && nvalid > 0) {
         const uint32_t kb = smem_u32(smem + s * C::kStageBytes);
         const uint32_t vb = kb + C::kCodeBytes;
-        const __half *sks = reinterpret_cast<const __half *>(smem + s * C::kStageBytes + 2 * C::kCodeBytes);
-        const __half *svs = sks + kPage;
+        const __half *sks = reinterpret_cast<const __half *>(smem + s * C::kStageBytes + 2 * C::kCodeBytes) + sofs;
+        const __half *svs = sks + kRowsPerStage;
 
         // S^T for two 16-token tiles (independent MMA chains)
         float sacc[2][4];
@@ -294,10 +354,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           sacc[t][0] = sacc[t][1] = sacc[t][2] = sacc[t][3] = 0.f;
-          const int lt = sub * 32 + t * 16 + g;
+          const int lt = tok_w + t * 16 + g;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const uint32_t addr = kb + swz128((lt + 8 * h) * (D / 2) + c * C::kKBytes);
+            const uint32_t addr = kb + swz128(kofs + (lt + 8 * h) * (D / 2) + c * C::kKBytes);
             if constexpr (C::kWords == 4) {
               const uint4 u = lds128(addr);
               kw[t][h][0] = u.x, kw[t][h][1] = u.y, kw[t][h][2] = u.z, kw[t][h][3] = u.w;
@@ -321,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float ts[2][4], fv[2][2];
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          const int lt = sub * 32 + t * 16 + g;
+          const int lt = tok_w + t * 16 + g;
           const bool v0 = t * 16 + g < nvalid, v1 = t * 16 + g + 8 < nvalid;
           const float f0 = __half2float(sks[lt]) * kf, f1 = __half2float(sks[lt + 8]) * kf;
           ts[t][0] = v0 ? (sacc[t][0] - bq0) * f0 : -INFINITY;
@@ -371,9 +431,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int jp = 0; jp < D / 64; ++jp) {
             const int q = lane >> 3;
-            const int vt = sub * 32 + t * 16 + ((q & 2) ? 8 : 0) + (lane & 7);
+            const int vt = tok_w + t * 16 + ((q & 2) ? 8 : 0) + (lane & 7);
             uint32_t r0, r1, r2, r3;
-            ldsm_x4_trans(vb + swz128(vt * (D / 2) + (2 * jp + (q & 1)) * 16), r0, r1, r2, r3);
+            ldsm_x4_trans(vb + swz128(kofs + vt * (D / 2) + (2 * jp + (q & 1)) * 16), r0, r1, r2, r3);
             uint32_t d0[4], d1[4], d2[4], d3[4];
             decode_sub(r0, d0);
             decode_sub(r1, d1);
@@ -421,27 +481,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     consumer_sync();
     const bool complete = l.s == 0 && cnt == l.n;
     const int64_t slot = l.s > 0 ? 2 * static_cast<int64_t>(blockIdx.x) : 2 * static_cast<int64_t>(blockIdx.x) + 1;
-    for (int idx = threadIdx.x; idx < G * D; idx += kConsumerWarps * 32) {
-      const int h = idx / D, d = idx - h * D;
-      float M = smm[h];
-#pragma unroll
-      for (int w = 1; w < kConsumerWarps; ++w) M = fmaxf(M, smm[w * 8 + h]);
+    for (int idx = threadIdx.x; idx < geo.hb * G * D; idx += kConsumerWarps * 32) {
+      const int hh = idx / (G * D), rem = idx - hh * G * D;  // kv-head in stage, q-head, d
+      const int h = rem / D, d = rem - h * D;
+      const int w0 = hh * geo.wph;
+      float M = smm[w0 * 8 + h];
+      for (int w = 1; w < geo.wph; ++w) M = fmaxf(M, smm[(w0 + w) * 8 + h]);
       float L = 0.f, acc = 0.f;
-#pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float sc = ex2(smm[w * 8 + h] - M);
-        L += sc * sml[w * 8 + h];
-        acc += sc * smo[(w * G + h) * D + d];
+      for (int w = 0; w < geo.wph; ++w) {
+        const float sc = ex2(smm[(w0 + w) * 8 + h] - M);
+        L += sc * sml[(w0 + w) * 8 + h];
+        acc += sc * smo[((w0 + w) * G + h) * D + d];
       }
       const bool live = L > 0.f;
       const float ov = live ? acc / L : 0.f;
       const float lse_v = live ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
       if (complete) {
-        const int64_t row = static_cast<int64_t>(l.b) * a.hq + l.kvh * G + h;
+        const int64_t row = static_cast<int64_t>(l.b) * a.hq + (l.hg * geo.hb + hh) * G + h;
         a.out[row * D + d] = __half_as_ushort(__float2half_rn(ov));
         if (d == 0 && a.lse) a.lse[row] = lse_v;
       } else {
-        const int64_t prow = slot * G + h;
+        const int64_t prow = slot * geo.hb * G + hh * G + h;
         a.partial_o[prow * D + d] = ov;
         if (d == 0) a.partial_lse[prow] = lse_v;
       }
@@ -451,10 +511,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// Merges the partials of every (sequence, kv-head) pair that the balanced
-// ranges cut: pair p spanning CTAs c0 < c1 has partials in slot 2*c0 + 1
-// (its start, in c0's last segment) and slots 2*c for c0 < c <= c1.  Pairs of
-// empty sequences get O = 0, lse = -inf.  One CTA per pair, warp h per head.
+// Merges the partials of every (sequence, head-group) segment that the
+// balanced ranges cut: a segment spanning CTAs c0 < c1 has partials in slot
+// 2*c0 + 1 (its start, in c0's last segment) and slots 2*c for c0 < c <= c1
+// whose range is not empty.  Segments of empty sequences get O = 0 and
+// lse = -inf.  Grid (segments, row blocks of 8); warp w merges one row.
 template <int D>
 __global__ void __launch_bounds__(256)
     decode_merge_kernel(const int32_t *__restrict__ seq_lens, int batch, int hkv, int G, int ctas,
@@ -464,11 +525,12 @@ __global__ void __launch_bounds__(256)
   __shared__ float wsh[8][QATTN_MAX_SPLITS + 1];
   __shared__ int red[2][8];
   pdl_wait();
-  const int b = blockIdx.x / hkv, kvh = blockIdx.x % hkv;
+  const StageGeo geo = stage_geo(hkv);
+  const int b = blockIdx.x / geo.groups, hg = blockIdx.x % geo.groups;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto stages = [&](int bb) {
     const int64_t len = min(static_cast<int64_t>(__ldg(seq_lens + bb)), limit);
-    return len > 0 ? static_cast<int>((len + kPage - 1) / kPage) : 0;
+    return len > 0 ? static_cast<int>((len + geo.tokens - 1) / geo.tokens) : 0;
   };
   int tot = 0, pre = 0;
   for (int bb = threadIdx.x; bb < batch; bb += 256) {
@@ -485,17 +547,19 @@ __global__ void __launch_bounds__(256)
   __syncthreads();
   tot = pre = 0;
   for (int w = 0; w < 8; ++w) tot += red[0][w], pre += red[1][w];
-  const int n = stages(b);
+  const int rows = geo.hb * G;
+  const int r = blockIdx.y * 8 + warp;  // row within the segment: kv-head r / G, q-head r % G
+  if (r >= rows) return;
   const int64_t hq = static_cast<int64_t>(hkv) * G;
-  if (warp >= G) return;
-  const int64_t row = static_cast<int64_t>(b) * hq + kvh * G + warp;
+  const int64_t row = static_cast<int64_t>(b) * hq + static_cast<int64_t>(hg) * rows + r;
+  const int n = stages(b);
   if (n == 0) {
     for (int d = lane; d < D; d += 32) out[row * D + d] = 0;
     if (lane == 0 && lse) lse[row] = -INFINITY;
     return;
   }
-  const int64_t T = static_cast<int64_t>(hkv) * tot;
-  const int64_t first = static_cast<int64_t>(hkv) * pre + static_cast<int64_t>(kvh) * n;
+  const int64_t T = static_cast<int64_t>(geo.groups) * tot;
+  const int64_t first = static_cast<int64_t>(geo.groups) * pre + static_cast<int64_t>(hg) * n;
   const int64_t c0 = owner_cta(first, T, ctas), c1 = owner_cta(first + n - 1, T, ctas);
   if (c0 == c1) return;  // finished inside one CTA
   const int np = static_cast<int>(c1 - c0 + 1);
@@ -503,16 +567,16 @@ __global__ void __launch_bounds__(256)
   // CTAs between c0 and c1 whose range is empty (more CTAs than stages) wrote nothing
   auto used = [&](int k) {
     const int64_t c = c0 + k;
-    return k == 0 || c * T / ctas < (c + 1) * T / ctas;
+    return k == 0 || range_start(c, T, ctas) < range_start(c + 1, T, ctas);
   };
   float M = -INFINITY;
   for (int k = lane; k < np; k += 32)
-    if (used(k)) M = fmaxf(M, pl[slot_of(k) * G + warp]);
+    if (used(k)) M = fmaxf(M, pl[slot_of(k) * rows + r]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float z = 0.f;
   for (int k = lane; k < np; k += 32) {
-    const float lv = used(k) ? pl[slot_of(k) * G + warp] : -INFINITY;
+    const float lv = used(k) ? pl[slot_of(k) * rows + r] : -INFINITY;
     const float e = lv == -INFINITY ? 0.f : expf(lv - M);
     wsh[warp][k] = e;
     z += e;
@@ -523,10 +587,11 @@ __global__ void __launch_bounds__(256)
   float acc[VPL];
 #pragma unroll
   for (int j = 0; j < VPL; ++j) acc[j] = 0.f;
+#pragma unroll 4
   for (int k = 0; k < np; ++k) {
     const float wk = wsh[warp][k];
     if (wk > 0.f) {
-      const float *src = po + (slot_of(k) * G + warp) * D + lane * VPL;
+      const float *src = po + (slot_of(k) * rows + r) * D + lane * VPL;
       if constexpr (VPL == 4) {
         const float4 x = __ldg(reinterpret_cast<const float4 *>(src));
         acc[0] += wk * x.x, acc[1] += wk * x.y, acc[2] += wk * x.z, acc[3] += wk * x.w;
@@ -551,8 +616,8 @@ cudaLaunchAttribute pdl_attr() {
 }
 
 template <int D>
-cudaError_t launch_d(const DecodeArgs &a, const KvView &cache, const CUtensorMap &kmap,
-                     const CUtensorMap &vmap, uint32_t *err, cudaStream_t stream) {
+cudaError_t launch_d(const DecodeArgs &a, const KvView &cache, const DecodeMaps &dm, uint32_t *err,
+                     cudaStream_t stream) {
   static bool configured = false;  // per-function attribute, set once per process
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -561,6 +626,9 @@ cudaError_t launch_d(const DecodeArgs &a, const KvView &cache, const CUtensorMap
     configured = true;
   }
   const int G = a.hq / cache.hkv;
+  const StageGeo geo = stage_geo(cache.hkv);
+  Maps maps;
+  maps.k = dm.k, maps.v = dm.v, maps.ks = dm.ks, maps.vs = dm.vs;
   cudaLaunchAttribute attr[1] = {pdl_attr()};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.ctas);
@@ -569,11 +637,11 @@ cudaError_t launch_d(const DecodeArgs &a, const KvView &cache, const CUtensorMap
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<D>, a, cache, kmap, vmap, err);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<D>, a, cache, maps, err);
   if (e != cudaSuccess) return e;
   const int64_t limit = cache.page_table ? static_cast<int64_t>(cache.max_pages) * kPage : cache.capacity;
   cudaLaunchConfig_t mc = {};
-  mc.gridDim = dim3(a.batch * cache.hkv);
+  mc.gridDim = dim3(a.batch * geo.groups, (geo.hb * G + 7) / 8);
   mc.blockDim = dim3(256);
   mc.stream = stream;
   mc.attrs = attr;
@@ -585,15 +653,28 @@ cudaError_t launch_d(const DecodeArgs &a, const KvView &cache, const CUtensorMap
 
 }  // namespace
 
+DecodeGeometry decode_geometry(int head_dim, int hkv, bool paged) {
+  const StageGeo g = stage_geo(hkv);
+  DecodeGeometry r;
+  r.heads_per_stage = g.hb;
+  r.tokens_per_stage = g.tokens;
+  r.groups = g.groups;
+  const bool split_pages = paged && g.tokens > kPage;
+  r.box_heads = split_pages ? 1 : g.hb;
+  r.box_tokens = paged ? (g.tokens > kPage ? kPage : g.tokens) : g.tokens;
+  r.box_rows = r.box_tokens * head_dim / 256;
+  return r;
+}
+
 int decode_smem_bytes(int head_dim, int group, int batch) {
   return head_dim == 128 ? smem_bytes<128>(group, batch) : smem_bytes<64>(group, batch);
 }
 
-cudaError_t launch_decode(const DecodeArgs &a, const KvView &cache, const CUtensorMap &kmap,
-                          const CUtensorMap &vmap, uint32_t *err, cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeArgs &a, const KvView &cache, const DecodeMaps &maps, uint32_t *err,
+                          cudaStream_t stream) {
   if (a.batch == 0 || a.ctas <= 0) return cudaSuccess;
-  return cache.head_dim == 128 ? launch_d<128>(a, cache, kmap, vmap, err, stream)
-                               : launch_d<64>(a, cache, kmap, vmap, err, stream);
+  return cache.head_dim == 128 ? launch_d<128>(a, cache, maps, err, stream)
+                               : launch_d<64>(a, cache, maps, err, stream);
 }
 
 }  // namespace qattn

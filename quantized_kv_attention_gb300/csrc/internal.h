@@ -29,8 +29,10 @@ cudaError_t launch_quantize(const void *k, const void *v, bool fp16_in, int batc
                             cudaStream_t stream);
 
 // decode.cu: persistent split-KV decode over `ctas` balanced key ranges plus
-// the merge of pairs the ranges cut.  Workspace: partial_o [2*ctas, G, D] and
-// partial_lse [2*ctas, G] fp32 (two slots per CTA).
+// the merge of segments the ranges cut.  A stage carries 256 (token, kv-head)
+// rows: tokens_per_stage tokens of heads_per_stage kv-heads.  Workspace:
+// partial_o [2*ctas, heads_per_stage*G, D] and partial_lse [2*ctas,
+// heads_per_stage*G] fp32 (two slots per CTA).
 struct DecodeArgs {
   const uint16_t *q;
   const int32_t *seq_lens;
@@ -41,9 +43,17 @@ struct DecodeArgs {
   int batch, hq, ctas;
   float scale_log2;  // softmax_scale * log2(e)
 };
+struct DecodeGeometry {
+  int heads_per_stage, tokens_per_stage, groups;
+  int box_heads, box_tokens, box_rows;  // TMA boxes of codes (rows of 128 B) and scales
+};
+DecodeGeometry decode_geometry(int head_dim, int hkv, bool paged);
+struct DecodeMaps {
+  CUtensorMap k, v, ks, vs;  // codes 3-D [heads][rows][128 B], scales 2-D [heads][tokens]
+};
 int decode_smem_bytes(int head_dim, int group, int batch);
-cudaError_t launch_decode(const DecodeArgs &a, const KvView &cache, const CUtensorMap &kmap,
-                          const CUtensorMap &vmap, uint32_t *err, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs &a, const KvView &cache, const DecodeMaps &maps, uint32_t *err,
+                          cudaStream_t stream);
 
 // combine.cu (pdl: launched as a programmatic dependent of the previous kernel)
 cudaError_t launch_combine(const float *partial_o, const float *partial_lse, int splits,

@@ -94,13 +94,18 @@ def test_quantize_and_combine_reject_bad_arguments():
 
 
 def test_workspace_size_host_arithmetic():
-    # explicit range counts need no device: two partial slots per range,
-    # partial_o [2 * ranges, G, D] fp32 padded to 256 bytes, then partial_lse [2 * ranges, G]
-    assert qa.decode_workspace_size(2, 8, 2, 128, 1000, 4) == 2 * 4 * 4 * 128 * 4 + 2 * 4 * 4 * 4
-    # ranges are capped by the number of 64-token stages: 1 * 1 * ceil(300 / 64) = 5
-    assert qa.decode_workspace_size(1, 1, 1, 64, 300, 9) == 2 * 5 * 64 * 4 + 2 * 5 * 4
-    assert qa.decode_workspace_size(1, 3, 1, 64, 64, 1) == 2 * 3 * 64 * 4 + 2 * 3 * 4       # one range, G = 3
+    # explicit range counts need no device.  A stage carries 256 (token, kv-head)
+    # rows: 256/Hkv tokens of every head for Hkv <= 4, 32 tokens of 8 heads for
+    # Hkv >= 8.  Two partial slots per range, each with (heads per stage * G)
+    # rows: partial_o fp32 [2 * ranges, rows, D] then partial_lse [2 * ranges, rows].
+    # Hkv=2: 128 tokens per stage; ranges min(4, 2 * ceil(1000/128)) = 4; rows 2*4
+    assert qa.decode_workspace_size(2, 8, 2, 128, 1000, 4) == 2 * 4 * 8 * 128 * 4 + 2 * 4 * 8 * 4
+    # Hkv=1: 256 tokens per stage, so at most ceil(300/256) = 2 ranges; rows 1
+    assert qa.decode_workspace_size(1, 1, 1, 64, 300, 9) == 2 * 2 * 1 * 64 * 4 + 2 * 2 * 1 * 4
+    assert qa.decode_workspace_size(1, 3, 1, 64, 64, 1) == 2 * 1 * 3 * 64 * 4 + 2 * 1 * 3 * 4
+    # Hkv=8: rows per slot 8 * G
+    assert qa.decode_workspace_size(8, 32, 8, 128, 4096, 152) == 2 * 152 * 32 * 128 * 4 + 2 * 152 * 32 * 4
     assert qa.decode_workspace_size(0, 8, 2, 128, 60, 4) == 0             # invalid sizes
     assert qa.decode_workspace_size(2, 8, 2, 96, 600, 4) == 0
-    assert qa.decode_workspace_size(2, 8, 3, 128, 600, 4) == 0
+    assert qa.decode_workspace_size(2, 12, 6, 128, 600, 4) == 0           # Hkv 6 unsupported
     assert qa.decode_workspace_size(4096, 8, 2, 128, 600, 4) == 0         # batch above the limit
