@@ -216,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t gs = gs0; gs < gs1;) {
         const Loc l = locate(gs, prefix, B, geo.groups);
         const int cnt = static_cast<int>(min(static_cast<int64_t>(l.n - l.s), gs1 - gs));
+        const int seg_len = static_cast<int>(min(static_cast<int64_t>(__ldg(a.seq_lens + l.b)), limit));
         for (int j = 0; j < cnt; ++j, ++it) {
           const int s = it % C::kStages;
           const uint32_t ph = (it / C::kStages) & 1;
@@ -239,9 +240,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sks, &maps.ks, tok0, head0, full_s);
             tma_load_2d(svs, &maps.vs, tok0, head0, full_s);
           } else {
+            // pages of this stage that hold tokens below the sequence length
+            // (a stage may run past the end of the sequence and of its table row)
             const int npages = geo.tokens > kPage ? geo.tokens / kPage : 1;
+            const int nused = min(npages, (seg_len - tok0 + kPage - 1) / kPage);
             bool ok = true;
-            for (int pi = 0; pi < npages; ++pi) {
+            for (int pi = 0; pi < nused; ++pi) {
               const int page = __ldg(cache.page_table + static_cast<int64_t>(l.b) * cache.max_pages +
                                      (tok0 + pi * kPage) / kPage);
               ok = ok && page >= 0 && page < cache.num_pages;
@@ -252,8 +256,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               mbar_arrive(full_s);  // a missing page: the stage's tokens are masked
               continue;
             }
-            mbar_arrive_expect_tx(full_s, 2 * C::kCodeBytes + 2 * C::kScaleBytes);
-            for (int pi = 0; pi < npages; ++pi) {
+            const uint32_t bytes = npages == 1
+                ? 2 * C::kCodeBytes + 2 * C::kScaleBytes
+                : nused * geo.hb * (2 * kPage * rows_per_tok + 2 * kPage * 2);
+            mbar_arrive_expect_tx(full_s, bytes);
+            for (int pi = 0; pi < nused; ++pi) {
               const int ptok = tok0 + pi * kPage;
               const int page = __ldg(cache.page_table + static_cast<int64_t>(l.b) * cache.max_pages + ptok / kPage);
               const int inner = ptok % kPage;  // token offset inside the page
