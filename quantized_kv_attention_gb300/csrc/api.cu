@@ -171,8 +171,8 @@ qattn_status check_cache(const qattn_kv_cache *c, int batch, KvView *v, uint64_t
 
 // Number of balanced key ranges (one persistent CTA each) for a decode call:
 // one per SM by default, never more than there can be stages.
-int plan_ctas(int batch, int hkv, int head_dim, int max_len, int requested, int sms) {
-  const DecodeGeometry geo = decode_geometry(head_dim, hkv, false);
+int plan_ctas(int batch, int hkv, int head_dim, int max_len, int requested, int sms, bool paged) {
+  const DecodeGeometry geo = decode_geometry(head_dim, hkv, paged);
   const int64_t stages = static_cast<int64_t>(batch) * geo.groups *
                          ((static_cast<int64_t>(max_len) + geo.tokens_per_stage - 1) / geo.tokens_per_stage);
   int64_t n = requested > 0 ? requested : sms;
@@ -189,7 +189,10 @@ size_t workspace_bytes(int ctas, int rows, int head_dim) {
   return (o + 255) / 256 * 256 + static_cast<size_t>(2) * ctas * rows * sizeof(float);
 }
 
-bool hkv_supported(int hkv) { return hkv == 1 || hkv == 2 || hkv == 4 || (hkv > 0 && hkv % 8 == 0); }
+// Paged pools stream up to 4 adjacent kv-heads per stage, so Hkv must split evenly.
+bool hkv_supported(int hkv, bool paged) {
+  return hkv > 0 && (!paged || hkv == 1 || hkv == 2 || hkv % 4 == 0);
+}
 
 }  // namespace
 
@@ -226,7 +229,7 @@ size_t qattn_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t n
                                    int32_t head_dim, int32_t max_seq_len, int32_t num_splits) {
   if (batch <= 0 || batch > QATTN_MAX_BATCH || num_q_heads <= 0 || num_kv_heads <= 0 ||
       num_q_heads % num_kv_heads || num_q_heads / num_kv_heads > QATTN_MAX_GROUP || max_seq_len < 0 ||
-      !hkv_supported(num_kv_heads) ||
+      num_kv_heads <= 0 ||
       num_splits < 0 || num_splits > QATTN_MAX_SPLITS || (head_dim != 64 && head_dim != 128))
     return 0;
   int sms = 152;
@@ -236,9 +239,16 @@ size_t qattn_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t n
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
   }
   cudaGetLastError();
-  const int ctas = plan_ctas(batch, num_kv_heads, head_dim, max_seq_len, num_splits, sms);
-  const DecodeGeometry geo = decode_geometry(head_dim, num_kv_heads, false);
-  return workspace_bytes(ctas, geo.heads_per_stage * (num_q_heads / num_kv_heads), head_dim);
+  // the larger of the two cache layouts' needs (the call does not say which one)
+  size_t need = 0;
+  for (int paged = 0; paged < 2; ++paged) {
+    if (paged && !hkv_supported(num_kv_heads, true)) continue;
+    const int ctas = plan_ctas(batch, num_kv_heads, head_dim, max_seq_len, num_splits, sms, paged != 0);
+    const DecodeGeometry geo = decode_geometry(head_dim, num_kv_heads, paged != 0);
+    const size_t n = workspace_bytes(ctas, geo.heads_per_stage * (num_q_heads / num_kv_heads), head_dim);
+    if (n > need) need = n;
+  }
+  return need;
 }
 
 qattn_status qattn_decode(const uint16_t *q, const qattn_kv_cache *cache, const int32_t *seq_lens,
@@ -257,8 +267,8 @@ qattn_status qattn_decode(const uint16_t *q, const qattn_kv_cache *cache, const 
   if (num_q_heads % view.hkv) return fail(QATTN_ERR_INVALID_ARG, "Hq %d is not a multiple of Hkv %d", num_q_heads, view.hkv);
   if (num_q_heads / view.hkv > QATTN_MAX_GROUP)
     return fail(QATTN_ERR_UNSUPPORTED, "group size %d > %d", num_q_heads / view.hkv, QATTN_MAX_GROUP);
-  if (!hkv_supported(view.hkv))
-    return fail(QATTN_ERR_UNSUPPORTED, "num_kv_heads %d (supported: 1, 2, 4 or a multiple of 8)", view.hkv);
+  if (!hkv_supported(view.hkv, view.page_table != nullptr))
+    return fail(QATTN_ERR_UNSUPPORTED, "paged num_kv_heads %d (supported: 1, 2 or a multiple of 4)", view.hkv);
   if (batch == 0) return QATTN_OK;
   if (!q || !seq_lens || !out) return fail(QATTN_ERR_INVALID_ARG, "q, seq_lens or out is NULL");
   if (!aligned16(q) || !aligned16(out)) return fail(QATTN_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
@@ -268,8 +278,9 @@ qattn_status qattn_decode(const uint16_t *q, const qattn_kv_cache *cache, const 
   const int64_t stage_limit = view.page_table ? view.max_pages : view.capacity / kPage;
   if (static_cast<int64_t>(batch) * view.hkv * stage_limit >= (int64_t(1) << 31))
     return fail(QATTN_ERR_UNSUPPORTED, "batch * Hkv * cached stages exceeds 2^31");
-  const int ctas = plan_ctas(batch, view.hkv, view.head_dim, max_seq_len, num_splits, ds->sms);
-  const DecodeGeometry geo = decode_geometry(view.head_dim, view.hkv, view.page_table != nullptr);
+  const bool paged = view.page_table != nullptr;
+  const int ctas = plan_ctas(batch, view.hkv, view.head_dim, max_seq_len, num_splits, ds->sms, paged);
+  const DecodeGeometry geo = decode_geometry(view.head_dim, view.hkv, paged);
   const int slot_rows = geo.heads_per_stage * G;
   const size_t need = workspace_bytes(ctas, slot_rows, view.head_dim);
   if (!workspace || workspace_size < need || !aligned16(workspace))

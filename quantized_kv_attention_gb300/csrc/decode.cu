@@ -113,16 +113,20 @@ __device__ __forceinline__ Loc locate(int64_t gs, const int *prefix, int batch, 
   return l;
 }
 
-// Geometry of one stage, from the number of kv-heads HB it carries.
+// Geometry of one stage.  A TMA box streams at full speed only when its
+// bytes are contiguous: in a contiguous cache a kv-head's tokens are, so a
+// stage is 256 tokens of one kv-head; in a paged pool the kv-heads of a page
+// are adjacent, so a stage is one page (64 tokens) of 4 kv-heads (256/Hkv
+// tokens of every head, page by page, when Hkv < 4).
 struct StageGeo {
-  int hb;      // kv-heads per stage (8, 4, 2 or 1)
+  int hb;      // kv-heads per stage
   int tokens;  // tokens per head per stage = 256 / hb
   int groups;  // head groups = Hkv / hb
   int wph;     // consumer warps per head = 8 / hb
 };
-__host__ __device__ __forceinline__ StageGeo stage_geo(int hkv) {
+__host__ __device__ __forceinline__ StageGeo stage_geo(int hkv, bool paged) {
   StageGeo g;
-  g.hb = hkv >= 8 ? 8 : hkv;
+  g.hb = paged ? (hkv >= 4 ? 4 : hkv) : 1;
   g.tokens = kRowsPerStage / g.hb;
   g.groups = hkv / g.hb;
   g.wph = kConsumerWarps / g.hb;
@@ -144,7 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   using C = Cfg<D>;
   const int G = a.hq / cache.hkv;
   const int B = a.batch, hkv = cache.hkv;
-  const StageGeo geo = stage_geo(hkv);
+  const StageGeo geo = stage_geo(hkv, cache.page_table != nullptr);
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -356,11 +360,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const __half *svs = sks + kRowsPerStage;
 
         // S^T for two 16-token tiles (independent MMA chains)
-        float sacc[2][4];
+        float sacc[2][4], sodd[2][4];
         uint32_t kw[2][2][C::kWords];
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           sacc[t][0] = sacc[t][1] = sacc[t][2] = sacc[t][3] = 0.f;
+          sodd[t][0] = sodd[t][1] = sodd[t][2] = sodd[t][3] = 0.f;
           const int lt = tok_w + t * 16 + g;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -381,9 +386,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t x0[4], x1[4];
             decode_sub(kw[t][0][i], x0);
             decode_sub(kw[t][1][i], x1);
-            mma_16816(sacc[t], x0[0], x1[0], x0[1], x1[1], qb[2 * i][0], qb[2 * i][1]);
-            mma_16816(sacc[t], x0[2], x1[2], x0[3], x1[3], qb[2 * i + 1][0], qb[2 * i + 1][1]);
+            if (i & 1) {  // two accumulation chains per tile
+              mma_16816(sodd[t], x0[0], x1[0], x0[1], x1[1], qb[2 * i][0], qb[2 * i][1]);
+              mma_16816(sodd[t], x0[2], x1[2], x0[3], x1[3], qb[2 * i + 1][0], qb[2 * i + 1][1]);
+            } else {
+              mma_16816(sacc[t], x0[0], x1[0], x0[1], x1[1], qb[2 * i][0], qb[2 * i][1]);
+              mma_16816(sacc[t], x0[2], x1[2], x0[3], x1[3], qb[2 * i + 1][0], qb[2 * i + 1][1]);
+            }
           }
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sacc[t][e] += sodd[t][e];
 
         float ts[2][4], fv[2][2];
 #pragma unroll
@@ -522,18 +536,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 // balanced ranges cut: a segment spanning CTAs c0 < c1 has partials in slot
 // 2*c0 + 1 (its start, in c0's last segment) and slots 2*c for c0 < c <= c1
 // whose range is not empty.  Segments of empty sequences get O = 0 and
-// lse = -inf.  Grid (segments, row blocks of 8); warp w merges one row.
+// lse = -inf.  Grid (segments, rows of a segment); the eight warps of a CTA
+// split one row's partials and add their sums in shared memory.
 template <int D>
 __global__ void __launch_bounds__(256)
     decode_merge_kernel(const int32_t *__restrict__ seq_lens, int batch, int hkv, int G, int ctas,
-                        int64_t limit, const float *__restrict__ po, const float *__restrict__ pl,
-                        uint16_t *__restrict__ out, float *__restrict__ lse) {
+                        int64_t limit, int paged, const float *__restrict__ po,
+                        const float *__restrict__ pl, uint16_t *__restrict__ out,
+                        float *__restrict__ lse) {
   constexpr int VPL = D / 32;
-  __shared__ float wsh[8][QATTN_MAX_SPLITS + 1];
-  __shared__ int red[2][8];
+  __shared__ float wsh[QATTN_MAX_SPLITS + 1];
+  __shared__ float accs[8][D];
+  __shared__ float red[2][8];
+  __shared__ int redi[2][8];
   pdl_wait();
-  const StageGeo geo = stage_geo(hkv);
+  const StageGeo geo = stage_geo(hkv, paged != 0);
   const int b = blockIdx.x / geo.groups, hg = blockIdx.x % geo.groups;
+  const int r = blockIdx.y;  // row within the segment: kv-head r / G, q-head r % G
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   auto stages = [&](int bb) {
     const int64_t len = min(static_cast<int64_t>(__ldg(seq_lens + bb)), limit);
@@ -550,19 +569,16 @@ __global__ void __launch_bounds__(256)
     tot += __shfl_xor_sync(0xffffffffu, tot, o);
     pre += __shfl_xor_sync(0xffffffffu, pre, o);
   }
-  if (lane == 0) red[0][warp] = tot, red[1][warp] = pre;
+  if (lane == 0) redi[0][warp] = tot, redi[1][warp] = pre;
   __syncthreads();
   tot = pre = 0;
-  for (int w = 0; w < 8; ++w) tot += red[0][w], pre += red[1][w];
+  for (int w = 0; w < 8; ++w) tot += redi[0][w], pre += redi[1][w];
   const int rows = geo.hb * G;
-  const int r = blockIdx.y * 8 + warp;  // row within the segment: kv-head r / G, q-head r % G
-  if (r >= rows) return;
-  const int64_t hq = static_cast<int64_t>(hkv) * G;
-  const int64_t row = static_cast<int64_t>(b) * hq + static_cast<int64_t>(hg) * rows + r;
+  const int64_t row = static_cast<int64_t>(b) * hkv * G + static_cast<int64_t>(hg) * rows + r;
   const int n = stages(b);
   if (n == 0) {
-    for (int d = lane; d < D; d += 32) out[row * D + d] = 0;
-    if (lane == 0 && lse) lse[row] = -INFINITY;
+    for (int d = threadIdx.x; d < D; d += 256) out[row * D + d] = 0;
+    if (threadIdx.x == 0 && lse) lse[row] = -INFINITY;
     return;
   }
   const int64_t T = static_cast<int64_t>(geo.groups) * tot;
@@ -576,27 +592,36 @@ __global__ void __launch_bounds__(256)
     const int64_t c = c0 + k;
     return k == 0 || range_start(c, T, ctas) < range_start(c + 1, T, ctas);
   };
-  float M = -INFINITY;
-  for (int k = lane; k < np; k += 32)
-    if (used(k)) M = fmaxf(M, pl[slot_of(k) * rows + r]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  float z = 0.f;
-  for (int k = lane; k < np; k += 32) {
+  float mx = -INFINITY;
+  for (int k = threadIdx.x; k < np; k += 256) {
     const float lv = used(k) ? pl[slot_of(k) * rows + r] : -INFINITY;
-    const float e = lv == -INFINITY ? 0.f : expf(lv - M);
-    wsh[warp][k] = e;
+    wsh[k] = lv;
+    mx = fmaxf(mx, lv);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) red[0][warp] = mx;
+  __syncthreads();
+  float M = red[0][0];
+  for (int w = 1; w < 8; ++w) M = fmaxf(M, red[0][w]);
+  float z = 0.f;
+  for (int k = threadIdx.x; k < np; k += 256) {
+    const float e = wsh[k] == -INFINITY ? 0.f : expf(wsh[k] - M);
+    wsh[k] = e;
     z += e;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-  __syncwarp();
+  if (lane == 0) red[1][warp] = z;
+  __syncthreads();
+  float Z = 0.f;
+  for (int w = 0; w < 8; ++w) Z += red[1][w];
   float acc[VPL];
 #pragma unroll
   for (int j = 0; j < VPL; ++j) acc[j] = 0.f;
 #pragma unroll 4
-  for (int k = 0; k < np; ++k) {
-    const float wk = wsh[warp][k];
+  for (int k = warp; k < np; k += 8) {
+    const float wk = wsh[k];
     if (wk > 0.f) {
       const float *src = po + (slot_of(k) * rows + r) * D + lane * VPL;
       if constexpr (VPL == 4) {
@@ -608,11 +633,17 @@ __global__ void __launch_bounds__(256)
       }
     }
   }
-  const float inv = M == -INFINITY ? 0.f : 1.f / z;
 #pragma unroll
-  for (int j = 0; j < VPL; ++j)
-    out[row * D + lane * VPL + j] = __half_as_ushort(__float2half_rn(acc[j] * inv));
-  if (lane == 0 && lse) lse[row] = M == -INFINITY ? -INFINITY : M + logf(z);
+  for (int j = 0; j < VPL; ++j) accs[warp][lane * VPL + j] = acc[j];
+  __syncthreads();
+  const float inv = M == -INFINITY ? 0.f : 1.f / Z;
+  for (int d = threadIdx.x; d < D; d += 256) {
+    float o = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) o += accs[w][d];
+    out[row * D + d] = __half_as_ushort(__float2half_rn(o * inv));
+  }
+  if (threadIdx.x == 0 && lse) lse[row] = M == -INFINITY ? -INFINITY : M + logf(Z);
 }
 
 cudaLaunchAttribute pdl_attr() {
@@ -633,7 +664,8 @@ cudaError_t launch_d(const DecodeArgs &a, const KvView &cache, const DecodeMaps 
     configured = true;
   }
   const int G = a.hq / cache.hkv;
-  const StageGeo geo = stage_geo(cache.hkv);
+  const bool paged = cache.page_table != nullptr;
+  const StageGeo geo = stage_geo(cache.hkv, paged);
   Maps maps;
   maps.k = dm.k, maps.v = dm.v, maps.ks = dm.ks, maps.vs = dm.vs;
   cudaLaunchAttribute attr[1] = {pdl_attr()};
@@ -648,20 +680,20 @@ cudaError_t launch_d(const DecodeArgs &a, const KvView &cache, const DecodeMaps 
   if (e != cudaSuccess) return e;
   const int64_t limit = cache.page_table ? static_cast<int64_t>(cache.max_pages) * kPage : cache.capacity;
   cudaLaunchConfig_t mc = {};
-  mc.gridDim = dim3(a.batch * geo.groups, (geo.hb * G + 7) / 8);
+  mc.gridDim = dim3(a.batch * geo.groups, geo.hb * G);
   mc.blockDim = dim3(256);
   mc.stream = stream;
   mc.attrs = attr;
   mc.numAttrs = 1;
   return cudaLaunchKernelEx(&mc, decode_merge_kernel<D>, a.seq_lens, a.batch, cache.hkv, G, a.ctas, limit,
-                            static_cast<const float *>(a.partial_o), static_cast<const float *>(a.partial_lse),
+                            static_cast<int>(paged), static_cast<const float *>(a.partial_o), static_cast<const float *>(a.partial_lse),
                             a.out, a.lse);
 }
 
 }  // namespace
 
 DecodeGeometry decode_geometry(int head_dim, int hkv, bool paged) {
-  const StageGeo g = stage_geo(hkv);
+  const StageGeo g = stage_geo(hkv, paged);
   DecodeGeometry r;
   r.heads_per_stage = g.hb;
   r.tokens_per_stage = g.tokens;

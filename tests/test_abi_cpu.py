@@ -94,18 +94,24 @@ def test_quantize_and_combine_reject_bad_arguments():
 
 
 def test_workspace_size_host_arithmetic():
-    # explicit range counts need no device.  A stage carries 256 (token, kv-head)
-    # rows: 256/Hkv tokens of every head for Hkv <= 4, 32 tokens of 8 heads for
-    # Hkv >= 8.  Two partial slots per range, each with (heads per stage * G)
-    # rows: partial_o fp32 [2 * ranges, rows, D] then partial_lse [2 * ranges, rows].
-    # Hkv=2: 128 tokens per stage; ranges min(4, 2 * ceil(1000/128)) = 4; rows 2*4
-    assert qa.decode_workspace_size(2, 8, 2, 128, 1000, 4) == 2 * 4 * 8 * 128 * 4 + 2 * 4 * 8 * 4
-    # Hkv=1: 256 tokens per stage, so at most ceil(300/256) = 2 ranges; rows 1
-    assert qa.decode_workspace_size(1, 1, 1, 64, 300, 9) == 2 * 2 * 1 * 64 * 4 + 2 * 2 * 1 * 4
-    assert qa.decode_workspace_size(1, 3, 1, 64, 64, 1) == 2 * 1 * 3 * 64 * 4 + 2 * 1 * 3 * 4
-    # Hkv=8: rows per slot 8 * G
-    assert qa.decode_workspace_size(8, 32, 8, 128, 4096, 152) == 2 * 152 * 32 * 128 * 4 + 2 * 152 * 32 * 4
+    # Explicit range counts need no device.  A stage carries 256 (token, kv-head)
+    # rows: 256 tokens of one kv-head in a contiguous cache, one 64-token page of
+    # 4 kv-heads in a paged pool (256/Hkv tokens of all heads when Hkv < 4).  Two
+    # partial slots per range, each with (kv-heads per stage * G) rows:
+    # partial_o fp32 [2 * ranges, rows, D], then partial_lse [2 * ranges, rows].
+    # The query does not know the layout, so it returns the larger need.
+    def need(ranges, rows, d):
+        return 2 * ranges * rows * d * 4 + 2 * ranges * rows * 4
+    # Hkv=2: contiguous ranges min(4, 2*2*ceil(1000/256)) = 4 with G=4 rows;
+    # paged stages hold both heads (rows 8), ranges min(4, 2*1*ceil(1000/128)) = 4
+    assert qa.decode_workspace_size(2, 8, 2, 128, 1000, 4) == need(4, 8, 128)
+    # Hkv=1: 256 tokens per stage either way, ceil(300/256) = 2 ranges, 1 row
+    assert qa.decode_workspace_size(1, 1, 1, 64, 300, 9) == need(2, 1, 64)
+    assert qa.decode_workspace_size(1, 3, 1, 64, 64, 1) == need(1, 3, 64)
+    # Hkv=8, G=4: paged slots hold 4 kv-heads (rows 16)
+    assert qa.decode_workspace_size(8, 32, 8, 128, 4096, 152) == need(152, 16, 128)
+    # Hkv=6 has no paged geometry (not a multiple of 4): contiguous rows only
+    assert qa.decode_workspace_size(2, 12, 6, 128, 600, 4) == need(4, 2, 128)
     assert qa.decode_workspace_size(0, 8, 2, 128, 60, 4) == 0             # invalid sizes
     assert qa.decode_workspace_size(2, 8, 2, 96, 600, 4) == 0
-    assert qa.decode_workspace_size(2, 12, 6, 128, 600, 4) == 0           # Hkv 6 unsupported
     assert qa.decode_workspace_size(4096, 8, 2, 128, 600, 4) == 0         # batch above the limit
