@@ -301,7 +301,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kofs = hbw * geo.tokens * (D / 2); // byte offset of the head's codes in a stage
   const int sofs = hbw * geo.tokens;           // element offset of the head's scales
   const float kf = a.scale_log2 * kTwo24;      // folds the 2^-24 of the subnormal codes
-  int it = 0;                                  // CTA-local stage index, as in the producer
+  // Stage-relative swizzled offsets of this lane's K rows (tile t, rows g / g+8)
+  // and of its ldmatrix.x4.trans rows (matrix q holds tokens (q & 2 ? 8 : 0) +
+  // 0..7 of tile t at 16-byte chunk 2 jp + (q & 1)); the same in every stage.
+  uint32_t koff[2][2], voff[2][D / 64];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      koff[t][h] = swz128(kofs + (tok_w + t * 16 + g + 8 * h) * (D / 2) + c * C::kKBytes);
+#pragma unroll
+    for (int jp = 0; jp < D / 64; ++jp) {
+      const int q = lane >> 3;
+      const int vt = tok_w + t * 16 + ((q & 2) ? 8 : 0) + (lane & 7);
+      voff[t][jp] = swz128(kofs + vt * (D / 2) + (2 * jp + (q & 1)) * 16);
+    }
+  }
+  const uint32_t ring = smem_u32(smem);
+  int slot = 0;          // ring slot of the next stage
+  uint32_t phase = 0;    // its mbarrier parity
   for (int64_t gs = gs0; gs < gs1;) {
     const Loc l = locate(gs, prefix, B, geo.groups);
     const int cnt = static_cast<int>(min(static_cast<int64_t>(l.n - l.s), gs1 - gs));
@@ -347,79 +365,108 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int mt = 0; mt < C::kMt; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
-    for (int j = 0; j < cnt; ++j, ++it) {
-      const int s = it % C::kStages;
-      const uint32_t ph = (it / C::kStages) & 1;
-      const bool got = mbar_wait(smem_u32(full + s), ph, err, *abort_flag ? kDrainCycles : kWaitCycles);
+    // Wait for the stage in `sl`; its tokens for this warp, or 0 if unusable.
+    auto acquire = [&](int sl, uint32_t ph, int j) -> int {
+      const bool got = mbar_wait(smem_u32(full + sl), ph, err, *abort_flag ? kDrainCycles : kWaitCycles);
       if (!got) *abort_flag = 1;
-      const int nvalid = len - (l.s + j) * geo.tokens - tok_w;
-      if (got && valid[s] && nvalid > 0) {
-        const uint32_t kb = smem_u32(smem + s * C::kStageBytes);
-        const uint32_t vb = kb + C::kCodeBytes;
-        const __half *sks = reinterpret_cast<const __half *>(smem + s * C::kStageBytes + 2 * C::kCodeBytes) + sofs;
-        const __half *svs = sks + kRowsPerStage;
-
-        // S^T for two 16-token tiles (independent MMA chains)
-        float sacc[2][4], sodd[2][4];
-        uint32_t kw[2][2][C::kWords];
+      const int nv = len - (l.s + j) * geo.tokens - tok_w;
+      return (got && valid[sl]) ? max(0, min(nv, 32)) : 0;
+    };
+    // S^T of the warp's 32 tokens in stage `sl`: two 16-token tiles, each
+    // split into two accumulation chains (even / odd code words).
+    auto qk = [&](int sl, float (&sa)[2][4]) {
+      const uint32_t kb = ring + sl * C::kStageBytes;
+      uint32_t kw[2][2][C::kWords];
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if constexpr (C::kWords == 4) {
+            const uint4 u = lds128(kb + koff[t][h]);
+            kw[t][h][0] = u.x, kw[t][h][1] = u.y, kw[t][h][2] = u.z, kw[t][h][3] = u.w;
+          } else {
+            const uint2 u = lds64(kb + koff[t][h]);
+            kw[t][h][0] = u.x, kw[t][h][1] = u.y;
+          }
+        }
+      float so[2][4];
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sa[t][e] = so[t][e] = 0.f;
+#pragma unroll
+      for (int i = 0; i < C::kWords; ++i)
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
-          sacc[t][0] = sacc[t][1] = sacc[t][2] = sacc[t][3] = 0.f;
-          sodd[t][0] = sodd[t][1] = sodd[t][2] = sodd[t][3] = 0.f;
-          const int lt = tok_w + t * 16 + g;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t addr = kb + swz128(kofs + (lt + 8 * h) * (D / 2) + c * C::kKBytes);
-            if constexpr (C::kWords == 4) {
-              const uint4 u = lds128(addr);
-              kw[t][h][0] = u.x, kw[t][h][1] = u.y, kw[t][h][2] = u.z, kw[t][h][3] = u.w;
-            } else {
-              const uint2 u = lds64(addr);
-              kw[t][h][0] = u.x, kw[t][h][1] = u.y;
-            }
+          uint32_t x0[4], x1[4];
+          decode_sub(kw[t][0][i], x0);
+          decode_sub(kw[t][1][i], x1);
+          if (i & 1) {
+            mma_16816(so[t], x0[0], x1[0], x0[1], x1[1], qb[2 * i][0], qb[2 * i][1]);
+            mma_16816(so[t], x0[2], x1[2], x0[3], x1[3], qb[2 * i + 1][0], qb[2 * i + 1][1]);
+          } else {
+            mma_16816(sa[t], x0[0], x1[0], x0[1], x1[1], qb[2 * i][0], qb[2 * i][1]);
+            mma_16816(sa[t], x0[2], x1[2], x0[3], x1[3], qb[2 * i + 1][0], qb[2 * i + 1][1]);
           }
         }
 #pragma unroll
-        for (int i = 0; i < C::kWords; ++i)
+      for (int t = 0; t < 2; ++t)
 #pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            uint32_t x0[4], x1[4];
-            decode_sub(kw[t][0][i], x0);
-            decode_sub(kw[t][1][i], x1);
-            if (i & 1) {  // two accumulation chains per tile
-              mma_16816(sodd[t], x0[0], x1[0], x0[1], x1[1], qb[2 * i][0], qb[2 * i][1]);
-              mma_16816(sodd[t], x0[2], x1[2], x0[3], x1[3], qb[2 * i + 1][0], qb[2 * i + 1][1]);
-            } else {
-              mma_16816(sacc[t], x0[0], x1[0], x0[1], x1[1], qb[2 * i][0], qb[2 * i][1]);
-              mma_16816(sacc[t], x0[2], x1[2], x0[3], x1[3], qb[2 * i + 1][0], qb[2 * i + 1][1]);
-            }
-          }
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) sacc[t][e] += sodd[t][e];
+        for (int e = 0; e < 4; ++e) sa[t][e] += so[t][e];
+    };
 
+    // Software pipeline: the QK of stage j+1 is issued before the softmax and
+    // PV of stage j, so the two dependency chains overlap in every warp.
+    float sacc[2][4], snext[2][4];
+    int cur = slot;
+    uint32_t cur_ph = phase;
+    int nvalid = acquire(cur, cur_ph, 0);
+    if (nvalid > 0) qk(cur, sacc);
+    for (int j = 0; j < cnt; ++j) {
+      int nxt = cur + 1;
+      uint32_t nxt_ph = cur_ph;
+      if (nxt == C::kStages) nxt = 0, nxt_ph ^= 1u;
+      int nvalid_next = 0;
+      if (j + 1 < cnt) {
+        nvalid_next = acquire(nxt, nxt_ph, j + 1);
+        if (nvalid_next > 0) qk(nxt, snext);
+      }
+      if (nvalid > 0) {
+        const uint32_t vb = ring + cur * C::kStageBytes + C::kCodeBytes;
+        const __half *sks = reinterpret_cast<const __half *>(smem + cur * C::kStageBytes + 2 * C::kCodeBytes) + sofs;
+        const __half *svs = sks + kRowsPerStage;
         float ts[2][4], fv[2][2];
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           const int lt = tok_w + t * 16 + g;
-          const bool v0 = t * 16 + g < nvalid, v1 = t * 16 + g + 8 < nvalid;
           const float f0 = __half2float(sks[lt]) * kf, f1 = __half2float(sks[lt + 8]) * kf;
-          ts[t][0] = v0 ? (sacc[t][0] - bq0) * f0 : -INFINITY;
-          ts[t][1] = v0 ? (sacc[t][1] - bq1) * f0 : -INFINITY;
-          ts[t][2] = v1 ? (sacc[t][2] - bq0) * f1 : -INFINITY;
-          ts[t][3] = v1 ? (sacc[t][3] - bq1) * f1 : -INFINITY;
-          fv[t][0] = v0 ? __half2float(svs[lt]) : 0.f;
-          fv[t][1] = v1 ? __half2float(svs[lt + 8]) : 0.f;
+          ts[t][0] = (sacc[t][0] - bq0) * f0;
+          ts[t][1] = (sacc[t][1] - bq1) * f0;
+          ts[t][2] = (sacc[t][2] - bq0) * f1;
+          ts[t][3] = (sacc[t][3] - bq1) * f1;
+          // the V scale carries an exact 2^-8: with a lazily raised max p can
+          // reach 2^8, and p * s_V must stay inside the fp16 range
+          fv[t][0] = __half2float(svs[lt]) * 0.00390625f;
+          fv[t][1] = __half2float(svs[lt + 8]) * 0.00390625f;
         }
-        float mx0 = fmaxf(fmaxf(ts[0][0], ts[0][2]), fmaxf(ts[1][0], ts[1][2]));
-        float mx1 = fmaxf(fmaxf(ts[0][1], ts[0][3]), fmaxf(ts[1][1], ts[1][3]));
+        if (nvalid < 32) {  // tail: mask tokens past the sequence end (never touch their scales)
 #pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+          for (int t = 0; t < 2; ++t) {
+            const bool v0 = t * 16 + g < nvalid, v1 = t * 16 + g + 8 < nvalid;
+            if (!v0) ts[t][0] = ts[t][1] = -INFINITY, fv[t][0] = 0.f;
+            if (!v1) ts[t][2] = ts[t][3] = -INFINITY, fv[t][1] = 0.f;
+          }
         }
-        if (__any_sync(0xffffffffu, mx0 > m0 || mx1 > m1)) {
+        // lazy running max: rescale only when a score exceeds the max by 2^8
+        const float lm0 = fmaxf(fmaxf(ts[0][0], ts[0][2]), fmaxf(ts[1][0], ts[1][2]));
+        const float lm1 = fmaxf(fmaxf(ts[0][1], ts[0][3]), fmaxf(ts[1][1], ts[1][3]));
+        if (__any_sync(0xffffffffu, lm0 > m0 + 8.f || lm1 > m1 + 8.f)) {
+          float mx0 = lm0, mx1 = lm1;
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+          }
           const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
           const float al0 = ex2(m0 - n0), al1 = ex2(m1 - n1);
           m0 = n0, m1 = n1;
@@ -445,16 +492,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           pb[t][0] = movmatrix_trans(r0);
           pb[t][1] = movmatrix_trans(r1);
         }
-        // O^T += V codes^T . P'^T; ldmatrix.x4.trans matrix q holds tokens
-        // (q & 2 ? 8 : 0) + 0..7 of the tile at 16-byte chunk 2 jp + (q & 1).
+        // O^T += V codes^T . P'^T
 #pragma unroll
         for (int t = 0; t < 2; ++t)
 #pragma unroll
           for (int jp = 0; jp < D / 64; ++jp) {
-            const int q = lane >> 3;
-            const int vt = tok_w + t * 16 + ((q & 2) ? 8 : 0) + (lane & 7);
             uint32_t r0, r1, r2, r3;
-            ldsm_x4_trans(vb + swz128(kofs + vt * (D / 2) + (2 * jp + (q & 1)) * 16), r0, r1, r2, r3);
+            ldsm_x4_trans(vb + voff[t][jp], r0, r1, r2, r3);
             uint32_t d0[4], d1[4], d2[4], d3[4];
             decode_sub(r0, d0);
             decode_sub(r1, d1);
@@ -466,9 +510,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(empty + s));
+      if (lane == 0) mbar_arrive(smem_u32(empty + cur));
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[t][e] = snext[t][e];
+      cur = nxt, cur_ph = nxt_ph, nvalid = nvalid_next;
     }
-
+    slot = cur, phase = cur_ph;  // the stage after this segment's last
     // --------------------------------------------- segment end: merge warps
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
@@ -484,15 +533,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int mt = jp * 4 + k;
         const float fac = (k & 1) ? kTwo24 / 16.f : kTwo24;
         const int dlo = 64 * jp + 4 * g + k, dhi = dlo + 32;
-        if (2 * c < G) {
+        if (2 * c < G) {  // P' carried 2^-8
           float *w0 = smo + (warp * G + 2 * c) * D;
-          w0[dlo] = o[mt][0] * fac - 8.f * ps0;
-          w0[dhi] = o[mt][2] * fac - 8.f * ps0;
+          w0[dlo] = (o[mt][0] * fac - 8.f * ps0) * 256.f;
+          w0[dhi] = (o[mt][2] * fac - 8.f * ps0) * 256.f;
         }
         if (2 * c + 1 < G) {
           float *w1 = smo + (warp * G + 2 * c + 1) * D;
-          w1[dlo] = o[mt][1] * fac - 8.f * ps1;
-          w1[dhi] = o[mt][3] * fac - 8.f * ps1;
+          w1[dlo] = (o[mt][1] * fac - 8.f * ps1) * 256.f;
+          w1[dhi] = (o[mt][3] * fac - 8.f * ps1) * 256.f;
         }
       }
     if (g == 0) {
