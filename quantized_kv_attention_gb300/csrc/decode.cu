@@ -55,18 +55,20 @@ struct Cfg {
   static constexpr int kCodeBytes = kRowsPerStage * D / 2;  // per tensor per stage
   static constexpr int kScaleBytes = kRowsPerStage * 2;
   static constexpr int kStageBytes = (2 * kCodeBytes + 2 * kScaleBytes + 1023) / 1024 * 1024;
-  static constexpr int kStages = D == 128 ? 5 : 8;
+  static constexpr int kStages = D == 128 ? 4 : 8;
+  static constexpr int kQSlot = 4 * QATTN_MAX_GROUP * D * 2;  // Q rows of one segment (<= 4 kv-heads)
   static constexpr int kRing = kStages * kStageBytes;
   static constexpr int kKBytes = D / 8;  // K code bytes per lane per token
   static constexpr int kWords = kKBytes / 4;
   static constexpr int kMt = D / 16;     // m-tiles of O^T, k-steps of S
 };
 
-// Dynamic shared memory: ring | merge (O per warp, q-head) | m, l | prefix | barriers, flags.
+// Dynamic shared memory: ring | 2 Q slots | merge (O per warp, q-head) | m, l |
+// prefix | lengths | barriers, flags.
 template <int D>
 __host__ __device__ constexpr int smem_bytes(int G, int batch) {
-  return Cfg<D>::kRing + kConsumerWarps * G * D * 4 + 2 * kConsumerWarps * 8 * 4 + (batch + 1) * 4 +
-         2 * Cfg<D>::kStages * 8 + Cfg<D>::kStages * 4 + 16 + 1024;
+  return Cfg<D>::kRing + 2 * Cfg<D>::kQSlot + kConsumerWarps * G * D * 4 + 2 * kConsumerWarps * 8 * 4 +
+         (2 * batch + 1) * 4 + (2 * Cfg<D>::kStages + 4) * 8 + Cfg<D>::kStages * 4 + 16 + 1024;
 }
 
 __device__ __forceinline__ void consumer_sync() {
@@ -152,14 +154,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  float *smo = reinterpret_cast<float *>(smem + C::kRing);           // [warp][G][D]
+  __half *qslot = reinterpret_cast<__half *>(smem + C::kRing);      // [2][rows of a segment][D]
+  float *smo = reinterpret_cast<float *>(smem + C::kRing + 2 * C::kQSlot);  // [warp][G][D]
   float *smm = smo + kConsumerWarps * G * D;                          // [warp][8]
   float *sml = smm + kConsumerWarps * 8;                              // [warp][8]
   int *prefix = reinterpret_cast<int *>(sml + kConsumerWarps * 8);    // [B + 1]
+  int *lens = prefix + B + 1;                                         // [B], clamped
   uint64_t *full = reinterpret_cast<uint64_t *>(
-      (reinterpret_cast<uintptr_t>(prefix + B + 1) + 7) & ~static_cast<uintptr_t>(7));
+      (reinterpret_cast<uintptr_t>(lens + B) + 7) & ~static_cast<uintptr_t>(7));
   uint64_t *empty = full + C::kStages;
-  int *valid = reinterpret_cast<int *>(empty + C::kStages);          // [kStages]: 0 = missing page
+  uint64_t *qfull = empty + C::kStages;                               // [2]
+  uint64_t *qempty = qfull + 2;                                       // [2]
+  int *valid = reinterpret_cast<int *>(qempty + 2);                  // [kStages]: 0 = missing page
   volatile int *abort_flag = valid + C::kStages;                     // set after a timed-out wait
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -171,8 +177,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(full + s), 1);
       mbar_init(smem_u32(empty + s), kConsumerWarps);
     }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(smem_u32(qfull + s), 1);
+      mbar_init(smem_u32(qempty + s), kConsumerWarps);
+    }
     *abort_flag = 0;
     fence_mbar_init();
+  }
+  if (threadIdx.x == kConsumerWarps * 32) {  // descriptors are kernel parameters: fetch early
+    prefetch_tmap(&maps.k);
+    prefetch_tmap(&maps.v);
+    prefetch_tmap(&maps.ks);
+    prefetch_tmap(&maps.vs);
   }
   pdl_wait();                // inputs may come from the preceding kernel on the stream
   pdl_launch_dependents();   // the merge kernel may be scheduled as SMs free up
@@ -184,6 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       len = static_cast<int>(limit);
       atomicOr(err, kFlagBadPage);
     }
+    if (len < 0) len = 0;
+    lens[b] = len;
     prefix[b + 1] = len > 0 ? geo.groups * ((len + geo.tokens - 1) / geo.tokens) : 0;
   }
   __syncthreads();
@@ -211,16 +229,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      prefetch_tmap(&maps.k);
-      prefetch_tmap(&maps.v);
-      prefetch_tmap(&maps.ks);
-      prefetch_tmap(&maps.vs);
       const int rows_per_tok = D / 2;  // code bytes per token
-      int it = 0;
-      for (int64_t gs = gs0; gs < gs1;) {
+      const uint32_t qbytes = geo.hb * G * D * 2;
+      int it = 0, seg = 0;
+      for (int64_t gs = gs0; gs < gs1; ++seg) {
         const Loc l = locate(gs, prefix, B, geo.groups);
         const int cnt = static_cast<int>(min(static_cast<int64_t>(l.n - l.s), gs1 - gs));
-        const int seg_len = static_cast<int>(min(static_cast<int64_t>(__ldg(a.seq_lens + l.b)), limit));
+        const int seg_len = lens[l.b];
+        // the segment's Q rows (its head group's q-heads are contiguous)
+        {
+          const int qs = seg & 1;
+          if (seg >= 2 && !mbar_wait(smem_u32(qempty + qs), ((seg >> 1) & 1) ^ 1, err,
+                                     *abort_flag ? kDrainCycles : kWaitCycles)) {
+            *abort_flag = 1;
+            return;
+          }
+          const uint32_t qf = smem_u32(qfull + qs);
+          mbar_arrive_expect_tx(qf, qbytes);
+          bulk_g2s(smem_u32(qslot) + qs * C::kQSlot,
+                   a.q + (static_cast<int64_t>(l.b) * a.hq + static_cast<int64_t>(l.hg) * geo.hb * G) * D, qbytes, qf);
+        }
         for (int j = 0; j < cnt; ++j, ++it) {
           const int s = it % C::kStages;
           const uint32_t ph = (it / C::kStages) & 1;
@@ -320,11 +348,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t ring = smem_u32(smem);
   int slot = 0;          // ring slot of the next stage
   uint32_t phase = 0;    // its mbarrier parity
-  for (int64_t gs = gs0; gs < gs1;) {
+  int seg = 0;           // segment counter (Q slot seg & 1)
+  for (int64_t gs = gs0; gs < gs1; ++seg) {
     const Loc l = locate(gs, prefix, B, geo.groups);
     const int cnt = static_cast<int>(min(static_cast<int64_t>(l.n - l.s), gs1 - gs));
-    const int len = static_cast<int>(min(static_cast<int64_t>(__ldg(a.seq_lens + l.b)), limit));
-    const int kvh = l.hg * geo.hb + hbw;
+    const int len = lens[l.b];
 
     // Q of q-head g as the B operand.  Lane c covers d = c*D/4 + 8i + {0..7}
     // (word i of its K code bytes); the decoder pairs (e, e+4), and nibble
@@ -332,13 +360,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t qb[C::kMt][2];
     float qsum = 0.f;
     {
+      const int qs = seg & 1;
+      if (!mbar_wait(smem_u32(qfull + qs), (seg >> 1) & 1, err, *abort_flag ? kDrainCycles : kWaitCycles))
+        *abort_flag = 1;
       const int dbase = c * (D / 4);
-      const uint4 *qv = reinterpret_cast<const uint4 *>(
-          a.q + (static_cast<int64_t>(l.b) * a.hq + kvh * G + min(g, G - 1)) * D + dbase);
+      const uint32_t qrow = smem_u32(qslot) + qs * C::kQSlot + ((hbw * G + min(g, G - 1)) * D + dbase) * 2;
       const __half2 sixteenth = __float2half2_rn(0.0625f);
 #pragma unroll
       for (int i = 0; i < C::kWords; ++i) {
-        const uint4 u = g < G ? __ldg(qv + i) : make_uint4(0, 0, 0, 0);
+        const uint4 u = g < G ? lds128(qrow + 16 * i) : make_uint4(0, 0, 0, 0);
         const uint32_t p0 = __byte_perm(u.x, u.z, 0x5410), p1 = __byte_perm(u.x, u.z, 0x7632);
         const uint32_t p2 = __byte_perm(u.y, u.w, 0x5410), p3 = __byte_perm(u.y, u.w, 0x7632);
         __half2 h1 = __hmul2(*reinterpret_cast<const __half2 *>(&p1), sixteenth);
@@ -354,6 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         qsum += f0.x + f0.y + f2.x + f2.y + 16.f * (f1.x + f1.y + f3.x + f3.y);
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(qempty + (seg & 1)));  // Q now lives in registers
     qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
     qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
     // raw-unit bias 8 * sum(q) * 2^-24 for the lane's q-heads 2c and 2c+1
@@ -585,30 +617,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 // balanced ranges cut: a segment spanning CTAs c0 < c1 has partials in slot
 // 2*c0 + 1 (its start, in c0's last segment) and slots 2*c for c0 < c <= c1
 // whose range is not empty.  Segments of empty sequences get O = 0 and
-// lse = -inf.  Grid (segments, rows of a segment); the eight warps of a CTA
-// split one row's partials and add their sums in shared memory.
+// lse = -inf.  Grid (segments, rows of a segment); the 16 warps of a CTA split
+// one row's partials, each folding its share with a running max so that the
+// lse and O of a partial are fetched together, then combine in shared memory.
+constexpr int kMergeWarps = 16;
+
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kMergeWarps * 32)
     decode_merge_kernel(const int32_t *__restrict__ seq_lens, int batch, int hkv, int G, int ctas,
                         int64_t limit, int paged, const float *__restrict__ po,
                         const float *__restrict__ pl, uint16_t *__restrict__ out,
                         float *__restrict__ lse) {
   constexpr int VPL = D / 32;
-  __shared__ float wsh[QATTN_MAX_SPLITS + 1];
-  __shared__ float accs[8][D];
-  __shared__ float red[2][8];
-  __shared__ int redi[2][8];
-  pdl_wait();
+  __shared__ float accs[kMergeWarps][D];
+  __shared__ float wm[kMergeWarps], wz[kMergeWarps];
+  __shared__ int redi[2][kMergeWarps];
   const StageGeo geo = stage_geo(hkv, paged != 0);
   const int b = blockIdx.x / geo.groups, hg = blockIdx.x % geo.groups;
   const int r = blockIdx.y;  // row within the segment: kv-head r / G, q-head r % G
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // The decode kernel triggers this launch only after its own wait on the
+  // inputs, so the lengths are final here; its partials are read after pdl_wait.
   auto stages = [&](int bb) {
     const int64_t len = min(static_cast<int64_t>(__ldg(seq_lens + bb)), limit);
     return len > 0 ? static_cast<int>((len + geo.tokens - 1) / geo.tokens) : 0;
   };
   int tot = 0, pre = 0;
-  for (int bb = threadIdx.x; bb < batch; bb += 256) {
+  for (int bb = threadIdx.x; bb < batch; bb += kMergeWarps * 32) {
     const int n = stages(bb);
     tot += n;
     if (bb < b) pre += n;
@@ -621,12 +656,13 @@ __global__ void __launch_bounds__(256)
   if (lane == 0) redi[0][warp] = tot, redi[1][warp] = pre;
   __syncthreads();
   tot = pre = 0;
-  for (int w = 0; w < 8; ++w) tot += redi[0][w], pre += redi[1][w];
+  for (int w = 0; w < kMergeWarps; ++w) tot += redi[0][w], pre += redi[1][w];
   const int rows = geo.hb * G;
   const int64_t row = static_cast<int64_t>(b) * hkv * G + static_cast<int64_t>(hg) * rows + r;
   const int n = stages(b);
-  if (n == 0) {
-    for (int d = threadIdx.x; d < D; d += 256) out[row * D + d] = 0;
+  if (n == 0) {  // no decode CTA touches this row
+    pdl_wait();
+    for (int d = threadIdx.x; d < D; d += kMergeWarps * 32) out[row * D + d] = 0;
     if (threadIdx.x == 0 && lse) lse[row] = -INFINITY;
     return;
   }
@@ -635,61 +671,48 @@ __global__ void __launch_bounds__(256)
   const int64_t c0 = owner_cta(first, T, ctas), c1 = owner_cta(first + n - 1, T, ctas);
   if (c0 == c1) return;  // finished inside one CTA
   const int np = static_cast<int>(c1 - c0 + 1);
-  auto slot_of = [&](int k) { return k == 0 ? 2 * c0 + 1 : 2 * (c0 + k); };
-  // CTAs between c0 and c1 whose range is empty (more CTAs than stages) wrote nothing
-  auto used = [&](int k) {
-    const int64_t c = c0 + k;
-    return k == 0 || range_start(c, T, ctas) < range_start(c + 1, T, ctas);
-  };
-  float mx = -INFINITY;
-  for (int k = threadIdx.x; k < np; k += 256) {
-    const float lv = used(k) ? pl[slot_of(k) * rows + r] : -INFINITY;
-    wsh[k] = lv;
-    mx = fmaxf(mx, lv);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if (lane == 0) red[0][warp] = mx;
-  __syncthreads();
-  float M = red[0][0];
-  for (int w = 1; w < 8; ++w) M = fmaxf(M, red[0][w]);
-  float z = 0.f;
-  for (int k = threadIdx.x; k < np; k += 256) {
-    const float e = wsh[k] == -INFINITY ? 0.f : expf(wsh[k] - M);
-    wsh[k] = e;
-    z += e;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-  if (lane == 0) red[1][warp] = z;
-  __syncthreads();
-  float Z = 0.f;
-  for (int w = 0; w < 8; ++w) Z += red[1][w];
-  float acc[VPL];
+  pdl_wait();
+  float m = -INFINITY, z = 0.f, acc[VPL];
 #pragma unroll
   for (int j = 0; j < VPL; ++j) acc[j] = 0.f;
 #pragma unroll 4
-  for (int k = warp; k < np; k += 8) {
-    const float wk = wsh[k];
-    if (wk > 0.f) {
-      const float *src = po + (slot_of(k) * rows + r) * D + lane * VPL;
-      if constexpr (VPL == 4) {
-        const float4 x = __ldg(reinterpret_cast<const float4 *>(src));
-        acc[0] += wk * x.x, acc[1] += wk * x.y, acc[2] += wk * x.z, acc[3] += wk * x.w;
-      } else {
-        const float2 x = __ldg(reinterpret_cast<const float2 *>(src));
-        acc[0] += wk * x.x, acc[1] += wk * x.y;
-      }
+  for (int k = warp; k < np; k += kMergeWarps) {
+    const int64_t c = c0 + k;
+    // CTAs between c0 and c1 whose range is empty (more CTAs than stages) wrote nothing
+    if (k > 0 && range_start(c, T, ctas) == range_start(c + 1, T, ctas)) continue;
+    const int64_t slot = k == 0 ? 2 * c0 + 1 : 2 * c;
+    const float lv = pl[slot * rows + r];
+    const float *src = po + (slot * rows + r) * D + lane * VPL;
+    float x[VPL];
+    if constexpr (VPL == 4) {
+      const float4 v = __ldg(reinterpret_cast<const float4 *>(src));
+      x[0] = v.x, x[1] = v.y, x[2] = v.z, x[3] = v.w;
+    } else {
+      const float2 v = __ldg(reinterpret_cast<const float2 *>(src));
+      x[0] = v.x, x[1] = v.y;
     }
+    if (lv == -INFINITY) continue;  // that split saw no key (its O is never used)
+    const float mn = fmaxf(m, lv);
+    const float sc = expf(m - mn), e = expf(lv - mn);
+    z = z * sc + e;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) acc[j] = acc[j] * sc + e * x[j];
+    m = mn;
   }
 #pragma unroll
   for (int j = 0; j < VPL; ++j) accs[warp][lane * VPL + j] = acc[j];
+  if (lane == 0) wm[warp] = m, wz[warp] = z;
   __syncthreads();
+  float M = wm[0];
+  for (int w = 1; w < kMergeWarps; ++w) M = fmaxf(M, wm[w]);
+  float Z = 0.f;
+  for (int w = 0; w < kMergeWarps; ++w) Z += wm[w] == -INFINITY ? 0.f : wz[w] * expf(wm[w] - M);
   const float inv = M == -INFINITY ? 0.f : 1.f / Z;
-  for (int d = threadIdx.x; d < D; d += 256) {
+  for (int d = threadIdx.x; d < D; d += kMergeWarps * 32) {
     float o = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) o += accs[w][d];
+    for (int w = 0; w < kMergeWarps; ++w)
+      if (wm[w] != -INFINITY) o += accs[w][d] * expf(wm[w] - M);
     out[row * D + d] = __half_as_ushort(__float2half_rn(o * inv));
   }
   if (threadIdx.x == 0 && lse) lse[row] = M == -INFINITY ? -INFINITY : M + logf(Z);
@@ -730,7 +753,7 @@ cudaError_t launch_d(const DecodeArgs &a, const KvView &cache, const DecodeMaps 
   const int64_t limit = cache.page_table ? static_cast<int64_t>(cache.max_pages) * kPage : cache.capacity;
   cudaLaunchConfig_t mc = {};
   mc.gridDim = dim3(a.batch * geo.groups, geo.hb * G);
-  mc.blockDim = dim3(256);
+  mc.blockDim = dim3(kMergeWarps * 32);
   mc.stream = stream;
   mc.attrs = attr;
   mc.numAttrs = 1;
