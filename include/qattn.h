@@ -89,7 +89,7 @@ typedef enum qattn_dtype {
 #define QATTN_PAGE_SIZE 64     /* tokens per page of a paged cache */
 #define QATTN_MAX_GROUP 8      /* largest Hq / Hkv */
 #define QATTN_MAX_SPLITS 1024  /* largest num_splits of qattn_decode */
-#define QATTN_MAX_BATCH 2048   /* largest batch of qattn_decode */
+#define QATTN_MAX_BATCH 1024   /* largest batch of qattn_decode */
 
 /* Bits of the device status word (qattn_read_device_flags). */
 #define QATTN_FLAG_WAIT_TIMEOUT 1u /* a pipeline wait gave up (kernel returned early) */

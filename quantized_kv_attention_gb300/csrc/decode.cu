@@ -55,20 +55,26 @@ struct Cfg {
   static constexpr int kCodeBytes = kRowsPerStage * D / 2;  // per tensor per stage
   static constexpr int kScaleBytes = kRowsPerStage * 2;
   static constexpr int kStageBytes = (2 * kCodeBytes + 2 * kScaleBytes + 1023) / 1024 * 1024;
-  static constexpr int kStages = D == 128 ? 4 : 8;
+  static constexpr int kStages = D == 128 ? 6 : 12;
   static constexpr int kQSlot = 4 * QATTN_MAX_GROUP * D * 2;  // Q rows of one segment (<= 4 kv-heads)
+  // fp32 row pitch of the cross-warp merge area laid over the last stage's
+  // buffer ([8 warps][8 q-heads][pitch]); with 4 words of padding the eight
+  // float4 stores of one quarter-warp (rows 2c, d = 4g) start 8c + 4g words
+  // apart modulo 32 banks, so they never share a bank
+  static constexpr int kMergePitch = D + 4;
+  static_assert(kConsumerWarps * 8 * kMergePitch * 4 <= kStageBytes, "merge area fits a stage");
   static constexpr int kRing = kStages * kStageBytes;
   static constexpr int kKBytes = D / 8;  // K code bytes per lane per token
   static constexpr int kWords = kKBytes / 4;
   static constexpr int kMt = D / 16;     // m-tiles of O^T, k-steps of S
 };
 
-// Dynamic shared memory: ring | 2 Q slots | merge (O per warp, q-head) | m, l |
-// prefix | lengths | barriers, flags.
+// Dynamic shared memory: ring | Q slot | m, l per (warp, q-head) | prefix |
+// lengths | barriers, flags.  The cross-warp merge reuses a ring slot.
 template <int D>
-__host__ __device__ constexpr int smem_bytes(int G, int batch) {
-  return Cfg<D>::kRing + 2 * Cfg<D>::kQSlot + kConsumerWarps * G * D * 4 + 2 * kConsumerWarps * 8 * 4 +
-         (2 * batch + 1) * 4 + (2 * Cfg<D>::kStages + 4) * 8 + Cfg<D>::kStages * 4 + 16 + 1024;
+__host__ __device__ constexpr int smem_bytes(int batch) {
+  return Cfg<D>::kRing + Cfg<D>::kQSlot + 2 * kConsumerWarps * 8 * 4 + (2 * batch + 1) * 4 +
+         (2 * Cfg<D>::kStages + 2) * 8 + Cfg<D>::kStages * 4 + 16 + 1024;
 }
 
 __device__ __forceinline__ void consumer_sync() {
@@ -154,18 +160,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  __half *qslot = reinterpret_cast<__half *>(smem + C::kRing);      // [2][rows of a segment][D]
-  float *smo = reinterpret_cast<float *>(smem + C::kRing + 2 * C::kQSlot);  // [warp][G][D]
-  float *smm = smo + kConsumerWarps * G * D;                          // [warp][8]
+  __half *qslot = reinterpret_cast<__half *>(smem + C::kRing);      // [rows of a segment][D]
+  float *smm = reinterpret_cast<float *>(smem + C::kRing + C::kQSlot);  // [warp][8]
   float *sml = smm + kConsumerWarps * 8;                              // [warp][8]
   int *prefix = reinterpret_cast<int *>(sml + kConsumerWarps * 8);    // [B + 1]
   int *lens = prefix + B + 1;                                         // [B], clamped
   uint64_t *full = reinterpret_cast<uint64_t *>(
       (reinterpret_cast<uintptr_t>(lens + B) + 7) & ~static_cast<uintptr_t>(7));
   uint64_t *empty = full + C::kStages;
-  uint64_t *qfull = empty + C::kStages;                               // [2]
-  uint64_t *qempty = qfull + 2;                                       // [2]
-  int *valid = reinterpret_cast<int *>(qempty + 2);                  // [kStages]: 0 = missing page
+  uint64_t *qfull = empty + C::kStages;
+  uint64_t *qempty = qfull + 1;
+  int *valid = reinterpret_cast<int *>(qempty + 1);                  // [kStages]: 0 = missing page
   volatile int *abort_flag = valid + C::kStages;                     // set after a timed-out wait
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -177,10 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(full + s), 1);
       mbar_init(smem_u32(empty + s), kConsumerWarps);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_u32(qfull + s), 1);
-      mbar_init(smem_u32(qempty + s), kConsumerWarps);
-    }
+    mbar_init(smem_u32(qfull), 1);
+    mbar_init(smem_u32(qempty), kConsumerWarps);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -238,15 +241,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int seg_len = lens[l.b];
         // the segment's Q rows (its head group's q-heads are contiguous)
         {
-          const int qs = seg & 1;
-          if (seg >= 2 && !mbar_wait(smem_u32(qempty + qs), ((seg >> 1) & 1) ^ 1, err,
+          if (seg >= 1 && !mbar_wait(smem_u32(qempty), (seg & 1) ^ 1, err,
                                      *abort_flag ? kDrainCycles : kWaitCycles)) {
             *abort_flag = 1;
             return;
           }
-          const uint32_t qf = smem_u32(qfull + qs);
+          const uint32_t qf = smem_u32(qfull);
           mbar_arrive_expect_tx(qf, qbytes);
-          bulk_g2s(smem_u32(qslot) + qs * C::kQSlot,
+          bulk_g2s(smem_u32(qslot),
                    a.q + (static_cast<int64_t>(l.b) * a.hq + static_cast<int64_t>(l.hg) * geo.hb * G) * D, qbytes, qf);
         }
         for (int j = 0; j < cnt; ++j, ++it) {
@@ -346,25 +348,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   const uint32_t ring = smem_u32(smem);
-  int slot = 0;          // ring slot of the next stage
-  uint32_t phase = 0;    // its mbarrier parity
-  int seg = 0;           // segment counter (Q slot seg & 1)
+  int cur = 0;           // ring slot of the next stage
+  uint32_t cur_ph = 0;   // its mbarrier parity
+  int seg = 0;           // segment counter (Q slot parity)
   for (int64_t gs = gs0; gs < gs1; ++seg) {
     const Loc l = locate(gs, prefix, B, geo.groups);
     const int cnt = static_cast<int>(min(static_cast<int64_t>(l.n - l.s), gs1 - gs));
     const int len = lens[l.b];
 
-    // Q of q-head g as the B operand.  Lane c covers d = c*D/4 + 8i + {0..7}
-    // (word i of its K code bytes); the decoder pairs (e, e+4), and nibble
-    // positions 1 and 3 come out 16x larger, so those columns carry q / 16.
+    // Q of q-head g as the B operand, from the segment's Q rows in shared
+    // memory.  Lane c covers d = c*D/4 + 8i + {0..7} (word i of its K code
+    // bytes); the decoder pairs (e, e+4), and nibble positions 1 and 3 come
+    // out 16x larger, so those columns carry q / 16.
     uint32_t qb[C::kMt][2];
     float qsum = 0.f;
     {
-      const int qs = seg & 1;
-      if (!mbar_wait(smem_u32(qfull + qs), (seg >> 1) & 1, err, *abort_flag ? kDrainCycles : kWaitCycles))
+      if (!mbar_wait(smem_u32(qfull), seg & 1, err, *abort_flag ? kDrainCycles : kWaitCycles))
         *abort_flag = 1;
       const int dbase = c * (D / 4);
-      const uint32_t qrow = smem_u32(qslot) + qs * C::kQSlot + ((hbw * G + min(g, G - 1)) * D + dbase) * 2;
+      const uint32_t qrow = smem_u32(qslot) + ((hbw * G + min(g, G - 1)) * D + dbase) * 2;
       const __half2 sixteenth = __float2half2_rn(0.0625f);
 #pragma unroll
       for (int i = 0; i < C::kWords; ++i) {
@@ -385,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(qempty + (seg & 1)));  // Q now lives in registers
+    if (lane == 0) mbar_arrive(smem_u32(qempty));  // Q now lives in registers
     qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
     qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
     // raw-unit bias 8 * sum(q) * 2^-24 for the lane's q-heads 2c and 2c+1
@@ -397,85 +399,61 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int mt = 0; mt < C::kMt; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
-    // Wait for the stage in `sl`; its tokens for this warp, or 0 if unusable.
-    auto acquire = [&](int sl, uint32_t ph, int j) -> int {
-      const bool got = mbar_wait(smem_u32(full + sl), ph, err, *abort_flag ? kDrainCycles : kWaitCycles);
-      if (!got) *abort_flag = 1;
-      const int nv = len - (l.s + j) * geo.tokens - tok_w;
-      return (got && valid[sl]) ? max(0, min(nv, 32)) : 0;
-    };
-    // S^T of the warp's 32 tokens in stage `sl`: two 16-token tiles, each
-    // split into two accumulation chains (even / odd code words).
-    auto qk = [&](int sl, float (&sa)[2][4]) {
-      const uint32_t kb = ring + sl * C::kStageBytes;
-      uint32_t kw[2][2][C::kWords];
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if constexpr (C::kWords == 4) {
-            const uint4 u = lds128(kb + koff[t][h]);
-            kw[t][h][0] = u.x, kw[t][h][1] = u.y, kw[t][h][2] = u.z, kw[t][h][3] = u.w;
-          } else {
-            const uint2 u = lds64(kb + koff[t][h]);
-            kw[t][h][0] = u.x, kw[t][h][1] = u.y;
-          }
-        }
-      float so[2][4];
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sa[t][e] = so[t][e] = 0.f;
-#pragma unroll
-      for (int i = 0; i < C::kWords; ++i)
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          uint32_t x0[4], x1[4];
-          decode_sub(kw[t][0][i], x0);
-          decode_sub(kw[t][1][i], x1);
-          if (i & 1) {
-            mma_16816(so[t], x0[0], x1[0], x0[1], x1[1], qb[2 * i][0], qb[2 * i][1]);
-            mma_16816(so[t], x0[2], x1[2], x0[3], x1[3], qb[2 * i + 1][0], qb[2 * i + 1][1]);
-          } else {
-            mma_16816(sa[t], x0[0], x1[0], x0[1], x1[1], qb[2 * i][0], qb[2 * i][1]);
-            mma_16816(sa[t], x0[2], x1[2], x0[3], x1[3], qb[2 * i + 1][0], qb[2 * i + 1][1]);
-          }
-        }
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sa[t][e] += so[t][e];
-    };
-
-    // Software pipeline: the QK of stage j+1 is issued before the softmax and
-    // PV of stage j, so the two dependency chains overlap in every warp.
-    float sacc[2][4], snext[2][4];
-    int cur = slot;
-    uint32_t cur_ph = phase;
-    int nvalid = acquire(cur, cur_ph, 0);
-    if (nvalid > 0) qk(cur, sacc);
+    int last = 0;  // slot of the segment's last stage: its buffer hosts the merge
     for (int j = 0; j < cnt; ++j) {
-      int nxt = cur + 1;
-      uint32_t nxt_ph = cur_ph;
-      if (nxt == C::kStages) nxt = 0, nxt_ph ^= 1u;
-      int nvalid_next = 0;
-      if (j + 1 < cnt) {
-        nvalid_next = acquire(nxt, nxt_ph, j + 1);
-        if (nvalid_next > 0) qk(nxt, snext);
-      }
+      const bool got = mbar_wait(smem_u32(full + cur), cur_ph, err, *abort_flag ? kDrainCycles : kWaitCycles);
+      if (!got) *abort_flag = 1;
+      const int nvalid =
+          (got && valid[cur]) ? max(0, min(len - (l.s + j) * geo.tokens - tok_w, 32)) : 0;
       if (nvalid > 0) {
-        const uint32_t vb = ring + cur * C::kStageBytes + C::kCodeBytes;
+        const uint32_t kb = ring + cur * C::kStageBytes;
+        const uint32_t vb = kb + C::kCodeBytes;
         const __half *sks = reinterpret_cast<const __half *>(smem + cur * C::kStageBytes + 2 * C::kCodeBytes) + sofs;
         const __half *svs = sks + kRowsPerStage;
+        // S^T of the warp's 32 tokens: two 16-token tiles, two accumulation
+        // chains each (even / odd code words)
+        uint32_t kw[2][2][C::kWords];
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if constexpr (C::kWords == 4) {
+              const uint4 u = lds128(kb + koff[t][h]);
+              kw[t][h][0] = u.x, kw[t][h][1] = u.y, kw[t][h][2] = u.z, kw[t][h][3] = u.w;
+            } else {
+              const uint2 u = lds64(kb + koff[t][h]);
+              kw[t][h][0] = u.x, kw[t][h][1] = u.y;
+            }
+          }
+        float sacc[2][4], so[2][4];
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sacc[t][e] = so[t][e] = 0.f;
+#pragma unroll
+        for (int i = 0; i < C::kWords; ++i)
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            uint32_t x0[4], x1[4];
+            decode_sub(kw[t][0][i], x0);
+            decode_sub(kw[t][1][i], x1);
+            if (i & 1) {
+              mma_16816(so[t], x0[0], x1[0], x0[1], x1[1], qb[2 * i][0], qb[2 * i][1]);
+              mma_16816(so[t], x0[2], x1[2], x0[3], x1[3], qb[2 * i + 1][0], qb[2 * i + 1][1]);
+            } else {
+              mma_16816(sacc[t], x0[0], x1[0], x0[1], x1[1], qb[2 * i][0], qb[2 * i][1]);
+              mma_16816(sacc[t], x0[2], x1[2], x0[3], x1[3], qb[2 * i + 1][0], qb[2 * i + 1][1]);
+            }
+          }
         float ts[2][4], fv[2][2];
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           const int lt = tok_w + t * 16 + g;
           const float f0 = __half2float(sks[lt]) * kf, f1 = __half2float(sks[lt + 8]) * kf;
-          ts[t][0] = (sacc[t][0] - bq0) * f0;
-          ts[t][1] = (sacc[t][1] - bq1) * f0;
-          ts[t][2] = (sacc[t][2] - bq0) * f1;
-          ts[t][3] = (sacc[t][3] - bq1) * f1;
+          ts[t][0] = (sacc[t][0] + so[t][0] - bq0) * f0;
+          ts[t][1] = (sacc[t][1] + so[t][1] - bq1) * f0;
+          ts[t][2] = (sacc[t][2] + so[t][2] - bq0) * f1;
+          ts[t][3] = (sacc[t][3] + so[t][3] - bq1) * f1;
           // the V scale carries an exact 2^-8: with a lazily raised max p can
           // reach 2^8, and p * s_V must stay inside the fp16 range
           fv[t][0] = __half2float(svs[lt]) * 0.00390625f;
@@ -542,15 +520,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(empty + cur));
-#pragma unroll
-      for (int t = 0; t < 2; ++t)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) sacc[t][e] = snext[t][e];
-      cur = nxt, cur_ph = nxt_ph, nvalid = nvalid_next;
+      if (j + 1 < cnt) {
+        if (lane == 0) mbar_arrive(smem_u32(empty + cur));
+      } else {
+        last = cur;  // released after the merge below
+      }
+      if (++cur == C::kStages) cur = 0, cur_ph ^= 1u;
     }
-    slot = cur, phase = cur_ph;  // the stage after this segment's last
+
     // --------------------------------------------- segment end: merge warps
+    // The last stage's buffer (every warp still holds it) becomes the merge
+    // area: [warp][q-head][D + pad] fp32, written as float4 runs along d.
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       l0 += __shfl_xor_sync(0xffffffffu, l0, off);
@@ -558,31 +538,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       ps0 += __shfl_xor_sync(0xffffffffu, ps0, off);
       ps1 += __shfl_xor_sync(0xffffffffu, ps1, off);
     }
+    consumer_sync();  // every warp has read its last stage
+    float *mo = reinterpret_cast<float *>(smem + last * C::kStageBytes);
+    // O^T m-tile jp*4+k holds d = 64 jp + 4 g + k (rows g) and +32 (rows g+8);
+    // nibble positions 1 and 3 (odd k) came out 16x larger; P' carried 2^-8.
 #pragma unroll
-    for (int jp = 0; jp < D / 64; ++jp)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int mt = jp * 4 + k;
-        const float fac = (k & 1) ? kTwo24 / 16.f : kTwo24;
-        const int dlo = 64 * jp + 4 * g + k, dhi = dlo + 32;
-        if (2 * c < G) {  // P' carried 2^-8
-          float *w0 = smo + (warp * G + 2 * c) * D;
-          w0[dlo] = (o[mt][0] * fac - 8.f * ps0) * 256.f;
-          w0[dhi] = (o[mt][2] * fac - 8.f * ps0) * 256.f;
-        }
-        if (2 * c + 1 < G) {
-          float *w1 = smo + (warp * G + 2 * c + 1) * D;
-          w1[dlo] = (o[mt][1] * fac - 8.f * ps1) * 256.f;
-          w1[dhi] = (o[mt][3] * fac - 8.f * ps1) * 256.f;
-        }
-      }
+    for (int jq = 0; jq < D / 32; ++jq) {  // d = 32 jq + 4 g + {0..3}
+      const int jp = jq >> 1, hi = jq & 1;
+      float4 v0, v1;
+      v0.x = (o[jp * 4 + 0][2 * hi] * kTwo24 - 8.f * ps0) * 256.f;
+      v0.y = (o[jp * 4 + 1][2 * hi] * (kTwo24 / 16.f) - 8.f * ps0) * 256.f;
+      v0.z = (o[jp * 4 + 2][2 * hi] * kTwo24 - 8.f * ps0) * 256.f;
+      v0.w = (o[jp * 4 + 3][2 * hi] * (kTwo24 / 16.f) - 8.f * ps0) * 256.f;
+      v1.x = (o[jp * 4 + 0][2 * hi + 1] * kTwo24 - 8.f * ps1) * 256.f;
+      v1.y = (o[jp * 4 + 1][2 * hi + 1] * (kTwo24 / 16.f) - 8.f * ps1) * 256.f;
+      v1.z = (o[jp * 4 + 2][2 * hi + 1] * kTwo24 - 8.f * ps1) * 256.f;
+      v1.w = (o[jp * 4 + 3][2 * hi + 1] * (kTwo24 / 16.f) - 8.f * ps1) * 256.f;
+      const int d = 32 * jq + 4 * g;
+      if (2 * c < G) *reinterpret_cast<float4 *>(mo + (warp * 8 + 2 * c) * C::kMergePitch + d) = v0;
+      if (2 * c + 1 < G) *reinterpret_cast<float4 *>(mo + (warp * 8 + 2 * c + 1) * C::kMergePitch + d) = v1;
+    }
     if (g == 0) {
       smm[warp * 8 + 2 * c] = m0, smm[warp * 8 + 2 * c + 1] = m1;
       sml[warp * 8 + 2 * c] = l0, sml[warp * 8 + 2 * c + 1] = l1;
     }
     consumer_sync();
     const bool complete = l.s == 0 && cnt == l.n;
-    const int64_t slot = l.s > 0 ? 2 * static_cast<int64_t>(blockIdx.x) : 2 * static_cast<int64_t>(blockIdx.x) + 1;
+    const int64_t pslot = l.s > 0 ? 2 * static_cast<int64_t>(blockIdx.x) : 2 * static_cast<int64_t>(blockIdx.x) + 1;
     for (int idx = threadIdx.x; idx < geo.hb * G * D; idx += kConsumerWarps * 32) {
       const int hh = idx / (G * D), rem = idx - hh * G * D;  // kv-head in stage, q-head, d
       const int h = rem / D, d = rem - h * D;
@@ -593,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int w = 0; w < geo.wph; ++w) {
         const float sc = ex2(smm[(w0 + w) * 8 + h] - M);
         L += sc * sml[(w0 + w) * 8 + h];
-        acc += sc * smo[((w0 + w) * G + h) * D + d];
+        acc += sc * mo[((w0 + w) * 8 + h) * C::kMergePitch + d];
       }
       const bool live = L > 0.f;
       const float ov = live ? acc / L : 0.f;
@@ -603,12 +585,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         a.out[row * D + d] = __half_as_ushort(__float2half_rn(ov));
         if (d == 0 && a.lse) a.lse[row] = lse_v;
       } else {
-        const int64_t prow = slot * geo.hb * G + hh * G + h;
+        const int64_t prow = pslot * geo.hb * G + hh * G + h;
         a.partial_o[prow * D + d] = ov;
         if (d == 0) a.partial_lse[prow] = lse_v;
       }
     }
-    consumer_sync();  // the merge buffer is free again
+    consumer_sync();  // the merge area is read; the stage can be refilled
+    if (lane == 0) mbar_arrive(smem_u32(empty + last));
     gs += cnt;
   }
 }
@@ -731,7 +714,7 @@ cudaError_t launch_d(const DecodeArgs &a, const KvView &cache, const DecodeMaps 
   static bool configured = false;  // per-function attribute, set once per process
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem_bytes<D>(QATTN_MAX_GROUP, QATTN_MAX_BATCH));
+                                         smem_bytes<D>(QATTN_MAX_BATCH));
     if (e != cudaSuccess) return e;
     configured = true;
   }
@@ -744,7 +727,7 @@ cudaError_t launch_d(const DecodeArgs &a, const KvView &cache, const DecodeMaps 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.ctas);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem_bytes<D>(G, a.batch);
+  cfg.dynamicSmemBytes = smem_bytes<D>(a.batch);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -775,10 +758,6 @@ DecodeGeometry decode_geometry(int head_dim, int hkv, bool paged) {
   r.box_tokens = paged ? (g.tokens > kPage ? kPage : g.tokens) : g.tokens;
   r.box_rows = r.box_tokens * head_dim / 256;
   return r;
-}
-
-int decode_smem_bytes(int head_dim, int group, int batch) {
-  return head_dim == 128 ? smem_bytes<128>(group, batch) : smem_bytes<64>(group, batch);
 }
 
 cudaError_t launch_decode(const DecodeArgs &a, const KvView &cache, const DecodeMaps &maps, uint32_t *err,

@@ -51,7 +51,6 @@ DecodeGeometry decode_geometry(int head_dim, int hkv, bool paged);
 struct DecodeMaps {
   CUtensorMap k, v, ks, vs;  // codes 3-D [heads][rows][128 B], scales 2-D [heads][tokens]
 };
-int decode_smem_bytes(int head_dim, int group, int batch);
 cudaError_t launch_decode(const DecodeArgs &a, const KvView &cache, const DecodeMaps &maps, uint32_t *err,
                           cudaStream_t stream);
 
