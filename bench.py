@@ -511,7 +511,7 @@ def run_prefill(name, args, device, gpu_index, rank, steps=None):
     peaks, pk_src = measured_peaks()
     achieved = flops / (pf_ms / 1e3) / 1e12
     peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    traffic = profiled_traffic(f"prefill_{name}_ncu.txt", source_digest("prefill.cu", "ptx.cuh"), flops)
+    traffic = profiled_traffic(f"prefill_{name}_ncu.txt", source_digest("prefill.cu", "ptx.cuh", "umma.cuh"), flops)
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(tmax * 1e3 / steps, 4),

@@ -80,20 +80,28 @@ EncodeFn encode_fn() {
   return fn;
 }
 
-// 2-D view of a code buffer as rows of 128 bytes; one box = one 64-token stage.
-qattn_status code_map(CUtensorMap *map, const void *base, uint64_t bytes, int head_dim) {
+// Prefill maps over q and out [batch*Hq, nq, D] fp16 (128B swizzle, 64
+// columns per box): Q boxes of 128 rows (loads), O boxes of 32 rows (one
+// warp's stores).  Rows past nq read as zero and are never written.
+qattn_status prefill_maps(CUtensorMap *qmap, CUtensorMap *omap, const void *q, const void *out, int batch, int hq,
+                          int nq, int head_dim) {
   EncodeFn enc = encode_fn();
   if (!enc) return fail(QATTN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
-  const uint64_t rows = bytes / 128;
-  if (rows == 0 || rows > 0x7fffffffull) return fail(QATTN_ERR_UNSUPPORTED, "code buffer of %llu bytes", (unsigned long long)bytes);
-  cuuint64_t dims[2] = {128, rows};
-  cuuint64_t strides[1] = {128};
-  cuuint32_t box[2] = {128, static_cast<cuuint32_t>(kPage * head_dim / 2 / 128)};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box,
-                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(QATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  const uint64_t heads = static_cast<uint64_t>(batch) * hq;
+  if (heads > 0x7fffffffull) return fail(QATTN_ERR_UNSUPPORTED, "batch * Hq too large");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(nq), heads};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2, static_cast<cuuint64_t>(nq) * head_dim * 2};
+  cuuint32_t es[3] = {1, 1, 1};
+  const void *bases[2] = {q, out};
+  CUtensorMap *maps[2] = {qmap, omap};
+  const cuuint32_t rows[2] = {128, 32};
+  for (int i = 0; i < 2; ++i) {
+    cuuint32_t box[3] = {64, rows[i], 1};
+    CUresult r = enc(maps[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(bases[i]), dims, strides, box,
+                     es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(QATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for prefill map %d", (int)r, i);
+  }
   return QATTN_OK;
 }
 
@@ -318,14 +326,13 @@ qattn_status qattn_prefill(const uint16_t *q, const qattn_kv_cache *cache, int32
   if (!aligned16(q) || !aligned16(out)) return fail(QATTN_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
   DeviceState *ds;
   if ((st = device_state(&ds)) != QATTN_OK) return st;
-  CUtensorMap kmap, vmap;
-  if ((st = code_map(&kmap, view.k_codes, code_bytes, view.head_dim)) != QATTN_OK) return st;
-  if ((st = code_map(&vmap, view.v_codes, code_bytes, view.head_dim)) != QATTN_OK) return st;
+  CUtensorMap qmap, omap;
+  if ((st = prefill_maps(&qmap, &omap, q, out, batch, num_q_heads, nq, view.head_dim)) != QATTN_OK) return st;
   PrefillArgs a;
   a.q = q, a.out = out, a.lse = lse;
   a.batch = batch, a.hq = num_q_heads, a.nq = nq, a.nk = nk, a.causal = causal;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
-  cudaError_t e = launch_prefill(a, view, kmap, vmap, ds->status, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_prefill(a, view, qmap, omap, ds->status, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "prefill launch");
 }
 

@@ -67,8 +67,10 @@ struct PrefillArgs {
   int batch, hq, nq, nk, causal;
   float scale_log2;
 };
-cudaError_t launch_prefill(const PrefillArgs &a, const KvView &cache, const CUtensorMap &kmap,
-                           const CUtensorMap &vmap, uint32_t *err, cudaStream_t stream);
+// qmap / omap: 3-D [batch*Hq][nq][D] fp16, 128B swizzle, boxes of 64 columns
+// x 128 rows (Q) and x 32 rows (O).
+cudaError_t launch_prefill(const PrefillArgs &a, const KvView &cache, const CUtensorMap &qmap,
+                           const CUtensorMap &omap, uint32_t *err, cudaStream_t stream);
 
 // api.cu: sets the message returned by qattn_last_error() on this thread.
 void record_error(const char *msg);
