@@ -38,8 +38,12 @@ constexpr int kBM = 128;  // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;  // keys per tile
 constexpr int kSoftmaxThreads = 256;
 constexpr int kDequantThreads = 128;
-constexpr int kMmaWarp = 12;
-constexpr int kThreads = kSoftmaxThreads + kDequantThreads + 32;  // 416
+constexpr int kMmaWarp = 12;        // warpgroup 3; its other three warps idle
+constexpr int kThreads = 512;       // four warpgroups: softmax 0, softmax 1, dequant, MMA
+// Registers per thread after the split (launch: 128); one warp of every
+// warpgroup sits on each SM sub-partition, so the per-partition total stays
+// 160 + 160 + 96 + 96 = 512 = 4 x 128.
+constexpr int kRegsSoftmax = 160, kRegsDequant = 96, kRegsMma = 96;
 constexpr int kKvBufs = 2;
 constexpr int kScaleSlots = 4;
 constexpr int kRedoSum = 256;  // a tile whose sum of 2^x exceeds this moves the max
@@ -141,6 +145,34 @@ __device__ __forceinline__ void store_row(uint32_t tile, int tok, const uint4 (&
   }
 }
 
+// Multiplies the P chunks already written (c of them) and, when `o_too`,
+// the O row by alpha.  Out of line: it runs only when a row maximum moves.
+template <int D>
+__device__ __noinline__ void rescale_tmem(uint32_t s_tm, uint32_t o_tm, int c, bool o_too, float alpha) {
+  tmem_st_wait();
+#pragma unroll 1
+  for (int c2 = 0; c2 < c; ++c2) {
+    uint32_t ph[16];
+    tmem_ld16(s_tm + c2 * 16, ph);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float2 f = __half22float2(*reinterpret_cast<__half2 *>(&ph[i]));
+      ph[i] = pack_half2(f.x * alpha, f.y * alpha);
+    }
+    tmem_st16(s_tm + c2 * 16, ph);
+  }
+  if (o_too) {
+#pragma unroll 1
+    for (int c2 = 0; c2 < D / 32; ++c2) {
+      uint32_t o[32];
+      tmem_ld32(o_tm + c2 * 32, o);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+      tmem_st32(o_tm + c2 * 32, o);
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(PrefillArgs a, KvView cache, const __grid_constant__ CUtensorMap qmap,
@@ -184,10 +216,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
+  const int wg = warp >> 2;
 
-  if (warp == kMmaWarp) {
+  // Each role sets its register budget inside its own branch, so that the
+  // compiler allocates every branch for that budget.
+  if (wg == 3) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsMma));
     // ------------------------------------------------------------ MMA issue
-    if (lane == 0) {
+    if (warp == kMmaWarp && lane == 0) {
       prefetch_tmap(&qmap);
       const uint32_t qf = smem_u32(&bars->q_full);
       mbar_arrive_expect_tx(qf, 2 * C::kTileBytes);
@@ -196,22 +232,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(sbase + C::kQOff + t * C::kTileBytes + s * C::kSubBytes, &qmap, 64 * s, w.r[t],
                       w.b * a.hq + w.h[t], qf);
       bool ok = mbar_wait(qf, 0, err);
+      // Descriptors are built once; a start address moves by adding its
+      // 16-byte-unit offset to the low field (addresses stay below 256 KB).
+      const uint64_t qdesc = sw128_desc(sbase + C::kQOff, 16, 1024);
+      const uint64_t kdesc = sw128_desc(sbase + C::kKOff, 16, 1024);
+      const uint64_t vdesc = sw128_desc(sbase + C::kVOff, C::kSubBytes, 1024);
+      constexpr uint32_t kTile16 = C::kTileBytes >> 4;
       auto issue_s = [&](int t, int j) {
-        const uint32_t qa = sbase + C::kQOff + t * C::kTileBytes;
-        const uint32_t kb = sbase + C::kKOff + (j % kKvBufs) * C::kTileBytes;
+        const uint64_t qa = qdesc + t * kTile16, kb = kdesc + (j % kKvBufs) * kTile16;
+        const uint32_t d = tmem + t * kBN;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * C::kSubBytes + (kk % 4) * 32;
-          umma_ss(tmem + t * kBN, sw128_desc(qa + off, 16, 1024), sw128_desc(kb + off, 16, 1024), C::kIdescS,
-                  kk > 0);
+          const uint32_t off = ((kk / 4) * C::kSubBytes + (kk % 4) * 32) >> 4;
+          umma_ss(d, qa + off, kb + off, C::kIdescS, kk > 0);
         }
       };
       auto issue_pv = [&](int t, int j) {
-        const uint32_t vb = sbase + C::kVOff + (j % kKvBufs) * C::kTileBytes;
+        const uint64_t vb = vdesc + (j % kKvBufs) * kTile16;
+        const uint32_t d = tmem + 256 + t * D, p = tmem + t * kBN;
+        const uint32_t acc0 = j > 0;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          umma_ts(tmem + 256 + t * D, tmem + t * kBN + kk * 8, sw128_desc(vb + kk * 2048, C::kSubBytes, 1024),
-                  C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kBN / 16; ++kk) umma_ts(d, p + kk * 8, vb + kk * (2048 >> 4), C::kIdescPV, kk > 0 ? 1u : acc0);
       };
       if (ok) ok = mbar_wait(smem_u32(&bars->k_full[0]), 0, err);
       if (ok) {
@@ -253,7 +294,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(smem_u32(&bars->o_full), 0, err, ok ? kWaitCycles : kDrainCycles);
     }
     __syncwarp();
-  } else if (warp >= kSoftmaxThreads / 32) {
+  } else if (wg == 2) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsDequant));
     // ---------------------------------------------------- dequantization
     const int tok_l = threadIdx.x - kSoftmaxThreads;  // token within the tile
     const int64_t row0 = (static_cast<int64_t>(w.b) * cache.hkv + w.kvh) * cache.capacity;
@@ -261,29 +303,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint4 *vc = reinterpret_cast<const uint4 *>(cache.v_codes + row0 * (D / 2));
     const __half *ks = reinterpret_cast<const __half *>(cache.k_scales) + row0;
     const __half *vs = reinterpret_cast<const __half *>(cache.v_scales) + row0;
-    uint4 ck[D / 32], cv[D / 32];
-    float fk = 0.f, fv = 0.f;
-    auto load = [&](int j, uint4(&k4)[D / 32], uint4(&v4)[D / 32], float &sk, float &sv) {
+    // No prefetch across tiles: the two operand buffers let this warpgroup
+    // run up to two tiles ahead of the tensor core, which hides the load.
+    for (int j = 0; j < n; ++j) {
       const int tok = j * kBN + tok_l;
+      uint4 ck[D / 32], cv[D / 32];
+      float fk = 0.f, fv = 0.f;
       if (tok < a.nk) {
 #pragma unroll
         for (int i = 0; i < D / 32; ++i) {
-          k4[i] = __ldg(kc + static_cast<int64_t>(tok) * (D / 32) + i);
-          v4[i] = __ldg(vc + static_cast<int64_t>(tok) * (D / 32) + i);
+          ck[i] = __ldg(kc + static_cast<int64_t>(tok) * (D / 32) + i);
+          cv[i] = __ldg(vc + static_cast<int64_t>(tok) * (D / 32) + i);
         }
-        sk = __half2float(ks[tok]) * a.scale_log2;
-        sv = __half2float(vs[tok]);
+        fk = __half2float(ks[tok]) * a.scale_log2;
+        fv = __half2float(vs[tok]);
       } else {
 #pragma unroll
-        for (int i = 0; i < D / 32; ++i) k4[i] = v4[i] = make_uint4(0, 0, 0, 0);
-        sk = 0.f, sv = 0.f;
+        for (int i = 0; i < D / 32; ++i) ck[i] = cv[i] = make_uint4(0, 0, 0, 0);
       }
-    };
-    if (n > 0) load(0, ck, cv, fk, fv);
-    for (int j = 0; j < n; ++j) {
-      uint4 nk4[D / 32], nv4[D / 32];
-      float nfk = 0.f, nfv = 0.f;
-      if (j + 1 < n) load(j + 1, nk4, nv4, nfk, nfv);
       const int buf = j % kKvBufs;
       const uint32_t par = ((j / kKvBufs) & 1) ^ 1;
       if (j >= kKvBufs && !mbar_wait(smem_u32(&bars->k_empty[buf]), par, err)) break;
@@ -301,11 +338,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       store_row<D>(sbase + C::kVOff + buf * C::kTileBytes, tok_l, cv);
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&bars->v_full[buf]));
-#pragma unroll
-      for (int i = 0; i < D / 32; ++i) ck[i] = nk4[i], cv[i] = nv4[i];
-      fk = nfk, fv = nfv;
     }
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     // ------------------------------------------------------------ softmax
     const int t = warp >> 2, wq = warp & 3;
     const int row_l = wq * 32 + lane;
@@ -388,28 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float mn = fmaxf(m, chunk_max(s, c));
           const float alpha = ex2(m - mn);
           m = mn, l *= alpha, tsum *= alpha;
-          if (c > 0) {
-            tmem_st_wait();
-            for (int c2 = 0; c2 < c; ++c2) {
-              uint32_t ph[16];
-              tmem_ld16(s_tm + c2 * 16, ph);
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float2 f = __half22float2(*reinterpret_cast<__half2 *>(&ph[i]));
-                ph[i] = pack_half2(f.x * alpha, f.y * alpha);
-              }
-              tmem_st16(s_tm + c2 * 16, ph);
-            }
-          }
-          if (j > 0) {
-            for (int c2 = 0; c2 < D / 32; ++c2) {
-              uint32_t o[32];
-              tmem_ld32(o_tm + c2 * 32, o);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-              tmem_st32(o_tm + c2 * 32, o);
-            }
-          }
+          rescale_tmem<D>(s_tm, o_tm, c, j > 0, alpha);
+          tmem_ld32(s_tm + c * 32, s);  // S chunk c is intact: P so far only covers chunks < c/2
           cs = chunk_exp(s, c, h);
         }
         tsum += cs;
