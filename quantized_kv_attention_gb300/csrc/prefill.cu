@@ -21,11 +21,16 @@
 //                       O_t += P_t . codes_V    (M=128, N=D, K=128; P from TMEM)
 //   softmax warps (2x4) one thread per query row: x = S*kf - m, p = 2^x,
 //                       P = fp16(p * vf) back into TMEM over S; lazy max:
-//                       m moves only when a tile's sum exceeds 2^8, then O is
-//                       rescaled in TMEM before the next PV
+//                       m moves only when a 32-key chunk's sum exceeds 2^8,
+//                       then P so far and O are rescaled in TMEM
 // TMEM: S_0 | S_1 | O_0 | O_1 (512 columns).  The epilogue divides O by the
 // row sum, stages it in the Q tile's shared memory and stores it with TMA.
+// Codes unpack to fp16 in the order d0 d4 d1 d5 d2 d6 d3 d7 inside every
+// group of 8 columns (the cheapest unpack); warpgroup 3 permutes Q the same
+// way once per CTA and the epilogue restores the order of O.
 #include <math.h>
+
+#include <type_traits>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -72,6 +77,21 @@ struct Bars {
   uint64_t sc_full[kScaleSlots], sc_empty[kScaleSlots];
   uint32_t tmem_base;
 };
+
+// Bounded mbarrier wait; the clock is read once every 32 polls so that a
+// waiting warp takes few issue slots from the working ones.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint32_t *err,
+                                           long long limit = kWaitCycles) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0 && clock64() - t0 > limit) {
+      atomicOr(err, kFlagWaitTimeout);
+      return false;
+    }
+  }
+}
 
 // One (query-tile pair) work item.
 struct Work {
@@ -121,10 +141,15 @@ __device__ __forceinline__ uint32_t nibble_pair(uint32_t w) {
   return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// 8 codes (one 32-bit word, element order) -> 16 bytes of fp16 at `dst`.
+// 8 codes (one 32-bit word) -> 16 bytes of fp16 at `dst`, in the order
+// d0 d4 d1 d5 d2 d6 d3 d7 that decode_nibbles yields.  Q is permuted the
+// same way inside every 8-column group (the contraction over d does not
+// see it) and the epilogue undoes it on O.
 __device__ __forceinline__ void store_word(uint32_t dst, uint32_t w) {
-  const uint32_t a = nibble_pair<0>(w), b = nibble_pair<1>(w), c = nibble_pair<2>(w), d = nibble_pair<3>(w);
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+  uint32_t x[4];
+  decode_nibbles(w, x);
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(x[0]), "r"(x[1]), "r"(x[2]), "r"(x[3])
+               : "memory");
 }
 
 // Writes one token row (D codes) as fp16 into a 128B-swizzled tile whose
@@ -171,6 +196,62 @@ __device__ __noinline__ void rescale_tmem(uint32_t s_tm, uint32_t o_tm, int c, b
       tmem_st32(o_tm + c2 * 32, o);
     }
   }
+}
+
+// Maximum of S * kf over one 32-key chunk; keys above `limit` are excluded
+// when MASK.  kf: shared address of the chunk's 32 factors; k0: its first key.
+template <bool MASK>
+__device__ __forceinline__ float chunk_max(const uint32_t (&s)[32], uint32_t kf, int k0, int limit) {
+  float mx = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 32; i += 4) {
+    const uint4 f = lds128(kf + i * 4);
+    float2 x01 = f2_split(mul2(f2(__uint_as_float(s[i]), __uint_as_float(s[i + 1])),
+                               f2(__uint_as_float(f.x), __uint_as_float(f.y))));
+    float2 x23 = f2_split(mul2(f2(__uint_as_float(s[i + 2]), __uint_as_float(s[i + 3])),
+                               f2(__uint_as_float(f.z), __uint_as_float(f.w))));
+    if (MASK) {
+      if (k0 + i > limit) x01.x = -INFINITY;
+      if (k0 + i + 1 > limit) x01.y = -INFINITY;
+      if (k0 + i + 2 > limit) x23.x = -INFINITY;
+      if (k0 + i + 3 > limit) x23.y = -INFINITY;
+    }
+    mx = fmax3(mx, x01.x, x01.y);
+    mx = fmax3(mx, x23.x, x23.y);
+  }
+  return mx;
+}
+
+// p = 2^(S * kf - m) over one chunk, lanes paired in f32x2 arithmetic; h gets
+// fp16 pairs of p * vf (the P operand); returns the sum of p.
+template <bool MASK>
+__device__ __forceinline__ float chunk_exp(const uint32_t (&s)[32], uint32_t kf, uint32_t vf, float m, int k0,
+                                           int limit, uint32_t (&h)[16]) {
+  const uint64_t nm = f2(-m, -m);
+  uint64_t acc0 = f2(0.f, 0.f), acc1 = f2(0.f, 0.f);
+#pragma unroll
+  for (int i = 0; i < 32; i += 4) {
+    const uint4 f = lds128(kf + i * 4);
+    const uint4 g = lds128(vf + i * 4);
+    float2 x01 = f2_split(fma2(f2(__uint_as_float(s[i]), __uint_as_float(s[i + 1])),
+                               f2(__uint_as_float(f.x), __uint_as_float(f.y)), nm));
+    float2 x23 = f2_split(fma2(f2(__uint_as_float(s[i + 2]), __uint_as_float(s[i + 3])),
+                               f2(__uint_as_float(f.z), __uint_as_float(f.w)), nm));
+    if (MASK) {
+      if (k0 + i > limit) x01.x = -INFINITY;
+      if (k0 + i + 1 > limit) x01.y = -INFINITY;
+      if (k0 + i + 2 > limit) x23.x = -INFINITY;
+      if (k0 + i + 3 > limit) x23.y = -INFINITY;
+    }
+    const uint64_t p01 = f2(ex2(x01.x), ex2(x01.y)), p23 = f2(ex2(x23.x), ex2(x23.y));
+    acc0 = add2(acc0, p01), acc1 = add2(acc1, p23);
+    const float2 q01 = f2_split(mul2(p01, f2(__uint_as_float(g.x), __uint_as_float(g.y))));
+    const float2 q23 = f2_split(mul2(p23, f2(__uint_as_float(g.z), __uint_as_float(g.w))));
+    h[i / 2] = pack_half2(q01.x, q01.y);
+    h[i / 2 + 1] = pack_half2(q23.x, q23.y);
+  }
+  const float2 t2 = f2_split(add2(acc0, acc1));
+  return t2.x + t2.y;
 }
 
 template <int D>
@@ -223,15 +304,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (wg == 3) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsMma));
     // ------------------------------------------------------------ MMA issue
+    const uint32_t qf = smem_u32(&bars->q_full);
     if (warp == kMmaWarp && lane == 0) {
       prefetch_tmap(&qmap);
-      const uint32_t qf = smem_u32(&bars->q_full);
       mbar_arrive_expect_tx(qf, 2 * C::kTileBytes);
       for (int t = 0; t < 2; ++t)
         for (int s = 0; s < C::kSub; ++s)
           tma_load_3d(sbase + C::kQOff + t * C::kTileBytes + s * C::kSubBytes, &qmap, 64 * s, w.r[t],
                       w.b * a.hq + w.h[t], qf);
-      bool ok = mbar_wait(qf, 0, err);
+    }
+    // Q columns into the K operand's order (d0 d4 d1 d5 d2 d6 d3 d7 per group of 8)
+    const bool qok = wait_bounded(qf, 0, err);
+    if (qok) {
+      for (int ch = threadIdx.x - 3 * 128; ch < 2 * C::kTileBytes / 16; ch += 128) {
+        const uint32_t addr = sbase + C::kQOff + ch * 16;
+        uint4 v = lds128(addr);
+        uint32_t n0, n1, n2, n3;
+        asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(n0) : "r"(v.x), "r"(v.z));
+        asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(n1) : "r"(v.x), "r"(v.z));
+        asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(n2) : "r"(v.y), "r"(v.w));
+        asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(n3) : "r"(v.y), "r"(v.w));
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(n0), "r"(n1), "r"(n2), "r"(n3)
+                     : "memory");
+      }
+      fence_proxy_async_smem();
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+    if (warp == kMmaWarp && lane == 0) {
+      bool ok = qok;
       // Descriptors are built once; a start address moves by adding its
       // 16-byte-unit offset to the low field (addresses stay below 256 KB).
       const uint64_t qdesc = sw128_desc(sbase + C::kQOff, 16, 1024);
@@ -254,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) umma_ts(d, p + kk * 8, vb + kk * (2048 >> 4), C::kIdescPV, kk > 0 ? 1u : acc0);
       };
-      if (ok) ok = mbar_wait(smem_u32(&bars->k_full[0]), 0, err);
+      if (ok) ok = wait_bounded(smem_u32(&bars->k_full[0]), 0, err);
       if (ok) {
         tc_fence_after();
         issue_s(0, 0);
@@ -266,19 +366,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; ok && j < n; ++j) {
         const int vbuf = j % kKvBufs;
         const uint32_t par = (j / kKvBufs) & 1;
-        if (!(ok = mbar_wait(smem_u32(&bars->v_full[vbuf]), par, err))) break;
-        if (!(ok = mbar_wait(smem_u32(&bars->p_full[0]), j & 1, err))) break;
+        if (!(ok = wait_bounded(smem_u32(&bars->v_full[vbuf]), par, err))) break;
+        if (!(ok = wait_bounded(smem_u32(&bars->p_full[0]), j & 1, err))) break;
         tc_fence_after();
         issue_pv(0, j);
         const bool more = j + 1 < n;
         if (more) {
           const int kb = (j + 1) % kKvBufs;
-          if (!(ok = mbar_wait(smem_u32(&bars->k_full[kb]), ((j + 1) / kKvBufs) & 1, err))) break;
+          if (!(ok = wait_bounded(smem_u32(&bars->k_full[kb]), ((j + 1) / kKvBufs) & 1, err))) break;
           tc_fence_after();
           issue_s(0, j + 1);
           tc_commit(smem_u32(&bars->s_full[0]));
         }
-        if (!(ok = mbar_wait(smem_u32(&bars->p_full[1]), j & 1, err))) break;
+        if (!(ok = wait_bounded(smem_u32(&bars->p_full[1]), j & 1, err))) break;
         tc_fence_after();
         issue_pv(1, j);
         tc_commit(smem_u32(&bars->v_empty[vbuf]));
@@ -291,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Always signal o_full so waiters end; then let every MMA finish
       // before the tensor memory is released.
       tc_commit(smem_u32(&bars->o_full));
-      mbar_wait(smem_u32(&bars->o_full), 0, err, ok ? kWaitCycles : kDrainCycles);
+      wait_bounded(smem_u32(&bars->o_full), 0, err, ok ? kWaitCycles : kDrainCycles);
     }
     __syncwarp();
   } else if (wg == 2) {
@@ -323,18 +423,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int buf = j % kKvBufs;
       const uint32_t par = ((j / kKvBufs) & 1) ^ 1;
-      if (j >= kKvBufs && !mbar_wait(smem_u32(&bars->k_empty[buf]), par, err)) break;
+      if (j >= kKvBufs && !wait_bounded(smem_u32(&bars->k_empty[buf]), par, err)) break;
       store_row<D>(sbase + C::kKOff + buf * C::kTileBytes, tok_l, ck);
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&bars->k_full[buf]));
       const int slot = j % kScaleSlots;
       if (j >= kScaleSlots &&
-          !mbar_wait(smem_u32(&bars->sc_empty[slot]), ((j / kScaleSlots) & 1) ^ 1, err))
+          !wait_bounded(smem_u32(&bars->sc_empty[slot]), ((j / kScaleSlots) & 1) ^ 1, err))
         break;
       scales[slot * 2 * kBN + tok_l] = fk;
       scales[slot * 2 * kBN + kBN + tok_l] = fv;
       mbar_arrive(smem_u32(&bars->sc_full[slot]));
-      if (j >= kKvBufs && !mbar_wait(smem_u32(&bars->v_empty[buf]), par, err)) break;
+      if (j >= kKvBufs && !wait_bounded(smem_u32(&bars->v_empty[buf]), par, err)) break;
       store_row<D>(sbase + C::kVOff + buf * C::kTileBytes, tok_l, cv);
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&bars->v_full[buf]));
@@ -356,80 +456,51 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     for (int j = 0; j < n; ++j) {
       const int slot = j % kScaleSlots;
-      if (!(ok = mbar_wait(smem_u32(&bars->sc_full[slot]), (j / kScaleSlots) & 1, err))) break;
-      if (!(ok = mbar_wait(smem_u32(&bars->s_full[t]), j & 1, err))) break;
+      if (!(ok = wait_bounded(smem_u32(&bars->sc_full[slot]), (j / kScaleSlots) & 1, err))) break;
+      if (!(ok = wait_bounded(smem_u32(&bars->s_full[t]), j & 1, err))) break;
       tc_fence_after();
-      const float *kf = scales + slot * 2 * kBN;
-      const float *vf = kf + kBN;
+      const uint32_t kf = smem_u32(scales + slot * 2 * kBN), vf = kf + kBN * 4;
       const int key0 = j * kBN;
       const bool masked = key0 + kBN - 1 > warp_limit;
 
-      // maximum of S*kf over one 32-key chunk (masked keys excluded)
-      auto chunk_max = [&](const uint32_t(&s)[32], int c) {
-        float mx = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 f = *reinterpret_cast<const float4 *>(kf + c * 32 + i);
-          const float fs[4] = {f.x, f.y, f.z, f.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float x = __uint_as_float(s[i + e]) * fs[e];
-            mx = fmaxf(mx, (masked && key0 + c * 32 + i + e > limit) ? -INFINITY : x);
+      // The tile body is instantiated twice: with per-key masking (tiles
+      // that cross the causal diagonal or the end of the keys) and without.
+      float tsum = 0.f;
+      auto tile = [&](auto mask_tag) {
+        constexpr bool M = decltype(mask_tag)::value;
+        if (j == 0) {  // the first tile fixes the reference maximum
+          float mx = -INFINITY;
+#pragma unroll 1
+          for (int c = 0; c < kBN / 32; ++c) {
+            uint32_t s[32];
+            tmem_ld32(s_tm + c * 32, s);
+            mx = fmaxf(mx, chunk_max<M>(s, kf + c * 128, key0 + c * 32, limit));
           }
+          m = mx == -INFINITY ? 0.f : mx;
         }
-        return mx;
-      };
-      // p = 2^(S*kf - m) of one chunk; h = fp16 pairs of p*vf; returns the sum of p
-      auto chunk_exp = [&](const uint32_t(&s)[32], int c, uint32_t(&h)[16]) {
-        float sum0 = 0.f, sum1 = 0.f;
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 f = *reinterpret_cast<const float4 *>(kf + c * 32 + i);
-          const float4 g = *reinterpret_cast<const float4 *>(vf + c * 32 + i);
-          const float fs[4] = {f.x, f.y, f.z, f.w}, gs[4] = {g.x, g.y, g.z, g.w};
-          float p[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float x = fmaf(__uint_as_float(s[i + e]), fs[e], -m);
-            if (masked && key0 + c * 32 + i + e > limit) x = -INFINITY;
-            p[e] = ex2(x);
-          }
-          sum0 += p[0] + p[2], sum1 += p[1] + p[3];
-          h[i / 2] = pack_half2(p[0] * gs[0], p[1] * gs[1]);
-          h[i / 2 + 1] = pack_half2(p[2] * gs[2], p[3] * gs[3]);
-        }
-        return sum0 + sum1;
-      };
-
-      if (j == 0) {  // the first tile fixes the reference maximum
-        float mx = -INFINITY;
+        // P chunk c (16 columns) overwrites S columns already read.
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
-          uint32_t s[32];
-          tmem_ld32(s_tm + c * 32, s);
-          mx = fmaxf(mx, chunk_max(s, c));
+          uint32_t cur[32], h[16];
+          tmem_ld32(s_tm + c * 32, cur);
+          float cs = chunk_exp<M>(cur, kf + c * 128, vf + c * 128, m, key0 + c * 32, limit, h);
+          if (__any_sync(0xffffffffu, !(cs <= static_cast<float>(kRedoSum)))) {
+            // the reference maximum moves: rescale what was built on the old one
+            const float mn = fmaxf(m, chunk_max<M>(cur, kf + c * 128, key0 + c * 32, limit));
+            const float alpha = ex2(m - mn);
+            m = mn, l *= alpha, tsum *= alpha;
+            rescale_tmem<D>(s_tm, o_tm, c, j > 0, alpha);
+            tmem_ld32(s_tm + c * 32, cur);  // S chunk c is intact: P so far only covers chunks < c/2
+            cs = chunk_exp<M>(cur, kf + c * 128, vf + c * 128, m, key0 + c * 32, limit, h);
+          }
+          tsum += cs;
+          tmem_st16(s_tm + c * 16, h);
         }
-        m = mx == -INFINITY ? 0.f : mx;
-      }
-      // P chunk c (16 columns) overwrites S columns already read.
-      float tsum = 0.f;
-#pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t s[32], h[16];
-        tmem_ld32(s_tm + c * 32, s);
-        float cs = chunk_exp(s, c, h);
-        if (__any_sync(0xffffffffu, !(cs <= static_cast<float>(kRedoSum)))) {
-          // the reference maximum moves: rescale what was built on the old one
-          const float mn = fmaxf(m, chunk_max(s, c));
-          const float alpha = ex2(m - mn);
-          m = mn, l *= alpha, tsum *= alpha;
-          rescale_tmem<D>(s_tm, o_tm, c, j > 0, alpha);
-          tmem_ld32(s_tm + c * 32, s);  // S chunk c is intact: P so far only covers chunks < c/2
-          cs = chunk_exp(s, c, h);
-        }
-        tsum += cs;
-        tmem_st16(s_tm + c * 16, h);
-      }
+      };
+      if (masked)
+        tile(std::true_type{});
+      else
+        tile(std::false_type{});
       l += tsum;
       tmem_st_wait();
       tc_fence_before();
@@ -438,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // ------------------------------------------------------------ epilogue
-    const bool done = mbar_wait(smem_u32(&bars->o_full), 0, err, ok ? kWaitCycles : kDrainCycles);
+    const bool done = wait_bounded(smem_u32(&bars->o_full), 0, err, ok ? kWaitCycles : kDrainCycles);
     tc_fence_after();
     if (done && ok) {
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -451,10 +522,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 4; ++q) {
           const int chunk = c * 4 + q;
           const uint32_t sub = chunk / 8, col = chunk % 8;
-          const uint32_t h0 = pack_half2(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 1]) * inv);
-          const uint32_t h1 = pack_half2(__uint_as_float(o[8 * q + 2]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
-          const uint32_t h2 = pack_half2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 5]) * inv);
-          const uint32_t h3 = pack_half2(__uint_as_float(o[8 * q + 6]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+          // column 8q+p of O holds d = 8q + (0 4 1 5 2 6 3 7)[p]
+          const uint32_t h0 = pack_half2(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 2]) * inv);
+          const uint32_t h1 = pack_half2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 6]) * inv);
+          const uint32_t h2 = pack_half2(__uint_as_float(o[8 * q + 1]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
+          const uint32_t h3 = pack_half2(__uint_as_float(o[8 * q + 5]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
           const uint32_t dst = stage + sub * C::kSubBytes + row_l * 128 + ((col ^ (row_l & 7)) << 4);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(h0), "r"(h1), "r"(h2), "r"(h3)
                        : "memory");
