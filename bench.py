@@ -296,7 +296,7 @@ def workload_config(name, splits=None):
         out["l2"] = "inputs larger than L2: Q and O are 134 MB each per step"
     else:
         if splits is None:
-            splits = 128 if name == "long_decode" else 0
+            splits = 152 if name == "long_decode" else 0
         out["splits"] = "auto" if splits == 0 else splits
         out["l2"] = "rotating KV-cache copies totalling more than 4x L2"
         if cfg["kind"] == "paged":
@@ -317,7 +317,7 @@ def run_decode(name, args, device, gpu_index, rank):
     B, Hq, Hkv, D = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"]
     paged = cfg["kind"] == "paged"
     seed = cfg["seed"] + 1000 * rank
-    splits = args.splits if args.splits >= 0 else (128 if name == "long_decode" else 0)
+    splits = args.splits if args.splits >= 0 else (152 if name == "long_decode" else 0)
     scale = 1.0 / math.sqrt(D)
     torch.manual_seed(seed)
     if paged:

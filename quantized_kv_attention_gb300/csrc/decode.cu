@@ -92,6 +92,12 @@ __device__ __forceinline__ void decode_sub(uint32_t w, uint32_t (&out)[4]) {
   out[3] = lop3_and_xor(w8, 0x00F000F0u, 0x00800080u);
 }
 
+__device__ __forceinline__ __half lds_f16(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return __ushort_as_half(v);
+}
+
 // Range of the flattened stage list owned by CTA i of n: [i*T/n, (i+1)*T/n).
 __host__ __device__ __forceinline__ int64_t range_start(int64_t i, int64_t T, int64_t n) {
   return i * T / n;
@@ -408,8 +414,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (nvalid > 0) {
         const uint32_t kb = ring + cur * C::kStageBytes;
         const uint32_t vb = kb + C::kCodeBytes;
-        const __half *sks = reinterpret_cast<const __half *>(smem + cur * C::kStageBytes + 2 * C::kCodeBytes) + sofs;
-        const __half *svs = sks + kRowsPerStage;
+        // scales by explicit shared-memory loads (the aligned base is not
+        // known to the compiler as shared, generic loads would be slower)
+        const uint32_t sks = kb + 2 * C::kCodeBytes + 2 * sofs;
+        const uint32_t svs = sks + 2 * kRowsPerStage;
         // S^T of the warp's 32 tokens: two 16-token tiles, two accumulation
         // chains each (even / odd code words)
         uint32_t kw[2][2][C::kWords];
@@ -449,15 +457,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
           const int lt = tok_w + t * 16 + g;
-          const float f0 = __half2float(sks[lt]) * kf, f1 = __half2float(sks[lt + 8]) * kf;
+          const float f0 = __half2float(lds_f16(sks + 2 * lt)) * kf, f1 = __half2float(lds_f16(sks + 2 * lt + 16)) * kf;
           ts[t][0] = (sacc[t][0] + so[t][0] - bq0) * f0;
           ts[t][1] = (sacc[t][1] + so[t][1] - bq1) * f0;
           ts[t][2] = (sacc[t][2] + so[t][2] - bq0) * f1;
           ts[t][3] = (sacc[t][3] + so[t][3] - bq1) * f1;
           // the V scale carries an exact 2^-8: with a lazily raised max p can
           // reach 2^8, and p * s_V must stay inside the fp16 range
-          fv[t][0] = __half2float(svs[lt]) * 0.00390625f;
-          fv[t][1] = __half2float(svs[lt + 8]) * 0.00390625f;
+          fv[t][0] = __half2float(lds_f16(svs + 2 * lt)) * 0.00390625f;
+          fv[t][1] = __half2float(lds_f16(svs + 2 * lt + 16)) * 0.00390625f;
         }
         if (nvalid < 32) {  // tail: mask tokens past the sequence end (never touch their scales)
 #pragma unroll
@@ -600,13 +608,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 // balanced ranges cut: a segment spanning CTAs c0 < c1 has partials in slot
 // 2*c0 + 1 (its start, in c0's last segment) and slots 2*c for c0 < c <= c1
 // whose range is not empty.  Segments of empty sequences get O = 0 and
-// lse = -inf.  Grid (segments, rows of a segment); the 16 warps of a CTA split
+// lse = -inf.  Grid (segments, rows of a segment); the 8 warps of a CTA split
 // one row's partials, each folding its share with a running max so that the
 // lse and O of a partial are fetched together, then combine in shared memory.
-constexpr int kMergeWarps = 16;
+// Small on purpose (256 threads, <= 64 registers, 4 KB shared memory): one
+// merge CTA fits on an SM beside a decode CTA, so the programmatic launch
+// makes it resident while the decode still runs and it starts the moment the
+// decode grid completes.
+constexpr int kMergeWarps = 8;
 
 template <int D>
-__global__ void __launch_bounds__(kMergeWarps * 32)
+__global__ void __launch_bounds__(kMergeWarps * 32, 4)
     decode_merge_kernel(const int32_t *__restrict__ seq_lens, int batch, int hkv, int G, int ctas,
                         int64_t limit, int paged, const float *__restrict__ po,
                         const float *__restrict__ pl, uint16_t *__restrict__ out,

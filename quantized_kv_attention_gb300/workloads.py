@@ -12,7 +12,8 @@ which themselves need model weights and datasets not available here):
   gqa_decode          B=8, Hq=32, Hkv=8, D=128, Nk=4096, one query each; K
                       has 4 outlier channels per kv-head scaled x10; seed 1
   long_decode         B=1, Hq=64, Hkv=8, D=128, Nk=131072, split-KV into
-                      64/128/256 chunks; seed 2
+                      64-256 chunks (the bench takes 152: one per GB300 SM);
+                      seed 2
   causal_prefill      B=2, Hq=32, Hkv=8, D=128, Nq=Nk=8192, causal; seed 3
   paged_decode        64 sequences, lengths uniform in [512, 32768], pages of
                       64 tokens in a randomly permuted pool, Hq=32, Hkv=8,
@@ -32,7 +33,7 @@ WORKLOADS = {
     "gqa_decode": dict(kind="decode", B=8, Hq=32, Hkv=8, D=128, Nk=4096, seed=1,
                        outliers=4, outlier_scale=10.0),
     "long_decode": dict(kind="decode", B=1, Hq=64, Hkv=8, D=128, Nk=131072, seed=2,
-                        splits=(64, 128, 256)),
+                        splits=(64, 128, 152, 256)),
     "causal_prefill": dict(kind="prefill", B=2, Hq=32, Hkv=8, D=128, Nq=8192, Nk=8192, seed=3),
     "paged_decode": dict(kind="paged", B=64, Hq=32, Hkv=8, D=128, len_lo=512, len_hi=32768,
                          page=64, seed=4, scales=(1.0 / math.sqrt(128), 1.0)),
