@@ -181,10 +181,14 @@ qattn_status qattn_decode(const uint16_t *q, const qattn_kv_cache *cache, const 
  * qattn_prefill -- Nq query rows per sequence against Nk cached keys
  * ([TA] §2.1 prefill, §2.2 FlashAttention tiling; dense contractions on
  * the tensor cores with the dequantization fused ahead of the operand
- * stage, [FAQ3] §3.1).  Contiguous cache only.
+ * stage, [FAQ3] §3.1).  Contiguous or paged cache (chunked prefill of a
+ * paged cache: the new rows' Q against every cached key).
  *
  *   q        [batch, Hq, Nq, D] fp16
  *   nq, nk   query rows and keys per sequence, 1 <= nq <= nk <= capacity
+ *            (paged: nk <= max_pages_per_seq * 64; a key in a missing page
+ *            raises QATTN_FLAG_BAD_PAGE and leaves that sequence's rows
+ *            undefined)
  *   causal   0 or 1 (bottom-right aligned)
  *   out      [batch, Hq, Nq, D] fp16
  *   lse      [batch, Hq, Nq] fp32, or NULL
@@ -213,6 +217,18 @@ qattn_status qattn_combine(const float *partial_o, const float *partial_lse, int
  * last clear, and clear them if `clear` is non-zero.
  */
 qattn_status qattn_read_device_flags(uint32_t *flags, int32_t clear);
+
+/*
+ * qattn_check_wait_timeout -- exercises the bounded waits every kernel of
+ * the library uses, without faulting or hanging the GPU.  One small kernel
+ * waits on an mbarrier that no thread ever arrives at, gives up after
+ * `limit_cycles` SM clock cycles (1 ... 2^31), and writes the QATTN_FLAG_*
+ * bits it raised to *flags (device, uint32): QATTN_FLAG_WAIT_TIMEOUT when
+ * the wait gave up as it must.  The device status word of
+ * qattn_read_device_flags is not touched and the context stays usable.  The
+ * pages have no counterpart: this is the library's own failure check.
+ */
+qattn_status qattn_check_wait_timeout(uint32_t *flags, int64_t limit_cycles, qattn_stream_t stream);
 
 /* Bytes of the library-owned scratch behind qattn_decode_noalloc (8 MiB per device). */
 #define QATTN_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)

@@ -36,7 +36,7 @@ FLAG_WAIT_TIMEOUT, FLAG_BAD_PAGE, FLAG_TMEM = 1, 2, 4
 EXPORTS = (
     "qattn_quantize_kv", "qattn_decode_workspace_size", "qattn_decode", "qattn_prefill",
     "qattn_combine", "qattn_read_device_flags", "qattn_status_string", "qattn_last_error",
-    "qattn_version", "qattn_decode_noalloc",
+    "qattn_version", "qattn_decode_noalloc", "qattn_check_wait_timeout",
 )
 
 
@@ -89,6 +89,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qattn_last_error": (ctypes.c_char_p, []),
         "qattn_version": (i32, []),
         "qattn_decode_noalloc": (i32, [vp, cache_p, vp, i32, i32, i32, f32, i32, vp, vp, vp]),
+        "qattn_check_wait_timeout": (i32, [vp, i64, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -237,6 +238,15 @@ def combine(partial_o: torch.Tensor, partial_lse: torch.Tensor, out: Optional[to
     _check(load_library().qattn_combine(_ptr(partial_o), _ptr(partial_lse), S, R, D, _ptr(out), _ptr(lse),
                                         _stream(partial_o.device)), "qattn_combine")
     return (out, lse) if return_lse else out
+
+
+def check_wait_timeout(limit_cycles: int = 2_000_000, device="cuda") -> int:
+    """Run the library's bounded-wait check on `device`; returns the QATTN_FLAG_*
+    bits the check raised (FLAG_WAIT_TIMEOUT when the wait gave up as it must)."""
+    flags = torch.full((1,), -1, dtype=torch.int32, device=device)
+    _check(load_library().qattn_check_wait_timeout(_ptr(flags), int(limit_cycles), _stream(flags.device)),
+           "qattn_check_wait_timeout")
+    return int(flags.cpu().item()) & 0xFFFFFFFF
 
 
 def read_device_flags(clear: bool = True) -> int:

@@ -317,10 +317,12 @@ qattn_status qattn_prefill(const uint16_t *q, const qattn_kv_cache *cache, int32
   uint64_t code_bytes = 0;
   qattn_status st = check_cache(cache, batch, &view, &code_bytes);
   if (st != QATTN_OK) return st;
-  if (view.page_table) return fail(QATTN_ERR_UNSUPPORTED, "prefill reads a contiguous cache only");
+
   if (num_q_heads % view.hkv) return fail(QATTN_ERR_INVALID_ARG, "Hq %d is not a multiple of Hkv %d", num_q_heads, view.hkv);
   if (nq > nk) return fail(QATTN_ERR_INVALID_ARG, "nq %d > nk %d", nq, nk);
-  if (nk > view.capacity) return fail(QATTN_ERR_INVALID_ARG, "nk %d > capacity %lld", nk, (long long)view.capacity);
+  const int64_t limit = view.page_table ? static_cast<int64_t>(view.max_pages) * kPage : view.capacity;
+  if (nk > limit)
+    return fail(QATTN_ERR_INVALID_ARG, "nk %d > the cache's %lld tokens per sequence", nk, (long long)limit);
   if (batch == 0 || nq == 0) return QATTN_OK;
   if (!q || !out) return fail(QATTN_ERR_INVALID_ARG, "q or out is NULL");
   if (!aligned16(q) || !aligned16(out)) return fail(QATTN_ERR_INVALID_ARG, "q and out must be 16-byte aligned");

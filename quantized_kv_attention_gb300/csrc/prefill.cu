@@ -398,25 +398,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsDequant));
     // ---------------------------------------------------- dequantization
     const int tok_l = threadIdx.x - kSoftmaxThreads;  // token within the tile
+    // Cache row of token `tok` of this (sequence, kv-head): contiguous
+    // [B, Hkv, capacity] or, through the page table, [pages, Hkv, 64];
+    // -1 for a token in a missing page (flagged; its codes read as zero).
+    const bool paged = cache.page_table != nullptr;
     const int64_t row0 = (static_cast<int64_t>(w.b) * cache.hkv + w.kvh) * cache.capacity;
-    const uint4 *kc = reinterpret_cast<const uint4 *>(cache.k_codes + row0 * (D / 2));
-    const uint4 *vc = reinterpret_cast<const uint4 *>(cache.v_codes + row0 * (D / 2));
-    const __half *ks = reinterpret_cast<const __half *>(cache.k_scales) + row0;
-    const __half *vs = reinterpret_cast<const __half *>(cache.v_scales) + row0;
+    auto cache_row = [&](int tok) -> int64_t {
+      if (!paged) return row0 + tok;
+      const int page = __ldg(cache.page_table + static_cast<int64_t>(w.b) * cache.max_pages + tok / kPage);
+      if (page < 0 || page >= cache.num_pages) return -1;
+      return (static_cast<int64_t>(page) * cache.hkv + w.kvh) * kPage + tok % kPage;
+    };
+    const uint4 *kc = reinterpret_cast<const uint4 *>(cache.k_codes);
+    const uint4 *vc = reinterpret_cast<const uint4 *>(cache.v_codes);
+    const __half *ks = reinterpret_cast<const __half *>(cache.k_scales);
+    const __half *vs = reinterpret_cast<const __half *>(cache.v_scales);
     // No prefetch across tiles: the two operand buffers let this warpgroup
     // run up to two tiles ahead of the tensor core, which hides the load.
     for (int j = 0; j < n; ++j) {
       const int tok = j * kBN + tok_l;
       uint4 ck[D / 32], cv[D / 32];
       float fk = 0.f, fv = 0.f;
-      if (tok < a.nk) {
+      const int64_t row = tok < a.nk ? cache_row(tok) : -1;
+      if (tok < a.nk && row < 0) atomicOr(err, kFlagBadPage);
+      if (row >= 0) {
 #pragma unroll
         for (int i = 0; i < D / 32; ++i) {
-          ck[i] = __ldg(kc + static_cast<int64_t>(tok) * (D / 32) + i);
-          cv[i] = __ldg(vc + static_cast<int64_t>(tok) * (D / 32) + i);
+          ck[i] = __ldg(kc + row * (D / 32) + i);
+          cv[i] = __ldg(vc + row * (D / 32) + i);
         }
-        fk = __half2float(ks[tok]) * a.scale_log2;
-        fv = __half2float(vs[tok]);
+        fk = __half2float(ks[row]) * a.scale_log2;
+        fv = __half2float(vs[row]);
       } else {
 #pragma unroll
         for (int i = 0; i < D / 32; ++i) ck[i] = cv[i] = make_uint4(0, 0, 0, 0);

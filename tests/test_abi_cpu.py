@@ -79,7 +79,9 @@ def test_prefill_rejects_bad_arguments():
     assert pf(nk=300) == qa.QATTN_ERR_INVALID_ARG                        # nk > capacity
     assert pf(causal=2) == qa.QATTN_ERR_INVALID_ARG
     assert pf(q=FAKE + 2) == qa.QATTN_ERR_INVALID_ARG                    # misaligned
-    assert pf(cache=_cache(page_table=FAKE, page_size=64, num_pages=4, max_pages_per_seq=2)) == qa.QATTN_ERR_UNSUPPORTED
+    paged = _cache(page_table=FAKE, page_size=64, num_pages=4, max_pages_per_seq=2)  # 128 tokens per sequence
+    assert pf(cache=paged, nk=129, nq=10) == qa.QATTN_ERR_INVALID_ARG   # nk beyond the page-table row
+    assert pf(cache=_cache(page_table=FAKE, page_size=32, num_pages=4, max_pages_per_seq=2)) == qa.QATTN_ERR_UNSUPPORTED
 
 
 def test_quantize_and_combine_reject_bad_arguments():
@@ -115,3 +117,9 @@ def test_workspace_size_host_arithmetic():
     assert qa.decode_workspace_size(0, 8, 2, 128, 60, 4) == 0             # invalid sizes
     assert qa.decode_workspace_size(2, 8, 2, 96, 600, 4) == 0
     assert qa.decode_workspace_size(4096, 8, 2, 128, 600, 4) == 0         # batch above the limit
+
+
+def test_wait_check_rejects_bad_arguments():
+    assert lib.qattn_check_wait_timeout(None, 1000, None) == qa.QATTN_ERR_INVALID_ARG
+    assert lib.qattn_check_wait_timeout(FAKE, 0, None) == qa.QATTN_ERR_INVALID_ARG
+    assert lib.qattn_check_wait_timeout(FAKE, (1 << 31) + 1, None) == qa.QATTN_ERR_INVALID_ARG

@@ -63,3 +63,31 @@ def test_prefill_row_equals_decode():
     for i in (0, 63, 64, 130, 199):
         od = qa.decode(q[:, :, i].contiguous(), cache, torch.tensor([i + 1], dtype=torch.int32).cuda(), N, 0.1, 1)
         assert (od.float() - out[:, :, i].float()).abs().max().item() <= 2e-3
+
+
+@pytest.mark.parametrize("nq,causal", [(100, True), (300, True), (77, False)])
+def test_prefill_paged(nq, causal):
+    """Chunked prefill of a paged cache: pages of each sequence scattered over
+    a randomly permuted pool, the last page row of the table unused (-1)."""
+    qa = require_gpu()
+    B, Hq, Hkv, D, nk, page = 2, 8, 2, 128, 300, 64
+    npg = -(-nk // page)
+    perm = torch.randperm(B * npg, generator=torch.Generator().manual_seed(5)).to(torch.int32)
+    table = torch.full((B, npg + 1), -1, dtype=torch.int32)
+    table[:, :npg] = perm.view(B, npg)
+    cache = qa.KvCache.paged(B * npg, Hkv, D, table)
+    k = wl.kv_block(43, "k", B, Hkv, nk, D)
+    v = wl.kv_block(43, "v", B, Hkv, nk, D)
+    for b in range(B):
+        sub = qa.KvCache(cache.k_codes, cache.k_scales, cache.v_codes, cache.v_scales, D, Hkv,
+                         page_table=cache.page_table[b:b + 1], num_pages=B * npg)
+        qa.quantize_kv(k[b:b + 1].cuda(), v[b:b + 1].cuda(), sub)
+    q = wl.queries(43, B, Hq, nq, D)
+    scale = 1 / math.sqrt(D)
+    out, lse = qa.prefill(q.cuda(), cache, nk, scale, causal, return_lse=True)
+    pk, sk = codec.quantize_pack(k.numpy())
+    pv, sv = codec.quantize_pack(v.numpy())
+    O, L = att.attention_quantized(q.numpy(), pk, sk, pv, sv, scale, causal)
+    assert_close_attention(out, O)
+    assert_close_lse(lse, L)
+    assert qa.read_device_flags() == 0
