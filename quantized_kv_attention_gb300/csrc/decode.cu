@@ -573,28 +573,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     consumer_sync();
     const bool complete = l.s == 0 && cnt == l.n;
     const int64_t pslot = l.s > 0 ? 2 * static_cast<int64_t>(blockIdx.x) : 2 * static_cast<int64_t>(blockIdx.x) + 1;
-    for (int idx = threadIdx.x; idx < geo.hb * G * D; idx += kConsumerWarps * 32) {
-      const int hh = idx / (G * D), rem = idx - hh * G * D;  // kv-head in stage, q-head, d
-      const int h = rem / D, d = rem - h * D;
+    // One thread per (row, 4 consecutive d): the row's warp weights
+    // 2^(m_w - M) are computed once per thread, then 4 columns are folded
+    // with float4 reads of the merge area.
+    for (int idx = threadIdx.x; idx < geo.hb * G * (D / 4); idx += kConsumerWarps * 32) {
+      const int r = idx / (D / 4), d = (idx - r * (D / 4)) * 4;  // row = kv-head in stage * G + q-head
+      const int hh = r / G, h = r - hh * G;
       const int w0 = hh * geo.wph;
       float M = smm[w0 * 8 + h];
       for (int w = 1; w < geo.wph; ++w) M = fmaxf(M, smm[(w0 + w) * 8 + h]);
-      float L = 0.f, acc = 0.f;
+      float L = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int w = 0; w < geo.wph; ++w) {
         const float sc = ex2(smm[(w0 + w) * 8 + h] - M);
         L += sc * sml[(w0 + w) * 8 + h];
-        acc += sc * mo[((w0 + w) * 8 + h) * C::kMergePitch + d];
+        const float4 x = *reinterpret_cast<const float4 *>(mo + ((w0 + w) * 8 + h) * C::kMergePitch + d);
+        acc.x += sc * x.x, acc.y += sc * x.y, acc.z += sc * x.z, acc.w += sc * x.w;
       }
       const bool live = L > 0.f;
-      const float ov = live ? acc / L : 0.f;
+      const float inv = live ? 1.f / L : 0.f;
       const float lse_v = live ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
       if (complete) {
         const int64_t row = static_cast<int64_t>(l.b) * a.hq + (l.hg * geo.hb + hh) * G + h;
-        a.out[row * D + d] = __half_as_ushort(__float2half_rn(ov));
+        const uint32_t h01 = pack_half2(acc.x * inv, acc.y * inv), h23 = pack_half2(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2 *>(a.out + row * D + d) = make_uint2(h01, h23);
         if (d == 0 && a.lse) a.lse[row] = lse_v;
       } else {
-        const int64_t prow = pslot * geo.hb * G + hh * G + h;
-        a.partial_o[prow * D + d] = ov;
+        const int64_t prow = pslot * geo.hb * G + r;
+        *reinterpret_cast<float4 *>(a.partial_o + prow * D + d) =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
         if (d == 0) a.partial_lse[prow] = lse_v;
       }
     }
