@@ -677,29 +677,38 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4)
   float m = -INFINITY, z = 0.f, acc[VPL];
 #pragma unroll
   for (int j = 0; j < VPL; ++j) acc[j] = 0.f;
-#pragma unroll 4
-  for (int k = warp; k < np; k += kMergeWarps) {
-    const int64_t c = c0 + k;
-    // CTAs between c0 and c1 whose range is empty (more CTAs than stages) wrote nothing
-    if (k > 0 && range_start(c, T, ctas) == range_start(c + 1, T, ctas)) continue;
-    const int64_t slot = k == 0 ? 2 * c0 + 1 : 2 * c;
-    const float lv = pl[slot * rows + r];
-    const float *src = po + (slot * rows + r) * D + lane * VPL;
-    float x[VPL];
-    if constexpr (VPL == 4) {
-      const float4 v = __ldg(reinterpret_cast<const float4 *>(src));
-      x[0] = v.x, x[1] = v.y, x[2] = v.z, x[3] = v.w;
-    } else {
-      const float2 v = __ldg(reinterpret_cast<const float2 *>(src));
-      x[0] = v.x, x[1] = v.y;
-    }
-    if (lv == -INFINITY) continue;  // that split saw no key (its O is never used)
-    const float mn = fmaxf(m, lv);
-    const float sc = expf(m - mn), e = expf(lv - mn);
-    z = z * sc + e;
+  // A warp folds partials k = warp, warp + 8, ... in batches of 4 whose loads
+  // are all issued before any is used.  Empty ranges (two 64-bit divisions
+  // to detect) exist only when there are fewer stages than CTAs.
+  const bool may_be_empty = T < ctas;
+  for (int k0 = warp; k0 < np; k0 += 4 * kMergeWarps) {
+    float lv[4], x[4][VPL];
 #pragma unroll
-    for (int j = 0; j < VPL; ++j) acc[j] = acc[j] * sc + e * x[j];
-    m = mn;
+    for (int i = 0; i < 4; ++i) {
+      const int k = k0 + i * kMergeWarps;
+      const int64_t c = c0 + k;
+      const bool ok = k < np && (k == 0 || !may_be_empty || range_start(c, T, ctas) != range_start(c + 1, T, ctas));
+      const int64_t slot = k == 0 ? 2 * c0 + 1 : 2 * c;
+      lv[i] = ok ? pl[slot * rows + r] : -INFINITY;
+      const float *src = po + (slot * rows + r) * D + lane * VPL;
+      if constexpr (VPL == 4) {
+        const float4 v = ok ? __ldg(reinterpret_cast<const float4 *>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        x[i][0] = v.x, x[i][1] = v.y, x[i][2] = v.z, x[i][3] = v.w;
+      } else {
+        const float2 v = ok ? __ldg(reinterpret_cast<const float2 *>(src)) : make_float2(0.f, 0.f);
+        x[i][0] = v.x, x[i][1] = v.y;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (lv[i] == -INFINITY) continue;  // absent, or that split saw no key (its O is never used)
+      const float mn = fmaxf(m, lv[i]);
+      const float sc = expf(m - mn), e = expf(lv[i] - mn);
+      z = z * sc + e;
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) acc[j] = acc[j] * sc + e * x[i][j];
+      m = mn;
+    }
   }
 #pragma unroll
   for (int j = 0; j < VPL; ++j) accs[warp][lane * VPL + j] = acc[j];
