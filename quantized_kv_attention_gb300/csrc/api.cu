@@ -107,11 +107,11 @@ qattn_status prefill_maps(CUtensorMap *qmap, CUtensorMap *omap, const void *q, c
 
 // Decode maps: codes as 3-D [heads][rows_per_head][128 B] (128B swizzle),
 // scales as 2-D [heads][tokens_per_head] fp16; boxes from decode_geometry().
-qattn_status decode_maps(DecodeMaps *m, const KvView &v, int batch) {
+qattn_status decode_maps(DecodeMaps *m, const KvView &v, int batch, int warps) {
   EncodeFn enc = encode_fn();
   if (!enc) return fail(QATTN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
   const bool paged = v.page_table != nullptr;
-  const DecodeGeometry geo = decode_geometry(v.head_dim, v.hkv, paged);
+  const DecodeGeometry geo = decode_geometry(v.head_dim, v.hkv, paged, warps);
   const uint64_t heads = paged ? static_cast<uint64_t>(v.num_pages) * v.hkv : static_cast<uint64_t>(batch) * v.hkv;
   const uint64_t tokens = paged ? kPage : static_cast<uint64_t>(v.capacity);
   const uint64_t rows = tokens * v.head_dim / 256;
@@ -179,8 +179,8 @@ qattn_status check_cache(const qattn_kv_cache *c, int batch, KvView *v, uint64_t
 
 // Number of balanced key ranges (one persistent CTA each) for a decode call:
 // one per SM by default, never more than there can be stages.
-int plan_ctas(int batch, int hkv, int head_dim, int max_len, int requested, int sms, bool paged) {
-  const DecodeGeometry geo = decode_geometry(head_dim, hkv, paged);
+int plan_ctas(int batch, int hkv, int head_dim, int max_len, int requested, int sms, bool paged, int warps) {
+  const DecodeGeometry geo = decode_geometry(head_dim, hkv, paged, warps);
   const int64_t stages = static_cast<int64_t>(batch) * geo.groups *
                          ((static_cast<int64_t>(max_len) + geo.tokens_per_stage - 1) / geo.tokens_per_stage);
   int64_t n = requested > 0 ? requested : sms;
@@ -249,12 +249,16 @@ size_t qattn_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t n
   cudaGetLastError();
   // the larger of the two cache layouts' needs (the call does not say which one)
   size_t need = 0;
+  // (and of both CTA layouts, so that the answer never depends on the choice)
   for (int paged = 0; paged < 2; ++paged) {
     if (paged && !hkv_supported(num_kv_heads, true)) continue;
-    const int ctas = plan_ctas(batch, num_kv_heads, head_dim, max_seq_len, num_splits, sms, paged != 0);
-    const DecodeGeometry geo = decode_geometry(head_dim, num_kv_heads, paged != 0);
-    const size_t n = workspace_bytes(ctas, geo.heads_per_stage * (num_q_heads / num_kv_heads), head_dim);
-    if (n > need) need = n;
+    for (int warps = 8; warps <= 12; warps += 4) {
+      if (paged && warps != 8) continue;
+      const int ctas = plan_ctas(batch, num_kv_heads, head_dim, max_seq_len, num_splits, sms, paged != 0, warps);
+      const DecodeGeometry geo = decode_geometry(head_dim, num_kv_heads, paged != 0, warps);
+      const size_t n = workspace_bytes(ctas, geo.heads_per_stage * (num_q_heads / num_kv_heads), head_dim);
+      if (n > need) need = n;
+    }
   }
   return need;
 }
@@ -287,22 +291,23 @@ qattn_status qattn_decode(const uint16_t *q, const qattn_kv_cache *cache, const 
   if (static_cast<int64_t>(batch) * view.hkv * stage_limit >= (int64_t(1) << 31))
     return fail(QATTN_ERR_UNSUPPORTED, "batch * Hkv * cached stages exceeds 2^31");
   const bool paged = view.page_table != nullptr;
-  const int ctas = plan_ctas(batch, view.hkv, view.head_dim, max_seq_len, num_splits, ds->sms, paged);
-  const DecodeGeometry geo = decode_geometry(view.head_dim, view.hkv, paged);
+  const int warps = decode_layout(batch, view.hkv, max_seq_len, paged, num_splits > 0 ? num_splits : ds->sms);
+  const int ctas = plan_ctas(batch, view.hkv, view.head_dim, max_seq_len, num_splits, ds->sms, paged, warps);
+  const DecodeGeometry geo = decode_geometry(view.head_dim, view.hkv, paged, warps);
   const int slot_rows = geo.heads_per_stage * G;
   const size_t need = workspace_bytes(ctas, slot_rows, view.head_dim);
   if (!workspace || workspace_size < need || !aligned16(workspace))
     return fail(QATTN_ERR_WORKSPACE, "workspace of %zu bytes (16-byte aligned) needed, %zu given", need,
                 workspace ? workspace_size : (size_t)0);
   DecodeMaps maps;
-  if ((st = decode_maps(&maps, view, batch)) != QATTN_OK) return st;
+  if ((st = decode_maps(&maps, view, batch, warps)) != QATTN_OK) return st;
 
   DecodeArgs a;
   a.q = q, a.seq_lens = seq_lens, a.out = out, a.lse = lse;
   a.partial_o = static_cast<float *>(workspace);
   const size_t o_bytes = static_cast<size_t>(2) * ctas * slot_rows * view.head_dim * sizeof(float);
   a.partial_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + (o_bytes + 255) / 256 * 256);
-  a.batch = batch, a.hq = num_q_heads, a.ctas = ctas;
+  a.batch = batch, a.hq = num_q_heads, a.ctas = ctas, a.warps = warps;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   cudaError_t e = launch_decode(a, view, maps, ds->status, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "decode launch");

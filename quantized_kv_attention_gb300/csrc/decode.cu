@@ -45,24 +45,38 @@
 namespace qattn {
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kRowsPerStage = 256;  // (token, kv-head) rows per stage
 constexpr float kTwo24 = 16777216.0f;
 
-template <int D>
+// Two CTA layouts, by the number W of consumer warps (32 tokens each per
+// stage):
+//   W = 8   stages of 256 rows, one producer warp, 9 warps (paged pools: a
+//           stage is one 64-token page of 4 kv-heads)
+//   W = 12  stages of 384 tokens of one kv-head (contiguous caches), three
+//           consumer warps per SM sub-partition; a producer warpgroup whose
+//           registers go to the consumers (setmaxnreg: 3 x 160 + 32 = 4 x 128)
+template <int W>
+struct Layout {
+  static constexpr int kConsumerWarps = W;
+  static constexpr int kRows = 32 * W;  // (token, kv-head) rows per stage
+  static constexpr bool kSplitRegs = W > 8;
+  static constexpr int kThreads = kSplitRegs ? (W + 4) * 32 : (W + 1) * 32;
+  static constexpr int kRegsConsumer = 160, kRegsProducer = 32;
+};
+
+template <int D, int W>
 struct Cfg {
-  static constexpr int kCodeBytes = kRowsPerStage * D / 2;  // per tensor per stage
-  static constexpr int kScaleBytes = kRowsPerStage * 2;
+  static constexpr int kRows = Layout<W>::kRows;
+  static constexpr int kCodeBytes = kRows * D / 2;  // per tensor per stage
+  static constexpr int kScaleBytes = kRows * 2;
   static constexpr int kStageBytes = (2 * kCodeBytes + 2 * kScaleBytes + 1023) / 1024 * 1024;
-  static constexpr int kStages = D == 128 ? 6 : 12;
+  static constexpr int kStages = D == 128 ? (W == 8 ? 6 : 4) : (W == 8 ? 12 : 8);
   static constexpr int kQSlot = 4 * QATTN_MAX_GROUP * D * 2;  // Q rows of one segment (<= 4 kv-heads)
   // fp32 row pitch of the cross-warp merge area laid over the last stage's
-  // buffer ([8 warps][8 q-heads][pitch]); with 4 words of padding the eight
+  // buffer ([W warps][8 q-heads][pitch]); with 4 words of padding the eight
   // float4 stores of one quarter-warp (rows 2c, d = 4g) start 8c + 4g words
   // apart modulo 32 banks, so they never share a bank
   static constexpr int kMergePitch = D + 4;
-  static_assert(kConsumerWarps * 8 * kMergePitch * 4 <= kStageBytes, "merge area fits a stage");
+  static_assert(W * 8 * kMergePitch * 4 <= kStageBytes, "merge area fits a stage");
   static constexpr int kRing = kStages * kStageBytes;
   static constexpr int kKBytes = D / 8;  // K code bytes per lane per token
   static constexpr int kWords = kKBytes / 4;
@@ -71,14 +85,15 @@ struct Cfg {
 
 // Dynamic shared memory: ring | Q slot | m, l per (warp, q-head) | prefix |
 // lengths | barriers, flags.  The cross-warp merge reuses a ring slot.
-template <int D>
+template <int D, int W>
 __host__ __device__ constexpr int smem_bytes(int batch) {
-  return Cfg<D>::kRing + Cfg<D>::kQSlot + 2 * kConsumerWarps * 8 * 4 + (2 * batch + 1) * 4 +
-         (2 * Cfg<D>::kStages + 2) * 8 + Cfg<D>::kStages * 4 + 16 + 1024;
+  return Cfg<D, W>::kRing + Cfg<D, W>::kQSlot + 2 * W * 8 * 4 + (2 * batch + 1) * 4 +
+         (2 * Cfg<D, W>::kStages + 2) * 8 + Cfg<D, W>::kStages * 4 + 16 + 1024;
 }
 
+template <int W>
 __device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(W * 32) : "memory");
 }
 
 // Nibbles -> fp16 subnormals: out[k] = (u_lo, u_hi) * 2^-24 for nibble k of
@@ -129,23 +144,26 @@ __device__ __forceinline__ Loc locate(int64_t gs, const int *prefix, int batch, 
 
 // Geometry of one stage.  A TMA box streams at full speed only when its
 // bytes are contiguous: in a contiguous cache a kv-head's tokens are, so a
-// stage is 256 tokens of one kv-head; in a paged pool the kv-heads of a page
-// are adjacent, so a stage is one page (64 tokens) of 4 kv-heads (256/Hkv
-// tokens of every head, page by page, when Hkv < 4).
+// stage is 256 (W = 8) or 384 (W = 12) tokens of one kv-head; in a paged
+// pool the kv-heads of a page are adjacent, so a stage is one page (64
+// tokens) of 4 kv-heads (256/Hkv tokens of every head, page by page, when
+// Hkv < 4; W = 8).
 struct StageGeo {
   int hb;      // kv-heads per stage
-  int tokens;  // tokens per head per stage = 256 / hb
+  int tokens;  // tokens per head per stage = rows / hb
   int groups;  // head groups = Hkv / hb
-  int wph;     // consumer warps per head = 8 / hb
+  int wph;     // consumer warps per head = W / hb
 };
+template <int W>
 __host__ __device__ __forceinline__ StageGeo stage_geo(int hkv, bool paged) {
   StageGeo g;
   g.hb = paged ? (hkv >= 4 ? 4 : hkv) : 1;
-  g.tokens = kRowsPerStage / g.hb;
+  g.tokens = Layout<W>::kRows / g.hb;
   g.groups = hkv / g.hb;
-  g.wph = kConsumerWarps / g.hb;
+  g.wph = W / g.hb;
   return g;
 }
+
 
 // Tensor maps of one cache (built on the host, passed by value):
 //   codes  3-D [heads_total][rows_per_head][128 B]; box [box_heads][box_rows][128 B], 128B swizzle
@@ -156,13 +174,16 @@ struct Maps {
   CUtensorMap k, v, ks, vs;
 };
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int D, int W>
+__global__ void __launch_bounds__(Layout<W>::kThreads, 1)
     decode_kernel(DecodeArgs a, KvView cache, const __grid_constant__ Maps maps, uint32_t *err) {
-  using C = Cfg<D>;
+  using C = Cfg<D, W>;
+  constexpr int kConsumerWarps = W;
+  constexpr int kThreads = Layout<W>::kThreads;
+  constexpr int kRowsPerStage = Layout<W>::kRows;
   const int G = a.hq / cache.hkv;
   const int B = a.batch, hkv = cache.hkv;
-  const StageGeo geo = stage_geo(hkv, cache.page_table != nullptr);
+  const StageGeo geo = stage_geo<W>(hkv, cache.page_table != nullptr);
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -235,9 +256,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t gs1 = range_start(blockIdx.x + 1, T, gridDim.x);
   if (gs1 <= gs0) return;
 
-  if (warp == kConsumerWarps) {
+  if (warp >= kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // (layout W = 12: a warpgroup whose registers go to the consumers; one
+    // thread of its first warp issues the loads)
+    if constexpr (Layout<W>::kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Layout<W>::kRegsProducer));
+    if (warp == kConsumerWarps && lane == 0) {
       const int rows_per_tok = D / 2;  // code bytes per token
       const uint32_t qbytes = geo.hb * G * D * 2;
       int it = 0, seg = 0;
@@ -277,8 +301,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(full_s, 2 * C::kCodeBytes + 2 * C::kScaleBytes);
             tma_load_3d(st, &maps.k, 0, row0, head0, full_s);
             tma_load_3d(stv, &maps.v, 0, row0, head0, full_s);
-            tma_load_2d(sks, &maps.ks, tok0, head0, full_s);
-            tma_load_2d(svs, &maps.vs, tok0, head0, full_s);
+            // scale boxes are at most 256 tokens: a 384-token stage takes two
+            constexpr int kSBox = kRowsPerStage > 256 ? kRowsPerStage / 2 : kRowsPerStage;
+#pragma unroll
+            for (int o = 0; o < kRowsPerStage; o += kSBox) {
+              tma_load_2d(sks + 2 * o, &maps.ks, tok0 + o, head0, full_s);
+              tma_load_2d(svs + 2 * o, &maps.vs, tok0 + o, head0, full_s);
+            }
           } else {
             // pages of this stage that hold tokens below the sequence length
             // (a stage may run past the end of the sequence and of its table row)
@@ -328,9 +357,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     return;
-  }
+  } else {  // each role sets its register budget inside its own branch
 
   // -------------------------------------------------------------- consumers
+  if constexpr (Layout<W>::kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Layout<W>::kRegsConsumer));
   const int g = lane >> 2, c = lane & 3;
   const int hbw = warp / geo.wph;              // this warp's kv-head within the stage
   const int tok_w = (warp % geo.wph) * 32;     // its 32 tokens within that head's stage tokens
@@ -546,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ps0 += __shfl_xor_sync(0xffffffffu, ps0, off);
       ps1 += __shfl_xor_sync(0xffffffffu, ps1, off);
     }
-    consumer_sync();  // every warp has read its last stage
+    consumer_sync<W>();  // every warp has read its last stage
     float *mo = reinterpret_cast<float *>(smem + last * C::kStageBytes);
     // O^T m-tile jp*4+k holds d = 64 jp + 4 g + k (rows g) and +32 (rows g+8);
     // nibble positions 1 and 3 (odd k) came out 16x larger; P' carried 2^-8.
@@ -570,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       smm[warp * 8 + 2 * c] = m0, smm[warp * 8 + 2 * c + 1] = m1;
       sml[warp * 8 + 2 * c] = l0, sml[warp * 8 + 2 * c + 1] = l1;
     }
-    consumer_sync();
+    consumer_sync<W>();
     const bool complete = l.s == 0 && cnt == l.n;
     const int64_t pslot = l.s > 0 ? 2 * static_cast<int64_t>(blockIdx.x) : 2 * static_cast<int64_t>(blockIdx.x) + 1;
     // One thread per (row, 4 consecutive d): the row's warp weights
@@ -605,9 +635,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (d == 0) a.partial_lse[prow] = lse_v;
       }
     }
-    consumer_sync();  // the merge area is read; the stage can be refilled
+    consumer_sync<W>();  // the merge area is read; the stage can be refilled
     if (lane == 0) mbar_arrive(smem_u32(empty + last));
     gs += cnt;
+  }
   }
 }
 
@@ -624,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // decode grid completes.
 constexpr int kMergeWarps = 8;
 
-template <int D>
+template <int D, int W>
 __global__ void __launch_bounds__(kMergeWarps * 32, 4)
     decode_merge_kernel(const int32_t *__restrict__ seq_lens, int batch, int hkv, int G, int ctas,
                         int64_t limit, int paged, const float *__restrict__ po,
@@ -634,7 +665,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4)
   __shared__ float accs[kMergeWarps][D];
   __shared__ float wm[kMergeWarps], wz[kMergeWarps];
   __shared__ int redi[2][kMergeWarps];
-  const StageGeo geo = stage_geo(hkv, paged != 0);
+  const StageGeo geo = stage_geo<W>(hkv, paged != 0);
   const int b = blockIdx.x / geo.groups, hg = blockIdx.x % geo.groups;
   const int r = blockIdx.y;  // row within the segment: kv-head r / G, q-head r % G
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -736,30 +767,30 @@ cudaLaunchAttribute pdl_attr() {
   return attr;
 }
 
-template <int D>
+template <int D, int W>
 cudaError_t launch_d(const DecodeArgs &a, const KvView &cache, const DecodeMaps &dm, uint32_t *err,
                      cudaStream_t stream) {
   static bool configured = false;  // per-function attribute, set once per process
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem_bytes<D>(QATTN_MAX_BATCH));
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         smem_bytes<D, W>(QATTN_MAX_BATCH));
     if (e != cudaSuccess) return e;
     configured = true;
   }
   const int G = a.hq / cache.hkv;
   const bool paged = cache.page_table != nullptr;
-  const StageGeo geo = stage_geo(cache.hkv, paged);
+  const StageGeo geo = stage_geo<W>(cache.hkv, paged);
   Maps maps;
   maps.k = dm.k, maps.v = dm.v, maps.ks = dm.ks, maps.vs = dm.vs;
   cudaLaunchAttribute attr[1] = {pdl_attr()};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.ctas);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem_bytes<D>(a.batch);
+  cfg.blockDim = dim3(Layout<W>::kThreads);
+  cfg.dynamicSmemBytes = smem_bytes<D, W>(a.batch);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<D>, a, cache, maps, err);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<D, W>, a, cache, maps, err);
   if (e != cudaSuccess) return e;
   const int64_t limit = cache.page_table ? static_cast<int64_t>(cache.max_pages) * kPage : cache.capacity;
   cudaLaunchConfig_t mc = {};
@@ -768,31 +799,43 @@ cudaError_t launch_d(const DecodeArgs &a, const KvView &cache, const DecodeMaps 
   mc.stream = stream;
   mc.attrs = attr;
   mc.numAttrs = 1;
-  return cudaLaunchKernelEx(&mc, decode_merge_kernel<D>, a.seq_lens, a.batch, cache.hkv, G, a.ctas, limit,
+  return cudaLaunchKernelEx(&mc, decode_merge_kernel<D, W>, a.seq_lens, a.batch, cache.hkv, G, a.ctas, limit,
                             static_cast<int>(paged), static_cast<const float *>(a.partial_o), static_cast<const float *>(a.partial_lse),
                             a.out, a.lse);
 }
 
 }  // namespace
 
-DecodeGeometry decode_geometry(int head_dim, int hkv, bool paged) {
-  const StageGeo g = stage_geo(hkv, paged);
+int decode_layout(int batch, int hkv, int max_len, bool paged, int ranges) {
+  if (paged || ranges <= 0) return 8;
+  const int64_t rows = static_cast<int64_t>(batch) * hkv * max_len;
+  return rows >= static_cast<int64_t>(ranges) * 12 * Layout<12>::kRows ? 12 : 8;
+}
+
+DecodeGeometry decode_geometry(int head_dim, int hkv, bool paged, int warps) {
+  const StageGeo g = (paged || warps == 8) ? stage_geo<8>(hkv, paged) : stage_geo<12>(hkv, false);
   DecodeGeometry r;
   r.heads_per_stage = g.hb;
   r.tokens_per_stage = g.tokens;
   r.groups = g.groups;
   const bool split_pages = paged && g.tokens > kPage;
   r.box_heads = split_pages ? 1 : g.hb;
-  r.box_tokens = paged ? (g.tokens > kPage ? kPage : g.tokens) : g.tokens;
-  r.box_rows = r.box_tokens * head_dim / 256;
+  // TMA boxes hold at most 256 elements per dimension: a 384-token contiguous
+  // stage loads its scales as two boxes of 192 (its codes, 192 rows of 128 B,
+  // stay one box)
+  r.box_tokens = paged ? (g.tokens > kPage ? kPage : g.tokens) : (g.tokens > 256 ? g.tokens / 2 : g.tokens);
+  r.box_rows = (paged ? r.box_tokens : g.tokens) * head_dim / 256;
   return r;
 }
 
 cudaError_t launch_decode(const DecodeArgs &a, const KvView &cache, const DecodeMaps &maps, uint32_t *err,
                           cudaStream_t stream) {
   if (a.batch == 0 || a.ctas <= 0) return cudaSuccess;
-  return cache.head_dim == 128 ? launch_d<128>(a, cache, maps, err, stream)
-                               : launch_d<64>(a, cache, maps, err, stream);
+  if (cache.page_table || a.warps == 8)
+    return cache.head_dim == 128 ? launch_d<128, 8>(a, cache, maps, err, stream)
+                                 : launch_d<64, 8>(a, cache, maps, err, stream);
+  return cache.head_dim == 128 ? launch_d<128, 12>(a, cache, maps, err, stream)
+                               : launch_d<64, 12>(a, cache, maps, err, stream);
 }
 
 }  // namespace qattn

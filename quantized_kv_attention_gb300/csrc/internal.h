@@ -41,13 +41,19 @@ struct DecodeArgs {
   float *partial_o;
   float *partial_lse;
   int batch, hq, ctas;
+  int warps;         // CTA layout: 8 or 12 consumer warps (decode_layout)
   float scale_log2;  // softmax_scale * log2(e)
 };
 struct DecodeGeometry {
   int heads_per_stage, tokens_per_stage, groups;
   int box_heads, box_tokens, box_rows;  // TMA boxes of codes (rows of 128 B) and scales
 };
-DecodeGeometry decode_geometry(int head_dim, int hkv, bool paged);
+// CTA layout of a decode call: 12 consumer warps on 384-token stages for a
+// contiguous cache with at least 12 such stages of work per range (long
+// sequences), else 8 warps on 256-row stages.  `ranges` = the requested
+// split count, or the SM count for the automatic choice.
+int decode_layout(int batch, int hkv, int max_len, bool paged, int ranges);
+DecodeGeometry decode_geometry(int head_dim, int hkv, bool paged, int warps);
 struct DecodeMaps {
   CUtensorMap k, v, ks, vs;  // codes 3-D [heads][rows][128 B], scales 2-D [heads][tokens]
 };
