@@ -9,24 +9,30 @@
 // written back as fp16; a quantized tile is 4x smaller, so a deep ring of
 // tiles fits on chip.
 //
-// Stage.  One pipeline stage holds 256 (token, kv-head) rows: 32 tokens of 8
-// kv-heads (Hkv >= 8, heads in groups of 8) or 256/Hkv tokens of every head
-// (Hkv = 1, 2, 4).  It arrives as four TMA requests -- K codes, V codes, K
-// scales, V scales -- of 16 KB, 16 KB, 512 B and 512 B at D = 128: few large
-// requests are what lets one CTA per SM stream at HBM speed.
+// Stage.  One pipeline stage holds 32 (token, kv-head) rows per consumer
+// warp: 256 rows with 8 consumer warps (a contiguous cache: 256 tokens of one
+// kv-head; a paged pool: one 64-token page of 4 kv-heads, or 256/Hkv tokens of
+// every head when Hkv < 4), 384 tokens of one kv-head with 12 consumer warps
+// (contiguous caches whose ranges hold at least 12 such stages).  It arrives
+// as a few large TMA requests -- K codes, V codes (16 or 24 KB at D = 128), K
+// scales, V scales: few large requests are what lets one CTA per SM stream at
+// HBM speed.
 //
 // Work split.  Stages of all (sequence, head-group) segments form one list;
 // a persistent grid of one CTA per SM cuts it into equal contiguous ranges,
 // so every SM streams the same number of bytes whatever the lengths.  A
 // segment inside one range is finished by its CTA (fp16 O and lse); a segment
 // cut by range boundaries leaves one fp32 partial per CTA it touches, merged
-// by decode_merge_kernel (launched as a programmatic dependent).
+// by decode_merge_kernel (launched as a programmatic dependent, small enough
+// to be resident beside the decode CTAs).
 //
-// CTA roles.
-//   warp 8      producer: one elected thread issues the stage's TMA loads
-//               into a 5-deep mbarrier ring.
-//   warps 0-7   consumers: warp w owns kv-head w / (8 / HB) of the group and
-//               32 tokens of it per stage (HB = heads per stage).
+// CTA roles (W = 8 or 12 consumer warps).
+//   producer    one elected thread of warp W issues the stage's TMA loads
+//               into a 6-deep (W = 8) or 4-deep (W = 12) mbarrier ring; with
+//               W = 12 warps W..W+3 form a warpgroup that hands its registers
+//               to the consumers (setmaxnreg).
+//   warps 0..W-1 consumers: warp w owns kv-head w / (W / HB) of the stage and
+//               32 tokens of it (HB = kv-heads per stage).
 //     S^T (16 tokens x 8 q-heads) = codes_K . Q^T on mma.sync m16n8k16 with
 //       tokens on M.  A nibble becomes the fp16 subnormal u * 2^-24,
 //       u = code + 8, in one LOP3 (a high nibble gives 16 u * 2^-24 and Q
