@@ -13,14 +13,14 @@
 // head: two query heads of one GQA group at the same rows when the group
 // size is even, otherwise two consecutive row blocks of one head.  It walks
 // the visible keys in tiles of 128:
-//   dequant warps (4)   codes of key tile j (plain 16-byte loads) -> exact
-//                       fp16 integers in 128B-swizzled K and V operand
-//                       tiles (double-buffered); per-token factors
-//                       kf = s_K * softmax_scale * log2(e) and vf = s_V
+//   dequant warps (4)   codes of key tile j (plain 16-byte loads) -> K as
+//                       exact fp16 integers, V as fp16 code * s_V, in
+//                       128B-swizzled operand tiles (double-buffered); per-
+//                       token factors kf = s_K * softmax_scale * log2(e)
 //   MMA thread (1)      S_t = Q_t . codes_K^T   (M=128, N=128, K=D; SMEM x SMEM)
-//                       O_t += P_t . codes_V    (M=128, N=D, K=128; P from TMEM)
+//                       O_t += P_t . V          (M=128, N=D, K=128; P from TMEM)
 //   softmax warps (2x4) one thread per query row: x = S*kf - m, p = 2^x,
-//                       P = fp16(p * vf) back into TMEM over S; lazy max:
+//                       P = fp16(p) back into TMEM over S; lazy max:
 //                       m moves only when a 32-key chunk's sum exceeds 2^8,
 //                       then P so far and O are rescaled in TMEM
 // TMEM: S_0 | S_1 | O_0 | O_1 (512 columns).  The epilogue divides O by the
@@ -62,7 +62,7 @@ struct TcCfg {
   static constexpr int kKOff = 2 * kTileBytes;
   static constexpr int kVOff = kKOff + kKvBufs * kTileBytes;
   static constexpr int kScOff = kVOff + kKvBufs * kTileBytes;
-  static constexpr int kBarOff = kScOff + kScaleSlots * 2 * kBN * 4;
+  static constexpr int kBarOff = kScOff + kScaleSlots * kBN * 4;
   static constexpr int kSmem = kBarOff + 256 + 1024;  // barriers + TMEM base, alignment slack
   static constexpr uint32_t kIdescS = idesc_f16(kBM, kBN, false);
   static constexpr uint32_t kIdescPV = idesc_f16(kBM, D, true);
@@ -125,37 +125,31 @@ __device__ __forceinline__ Work decode_work(const PrefillArgs &a, int hkv) {
   return w;
 }
 
-// Two signed nibbles of byte `k` of w -> (low, high) as exact fp16 integers.
-// The byte is copied into both halves; the low nibble (xor 8) becomes the
-// mantissa of 1024 + (c + 8) in the low half, the high nibble the mantissa
-// of 1024 + 16 (c + 8) in the high half; one fma with per-half constants
-// leaves c in each.
-template <int K>
-__device__ __forceinline__ uint32_t nibble_pair(uint32_t w) {
-  uint32_t t, x;
-  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(t) : "r"(w), "n"(K | (4 << 4) | (K << 8) | (4 << 12)));
-  asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(x) : "r"(t), "r"(0x00F0000Fu), "r"(0x64806408u));
-  const __half2 mul = __halves2half2(__ushort_as_half(0x3C00), __ushort_as_half(0x2C00));   // 1, 1/16
-  const __half2 add = __halves2half2(__ushort_as_half(0xE408), __ushort_as_half(0xD480));   // -1032, -72
-  __half2 h = __hfma2(*reinterpret_cast<__half2 *>(&x), mul, add);
-  return *reinterpret_cast<uint32_t *>(&h);
-}
-
 // 8 codes (one 32-bit word) -> 16 bytes of fp16 at `dst`, in the order
-// d0 d4 d1 d5 d2 d6 d3 d7 that decode_nibbles yields.  Q is permuted the
-// same way inside every 8-column group (the contraction over d does not
-// see it) and the epilogue undoes it on O.
-__device__ __forceinline__ void store_word(uint32_t dst, uint32_t w) {
+// d0 d4 d1 d5 d2 d6 d3 d7 that decode_nibbles yields; when SCALED each code
+// is multiplied by the token's scale s2 (one rounding of code * scale).  Q is
+// permuted the same way inside every 8-column group (the contraction over d
+// does not see it) and the epilogue undoes it on O.
+template <bool SCALED>
+__device__ __forceinline__ void store_word(uint32_t dst, uint32_t w, __half2 s2) {
   uint32_t x[4];
   decode_nibbles(w, x);
+  if (SCALED) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __half2 y = __hmul2(*reinterpret_cast<__half2 *>(&x[k]), s2);
+      x[k] = *reinterpret_cast<const uint32_t *>(&y);
+    }
+  }
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(x[0]), "r"(x[1]), "r"(x[2]), "r"(x[3])
                : "memory");
 }
 
-// Writes one token row (D codes) as fp16 into a 128B-swizzled tile whose
-// rows are tokens: subtile d/64, row `tok`, 16-byte chunk (d%64)/8.
-template <int D>
-__device__ __forceinline__ void store_row(uint32_t tile, int tok, const uint4 (&c)[D / 32]) {
+// Writes one token row (D codes, times s2 when SCALED) as fp16 into a
+// 128B-swizzled tile whose rows are tokens: subtile d/64, row `tok`, 16-byte
+// chunk (d%64)/8.
+template <int D, bool SCALED>
+__device__ __forceinline__ void store_row(uint32_t tile, int tok, const uint4 (&c)[D / 32], __half2 s2) {
   const uint32_t row = tile + tok * 128;
   const uint32_t x = tok & 7;
 #pragma unroll
@@ -165,7 +159,7 @@ __device__ __forceinline__ void store_row(uint32_t tile, int tok, const uint4 (&
     for (int q = 0; q < 4; ++q) {
       const int chunk = i * 4 + q;  // 8 elements per chunk
       const uint32_t sub = chunk / 8, col = chunk % 8;
-      store_word(row + sub * TcCfg<D>::kSubBytes + ((col ^ x) << 4), words[q]);
+      store_word<SCALED>(row + sub * TcCfg<D>::kSubBytes + ((col ^ x) << 4), words[q], s2);
     }
   }
 }
@@ -223,16 +217,15 @@ __device__ __forceinline__ float chunk_max(const uint32_t (&s)[32], uint32_t kf,
 }
 
 // p = 2^(S * kf - m) over one chunk, lanes paired in f32x2 arithmetic; h gets
-// fp16 pairs of p * vf (the P operand); returns the sum of p.
+// the fp16 pairs of p (the P operand); returns the sum of p.
 template <bool MASK>
-__device__ __forceinline__ float chunk_exp(const uint32_t (&s)[32], uint32_t kf, uint32_t vf, float m, int k0,
-                                           int limit, uint32_t (&h)[16]) {
+__device__ __forceinline__ float chunk_exp(const uint32_t (&s)[32], uint32_t kf, float m, int k0, int limit,
+                                           uint32_t (&h)[16]) {
   const uint64_t nm = f2(-m, -m);
   uint64_t acc0 = f2(0.f, 0.f), acc1 = f2(0.f, 0.f);
 #pragma unroll
   for (int i = 0; i < 32; i += 4) {
     const uint4 f = lds128(kf + i * 4);
-    const uint4 g = lds128(vf + i * 4);
     float2 x01 = f2_split(fma2(f2(__uint_as_float(s[i]), __uint_as_float(s[i + 1])),
                                f2(__uint_as_float(f.x), __uint_as_float(f.y)), nm));
     float2 x23 = f2_split(fma2(f2(__uint_as_float(s[i + 2]), __uint_as_float(s[i + 3])),
@@ -243,12 +236,10 @@ __device__ __forceinline__ float chunk_exp(const uint32_t (&s)[32], uint32_t kf,
       if (k0 + i + 2 > limit) x23.x = -INFINITY;
       if (k0 + i + 3 > limit) x23.y = -INFINITY;
     }
-    const uint64_t p01 = f2(ex2(x01.x), ex2(x01.y)), p23 = f2(ex2(x23.x), ex2(x23.y));
-    acc0 = add2(acc0, p01), acc1 = add2(acc1, p23);
-    const float2 q01 = f2_split(mul2(p01, f2(__uint_as_float(g.x), __uint_as_float(g.y))));
-    const float2 q23 = f2_split(mul2(p23, f2(__uint_as_float(g.z), __uint_as_float(g.w))));
-    h[i / 2] = pack_half2(q01.x, q01.y);
-    h[i / 2 + 1] = pack_half2(q23.x, q23.y);
+    const float p0 = ex2(x01.x), p1 = ex2(x01.y), p2 = ex2(x23.x), p3 = ex2(x23.y);
+    acc0 = add2(acc0, f2(p0, p1)), acc1 = add2(acc1, f2(p2, p3));
+    h[i / 2] = pack_half2(p0, p1);
+    h[i / 2 + 1] = pack_half2(p2, p3);
   }
   const float2 t2 = f2_split(add2(acc0, acc1));
   return t2.x + t2.y;
@@ -263,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   Bars *bars = reinterpret_cast<Bars *>(smem + C::kBarOff);
-  float *scales = reinterpret_cast<float *>(smem + C::kScOff);  // [slot][kf 128 | vf 128]
+  float *scales = reinterpret_cast<float *>(smem + C::kScOff);  // [slot][kf of 128 keys]
   const uint32_t sbase = smem_u32(smem);
 
   const Work w = decode_work(a, cache.hkv);
@@ -418,7 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < n; ++j) {
       const int tok = j * kBN + tok_l;
       uint4 ck[D / 32], cv[D / 32];
-      float fk = 0.f, fv = 0.f;
+      float fk = 0.f;
+      __half2 sv = __float2half2_rn(0.f);
       const int64_t row = tok < a.nk ? cache_row(tok) : -1;
       if (tok < a.nk && row < 0) atomicOr(err, kFlagBadPage);
       if (row >= 0) {
@@ -428,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           cv[i] = __ldg(vc + row * (D / 32) + i);
         }
         fk = __half2float(ks[row]) * a.scale_log2;
-        fv = __half2float(vs[row]);
+        sv = __half2half2(vs[row]);
       } else {
 #pragma unroll
         for (int i = 0; i < D / 32; ++i) ck[i] = cv[i] = make_uint4(0, 0, 0, 0);
@@ -436,18 +428,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int buf = j % kKvBufs;
       const uint32_t par = ((j / kKvBufs) & 1) ^ 1;
       if (j >= kKvBufs && !wait_bounded(smem_u32(&bars->k_empty[buf]), par, err)) break;
-      store_row<D>(sbase + C::kKOff + buf * C::kTileBytes, tok_l, ck);
+      store_row<D, false>(sbase + C::kKOff + buf * C::kTileBytes, tok_l, ck, sv);
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&bars->k_full[buf]));
       const int slot = j % kScaleSlots;
       if (j >= kScaleSlots &&
           !wait_bounded(smem_u32(&bars->sc_empty[slot]), ((j / kScaleSlots) & 1) ^ 1, err))
         break;
-      scales[slot * 2 * kBN + tok_l] = fk;
-      scales[slot * 2 * kBN + kBN + tok_l] = fv;
+      scales[slot * kBN + tok_l] = fk;
       mbar_arrive(smem_u32(&bars->sc_full[slot]));
       if (j >= kKvBufs && !wait_bounded(smem_u32(&bars->v_empty[buf]), par, err)) break;
-      store_row<D>(sbase + C::kVOff + buf * C::kTileBytes, tok_l, cv);
+      store_row<D, true>(sbase + C::kVOff + buf * C::kTileBytes, tok_l, cv, sv);
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&bars->v_full[buf]));
     }
@@ -471,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = wait_bounded(smem_u32(&bars->sc_full[slot]), (j / kScaleSlots) & 1, err))) break;
       if (!(ok = wait_bounded(smem_u32(&bars->s_full[t]), j & 1, err))) break;
       tc_fence_after();
-      const uint32_t kf = smem_u32(scales + slot * 2 * kBN), vf = kf + kBN * 4;
+      const uint32_t kf = smem_u32(scales + slot * kBN);
       const int key0 = j * kBN;
       const bool masked = key0 + kBN - 1 > warp_limit;
 
@@ -495,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kBN / 32; ++c) {
           uint32_t cur[32], h[16];
           tmem_ld32(s_tm + c * 32, cur);
-          float cs = chunk_exp<M>(cur, kf + c * 128, vf + c * 128, m, key0 + c * 32, limit, h);
+          float cs = chunk_exp<M>(cur, kf + c * 128, m, key0 + c * 32, limit, h);
           if (__any_sync(0xffffffffu, !(cs <= static_cast<float>(kRedoSum)))) {
             // the reference maximum moves: rescale what was built on the old one
             const float mn = fmaxf(m, chunk_max<M>(cur, kf + c * 128, key0 + c * 32, limit));
@@ -503,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             m = mn, l *= alpha, tsum *= alpha;
             rescale_tmem<D>(s_tm, o_tm, c, j > 0, alpha);
             tmem_ld32(s_tm + c * 32, cur);  // S chunk c is intact: P so far only covers chunks < c/2
-            cs = chunk_exp<M>(cur, kf + c * 128, vf + c * 128, m, key0 + c * 32, limit, h);
+            cs = chunk_exp<M>(cur, kf + c * 128, m, key0 + c * 32, limit, h);
           }
           tsum += cs;
           tmem_st16(s_tm + c * 16, h);
