@@ -178,6 +178,30 @@ qattn_status qattn_decode(const uint16_t *q, const qattn_kv_cache *cache, const 
                           qattn_stream_t stream);
 
 /*
+ * qattn_decode_append -- one decoding step in one launch: each sequence's
+ * new key and value rows are quantized into the cache (as qattn_quantize_kv
+ * would, bit for bit) at position seq_lens[b] - 1 and attended together with
+ * the cached keys ([TA] §2.1: a decoding step appends k_t, v_t to the cache,
+ * then attends the new query against all of it).
+ *
+ *   k_new, v_new [batch, Hkv, D] of x_dtype (QATTN_F32 or QATTN_F16),
+ *                16-byte aligned, read-only
+ *   seq_lens     [batch] int32, lengths AFTER the append: the new row of
+ *                sequence b goes to position seq_lens[b] - 1 (nothing is
+ *                written for seq_lens[b] = 0); a position beyond the cache
+ *                (capacity, or max_pages_per_seq * 64) is not written and is
+ *                flagged QATTN_FLAG_BAD_PAGE, like a row of a missing page
+ *   everything else as qattn_decode (same workspace size).
+ * Errors: as qattn_decode; QATTN_ERR_INVALID_ARG for a NULL or misaligned
+ * k_new / v_new or another x_dtype.
+ */
+qattn_status qattn_decode_append(const uint16_t *q, const void *k_new, const void *v_new, qattn_dtype x_dtype,
+                                 const qattn_kv_cache *cache, const int32_t *seq_lens, int32_t batch,
+                                 int32_t num_q_heads, int32_t max_seq_len, float softmax_scale,
+                                 int32_t num_splits, void *workspace, size_t workspace_bytes,
+                                 uint16_t *out, float *lse, qattn_stream_t stream);
+
+/*
  * qattn_prefill -- Nq query rows per sequence against Nk cached keys
  * ([TA] §2.1 prefill, §2.2 FlashAttention tiling; dense contractions on
  * the tensor cores with the dequantization fused ahead of the operand

@@ -36,7 +36,7 @@ FLAG_WAIT_TIMEOUT, FLAG_BAD_PAGE, FLAG_TMEM = 1, 2, 4
 EXPORTS = (
     "qattn_quantize_kv", "qattn_decode_workspace_size", "qattn_decode", "qattn_prefill",
     "qattn_combine", "qattn_read_device_flags", "qattn_status_string", "qattn_last_error",
-    "qattn_version", "qattn_decode_noalloc", "qattn_check_wait_timeout",
+    "qattn_version", "qattn_decode_noalloc", "qattn_check_wait_timeout", "qattn_decode_append",
 )
 
 
@@ -90,6 +90,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qattn_version": (i32, []),
         "qattn_decode_noalloc": (i32, [vp, cache_p, vp, i32, i32, i32, f32, i32, vp, vp, vp]),
         "qattn_check_wait_timeout": (i32, [vp, i64, vp]),
+        "qattn_decode_append": (i32, [vp, vp, vp, i32, cache_p, vp, i32, i32, i32, f32, i32, vp, sz, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -206,6 +207,36 @@ def decode(q: torch.Tensor, cache: KvCache, seq_lens: torch.Tensor, max_seq_len:
     _check(load_library().qattn_decode(_ptr(q), ctypes.byref(st), _ptr(sl), B, Hq, max_seq_len,
                                        float(softmax_scale), num_splits, _ptr(workspace), ws_bytes,
                                        _ptr(out), _ptr(lse), _stream(q.device)), "qattn_decode")
+    return (out, lse) if return_lse else out
+
+
+def decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, cache: KvCache,
+                  seq_lens: torch.Tensor, max_seq_len: int, softmax_scale: float, num_splits: int = 0,
+                  workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                  lse: Optional[torch.Tensor] = None, return_lse: bool = False):
+    """One decoding step in one launch: k_new, v_new [B, Hkv, D] (fp32 or fp16)
+    are quantized into the cache at position seq_lens[b] - 1 (lengths after the
+    append), then q [B, Hq, D] fp16 attends over all seq_lens[b] keys."""
+    q = q.contiguous()
+    B, Hq, D = q.shape
+    if k_new.dtype != v_new.dtype or k_new.dtype not in (torch.float32, torch.float16):
+        raise ValueError("k_new and v_new must both be float32 or both float16")
+    k_new, v_new = k_new.contiguous(), v_new.contiguous()
+    dt = QATTN_F16 if k_new.dtype == torch.float16 else QATTN_F32
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    need = decode_workspace_size(B, Hq, cache.num_kv_heads, D, max_seq_len, num_splits)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    sl = seq_lens.to(device=q.device, dtype=torch.int32).contiguous()
+    st = cache.struct()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().qattn_decode_append(_ptr(q), _ptr(k_new), _ptr(v_new), dt, ctypes.byref(st), _ptr(sl),
+                                              B, Hq, max_seq_len, float(softmax_scale), num_splits,
+                                              _ptr(workspace), ws_bytes, _ptr(out), _ptr(lse), _stream(q.device)),
+           "qattn_decode_append")
     return (out, lse) if return_lse else out
 
 

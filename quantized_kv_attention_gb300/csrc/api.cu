@@ -263,10 +263,16 @@ size_t qattn_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t n
   return need;
 }
 
-qattn_status qattn_decode(const uint16_t *q, const qattn_kv_cache *cache, const int32_t *seq_lens,
-                          int32_t batch, int32_t num_q_heads, int32_t max_seq_len,
-                          float softmax_scale, int32_t num_splits, void *workspace,
-                          size_t workspace_size, uint16_t *out, float *lse, qattn_stream_t stream) {
+}  // extern "C"
+
+namespace qattn {
+namespace {
+
+// qattn_decode and qattn_decode_append: the latter passes the new rows.
+qattn_status decode_impl(const uint16_t *q, const void *k_new, const void *v_new, bool new_fp16,
+                         const qattn_kv_cache *cache, const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
+                         int32_t max_seq_len, float softmax_scale, int32_t num_splits, void *workspace,
+                         size_t workspace_size, uint16_t *out, float *lse, qattn_stream_t stream) {
   if (batch < 0 || num_q_heads <= 0 || max_seq_len < 0)
     return fail(QATTN_ERR_INVALID_ARG, "batch %d, num_q_heads %d, max_seq_len %d", batch, num_q_heads, max_seq_len);
   if (batch > QATTN_MAX_BATCH) return fail(QATTN_ERR_UNSUPPORTED, "batch %d > %d", batch, QATTN_MAX_BATCH);
@@ -284,6 +290,9 @@ qattn_status qattn_decode(const uint16_t *q, const qattn_kv_cache *cache, const 
   if (batch == 0) return QATTN_OK;
   if (!q || !seq_lens || !out) return fail(QATTN_ERR_INVALID_ARG, "q, seq_lens or out is NULL");
   if (!aligned16(q) || !aligned16(out)) return fail(QATTN_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+  if ((k_new == nullptr) != (v_new == nullptr)) return fail(QATTN_ERR_INVALID_ARG, "k_new and v_new: both or neither");
+  if (k_new && (!aligned16(k_new) || !aligned16(v_new)))
+    return fail(QATTN_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
   DeviceState *ds;
   if ((st = device_state(&ds)) != QATTN_OK) return st;
   const int G = num_q_heads / view.hkv;
@@ -307,10 +316,35 @@ qattn_status qattn_decode(const uint16_t *q, const qattn_kv_cache *cache, const 
   a.partial_o = static_cast<float *>(workspace);
   const size_t o_bytes = static_cast<size_t>(2) * ctas * slot_rows * view.head_dim * sizeof(float);
   a.partial_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + (o_bytes + 255) / 256 * 256);
+  a.k_new = k_new, a.v_new = v_new, a.new_fp16 = new_fp16 ? 1 : 0;
   a.batch = batch, a.hq = num_q_heads, a.ctas = ctas, a.warps = warps;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   cudaError_t e = launch_decode(a, view, maps, ds->status, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "decode launch");
+}
+
+}  // namespace
+}  // namespace qattn
+
+extern "C" {
+
+qattn_status qattn_decode(const uint16_t *q, const qattn_kv_cache *cache, const int32_t *seq_lens,
+                          int32_t batch, int32_t num_q_heads, int32_t max_seq_len,
+                          float softmax_scale, int32_t num_splits, void *workspace,
+                          size_t workspace_size, uint16_t *out, float *lse, qattn_stream_t stream) {
+  return decode_impl(q, nullptr, nullptr, false, cache, seq_lens, batch, num_q_heads, max_seq_len, softmax_scale,
+                     num_splits, workspace, workspace_size, out, lse, stream);
+}
+
+qattn_status qattn_decode_append(const uint16_t *q, const void *k_new, const void *v_new, qattn_dtype x_dtype,
+                                 const qattn_kv_cache *cache, const int32_t *seq_lens, int32_t batch,
+                                 int32_t num_q_heads, int32_t max_seq_len, float softmax_scale,
+                                 int32_t num_splits, void *workspace, size_t workspace_size, uint16_t *out,
+                                 float *lse, qattn_stream_t stream) {
+  if (x_dtype != QATTN_F32 && x_dtype != QATTN_F16) return fail(QATTN_ERR_INVALID_ARG, "x_dtype %d", (int)x_dtype);
+  if (batch > 0 && (!k_new || !v_new)) return fail(QATTN_ERR_INVALID_ARG, "k_new or v_new is NULL");
+  return decode_impl(q, k_new, v_new, x_dtype == QATTN_F16, cache, seq_lens, batch, num_q_heads, max_seq_len,
+                     softmax_scale, num_splits, workspace, workspace_size, out, lse, stream);
 }
 
 qattn_status qattn_prefill(const uint16_t *q, const qattn_kv_cache *cache, int32_t batch,

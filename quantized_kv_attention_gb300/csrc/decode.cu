@@ -47,6 +47,7 @@
 #include "../../include/qattn.h"
 #include "internal.h"
 #include "ptx.cuh"
+#include "quant_row.cuh"
 
 namespace qattn {
 namespace {
@@ -146,6 +147,55 @@ __device__ __forceinline__ Loc locate(int64_t gs, const int *prefix, int batch, 
   l.hg = r / l.n;
   l.s = r - l.hg * l.n;
   return l;
+}
+
+// Fused append (TurboAttention §2.1: a decoding step appends k_t, v_t to the cache
+// and attends over it).  The range holding the last stage of a segment
+// quantizes that segment's new rows (k and v of each kv-head of the group)
+// into the cache at position seq_lens[b] - 1, one warp per row, before its
+// producer issues any load; no other range reads those rows.  A new token
+// beyond the cache (a clamped length) or in a missing page is not written.
+template <int D>
+__device__ void append_rows(const DecodeArgs &a, const KvView &cache, int hb, int groups, const int *prefix,
+                            int64_t gs0, int64_t gs1, uint32_t *err, int warp, int lane, int nwarps) {
+  const int64_t limit = cache.page_table ? static_cast<int64_t>(cache.max_pages) * kPage : cache.capacity;
+  int item = 0;  // (segment, row) items of this range, dealt round-robin to the warps
+  for (int64_t gs = gs0; gs < gs1;) {
+    const Loc l = locate(gs, prefix, a.batch, groups);
+    const int64_t last = gs - l.s + l.n - 1;  // the segment's last stage
+    if (last < gs1) {
+      const int64_t pos = static_cast<int64_t>(__ldg(a.seq_lens + l.b)) - 1;  // the new token
+      for (int r = 0; r < 2 * hb; ++r, ++item) {
+        if (item % nwarps != warp) continue;
+        const int h = l.hg * hb + (r >> 1);
+        int64_t dst = -1;
+        if (pos >= limit) {
+          // the length was clamped (and flagged) by the caller of this function
+        } else if (!cache.page_table) {
+          dst = (static_cast<int64_t>(l.b) * cache.hkv + h) * cache.capacity + pos;
+        } else {
+          const int page = __ldg(cache.page_table + static_cast<int64_t>(l.b) * cache.max_pages + pos / kPage);
+          if (page >= 0 && page < cache.num_pages)
+            dst = (static_cast<int64_t>(page) * cache.hkv + h) * kPage + pos % kPage;
+          else if (lane == 0)
+            atomicOr(err, kFlagBadPage);
+        }
+        if (dst < 0) continue;  // warp-uniform
+        const bool is_v = r & 1;
+        const int64_t src_row = static_cast<int64_t>(l.b) * cache.hkv + h;
+        uint8_t *codes = (is_v ? cache.v_codes : cache.k_codes) + dst * (D / 2);
+        uint16_t *scale = (is_v ? cache.v_scales : cache.k_scales) + dst;
+        const void *src = is_v ? a.v_new : a.k_new;
+        if (a.new_fp16)
+          quantize_row_warp<__half, D>(static_cast<const __half *>(src) + src_row * D, codes, scale, lane);
+        else
+          quantize_row_warp<float, D>(static_cast<const float *>(src) + src_row * D, codes, scale, lane);
+        // the rows are read back by this CTA's TMA loads (async proxy)
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
+    }
+    gs = last + 1;
+  }
 }
 
 // Geometry of one stage.  A TMA box streams at full speed only when its
@@ -261,6 +311,10 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
   const int64_t gs0 = range_start(blockIdx.x, T, gridDim.x);
   const int64_t gs1 = range_start(blockIdx.x + 1, T, gridDim.x);
   if (gs1 <= gs0) return;
+  if (a.k_new) {  // fused append: written before any load of this range is issued
+    append_rows<D>(a, cache, geo.hb, geo.groups, prefix, gs0, gs1, err, warp, lane, kThreads / 32);
+    __syncthreads();
+  }
 
   if (warp >= kConsumerWarps) {
     // ------------------------------------------------------------ producer

@@ -40,6 +40,11 @@ struct DecodeArgs {
   float *lse;
   float *partial_o;
   float *partial_lse;
+  // fused append: the new K and V rows [batch, Hkv, D] (fp32, or fp16 when
+  // new_fp16), quantized into the cache at position seq_lens[b] - 1 before
+  // they are attended; NULL for a plain decode
+  const void *k_new, *v_new;
+  int new_fp16;
   int batch, hq, ctas;
   int warps;         // CTA layout: 8 or 12 consumer warps (decode_layout)
   float scale_log2;  // softmax_scale * log2(e)

@@ -1,0 +1,97 @@
+// quant_row.cuh -- quantization of one K or V row (D values) by one warp,
+// shared by the append kernel and the fused append + decode step so that
+// both write the same bits.
+//
+// TurboAttention (arXiv 2412.08585) §2.3: symmetric quantization, zero point
+// 0; "Quantized Cross-Attention ... In-SRAM Dequantization" §3.2: 4-bit codes
+// with one FP16 scale per token.  s = fp16(fp32(absmax / 7)), both roundings
+// to nearest even, saturating at 65504; code = round-half-even(x / s) clamped
+// to [-7, 7], decided by exact comparisons with the half-way points
+// (k + 1/2) s, which are exact in fp32 (s has 11 significant bits, 2k + 1 at
+// most 4 bits), so the result equals rounding of the exact quotient.
+#pragma once
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace qattn {
+
+template <typename T, int VPL>
+struct RowLoad;
+
+template <>
+struct RowLoad<float, 4> {
+  static __device__ __forceinline__ void load(const float *p, float (&x)[4]) {
+    float4 v = __ldg(reinterpret_cast<const float4 *>(p));
+    x[0] = v.x, x[1] = v.y, x[2] = v.z, x[3] = v.w;
+  }
+};
+template <>
+struct RowLoad<float, 2> {
+  static __device__ __forceinline__ void load(const float *p, float (&x)[2]) {
+    float2 v = __ldg(reinterpret_cast<const float2 *>(p));
+    x[0] = v.x, x[1] = v.y;
+  }
+};
+template <>
+struct RowLoad<__half, 4> {
+  static __device__ __forceinline__ void load(const __half *p, float (&x)[4]) {
+    uint2 v = __ldg(reinterpret_cast<const uint2 *>(p));
+    float2 a = __half22float2(*reinterpret_cast<__half2 *>(&v.x));
+    float2 b = __half22float2(*reinterpret_cast<__half2 *>(&v.y));
+    x[0] = a.x, x[1] = a.y, x[2] = b.x, x[3] = b.y;
+  }
+};
+template <>
+struct RowLoad<__half, 2> {
+  static __device__ __forceinline__ void load(const __half *p, float (&x)[2]) {
+    uint32_t v = __ldg(reinterpret_cast<const unsigned int *>(p));
+    float2 a = __half22float2(*reinterpret_cast<__half2 *>(&v));
+    x[0] = a.x, x[1] = a.y;
+  }
+};
+
+// Round-half-even of |x| / s on the exact quotient, clamped to 7: count the
+// half-way points (2j+1) s / 2 below |x|; at an exact half-way point round to
+// the even neighbour, i.e. count that point only when j is odd.
+__device__ __forceinline__ int code_of(float x, float s) {
+  const float ax = fabsf(x);
+  const float h = 0.5f * s;
+  int m = (ax > h) + (ax >= 3.f * h) + (ax > 5.f * h) + (ax >= 7.f * h) + (ax > 9.f * h) +
+          (ax >= 11.f * h) + (ax > 13.f * h);
+  return x < 0.f ? -m : m;
+}
+
+// Quantizes row `src` (D values of type T) with the 32 lanes of a warp: lane
+// i covers elements 4i..4i+3 (D = 128) or 2i, 2i+1 (D = 64) and writes their
+// packed nibbles (low nibble = even element) to dst_codes + i * D / 64; lane
+// 0 writes the fp16 scale.  Every lane of the warp must call it.
+template <typename T, int D>
+__device__ __forceinline__ void quantize_row_warp(const T *src, uint8_t *dst_codes, uint16_t *dst_scale,
+                                                  int lane) {
+  constexpr int VPL = D / 32;  // values per lane
+  float x[VPL];
+  RowLoad<T, VPL>::load(src + lane * VPL, x);
+  float am = 0.f;
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) am = fmaxf(am, fabsf(x[j]));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+
+  __half hs = __float2half_rn(__fdiv_rn(am, 7.0f));
+  if (__hisinf(hs)) hs = __ushort_as_half(0x7BFF);
+  const float s = __half2float(hs);
+
+  uint32_t packed = 0;
+  if (s > 0.f) {
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) packed |= static_cast<uint32_t>(code_of(x[j], s) & 0xF) << (4 * j);
+  }
+  uint8_t *dst = dst_codes + lane * (VPL / 2);
+  if constexpr (VPL == 4)
+    *reinterpret_cast<uint16_t *>(dst) = static_cast<uint16_t>(packed);
+  else
+    *dst = static_cast<uint8_t>(packed);
+  if (lane == 0) *dst_scale = __half_as_ushort(hs);
+}
+
+}  // namespace qattn

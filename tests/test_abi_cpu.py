@@ -123,3 +123,17 @@ def test_wait_check_rejects_bad_arguments():
     assert lib.qattn_check_wait_timeout(None, 1000, None) == qa.QATTN_ERR_INVALID_ARG
     assert lib.qattn_check_wait_timeout(FAKE, 0, None) == qa.QATTN_ERR_INVALID_ARG
     assert lib.qattn_check_wait_timeout(FAKE, (1 << 31) + 1, None) == qa.QATTN_ERR_INVALID_ARG
+
+
+def test_decode_append_rejects_bad_arguments():
+    c = _cache()
+
+    def da(k=FAKE, v=FAKE, dt=qa.QATTN_F32, batch=1):
+        return lib.qattn_decode_append(FAKE, k, v, dt, ctypes.byref(c), FAKE, batch, 4, 100, 1.0, 0, None, 0,
+                                       FAKE, None, None)
+    assert da(dt=7) == qa.QATTN_ERR_INVALID_ARG
+    assert da(k=None) == qa.QATTN_ERR_INVALID_ARG
+    assert da(v=None) == qa.QATTN_ERR_INVALID_ARG
+    assert da(k=FAKE + 4) == qa.QATTN_ERR_INVALID_ARG   # misaligned
+    assert da(v=FAKE + 8) == qa.QATTN_ERR_INVALID_ARG
+    assert da(batch=0) == qa.QATTN_OK                   # nothing to do
