@@ -305,7 +305,7 @@ def workload_config(name, splits=None):
         else:
             out["kv_bytes_per_step"] = cfg["B"] * cfg["Hkv"] * cfg["Nk"] * (D + 4)
     out["step"] = ("append all K/V rows (quantize) + causal prefill" if cfg["kind"] == "prefill"
-                   else "append one K/V row per sequence (quantize) + split-KV decode + combine")
+                   else "append one K/V row per sequence + split-KV decode (one fused launch) + merge")
     return out
 
 
@@ -348,30 +348,24 @@ def run_decode(name, args, device, gpu_index, rank):
             _fill_contiguous(qa, torch, c, B, Hkv, Nk, D, seed * 31 + r, device, oc, cfg.get("outlier_scale", 1.0))
         caches.append(c)
     torch.cuda.synchronize()
+    # lengths after the append: the new row of sequence b is token lens[b] - 1
     sl = torch.tensor([int(x) for x in lens], dtype=torch.int32, device=device)
-    start_pos = (sl - 1).clamp(min=0)
     q = torch.randn(B, Hq, D, device=device).half()
-    new_k = torch.randn(B, Hkv, 1, D, device=device)
-    new_v = torch.randn(B, Hkv, 1, D, device=device)
+    new_k = torch.randn(B, Hkv, D, device=device)
+    new_v = torch.randn(B, Hkv, D, device=device)
     out = torch.empty(B, Hq, D, dtype=torch.float16, device=device)
     ws_bytes = qa.decode_workspace_size(B, Hq, Hkv, D, max_len, splits)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
-    launches = 2 + (1 if ws_bytes > 0 else 0)
+    launches = 1 + (1 if ws_bytes > 0 else 0)
 
-    def append(r):
-        qa.quantize_kv(new_k, new_v, caches[r], start_pos)
-
-    def attend(r):
-        qa.decode(q, caches[r], sl, max_len, scale, splits, workspace=ws, out=out)
+    def step(r):  # append + attend, one qattn_decode_append call
+        qa.decode_append(q, new_k, new_v, caches[r], sl, max_len, scale, splits, workspace=ws, out=out)
 
     def enqueue_steps(n):
         for i in range(n):
-            append(i % copies)
-            attend(i % copies)
+            step(i % copies)
 
-    def enqueue_inner(n):
-        for i in range(n):
-            attend(i % copies)
+    enqueue_inner = enqueue_steps
 
     enqueue_steps(max(args.warmup, 1))
     torch.cuda.synchronize()
@@ -392,8 +386,7 @@ def run_decode(name, args, device, gpu_index, rank):
         q_d.copy_(q_h, non_blocking=True)
         k_d.copy_(k_h, non_blocking=True)
         v_d.copy_(v_h, non_blocking=True)
-        qa.quantize_kv(k_d, v_d, caches[r], start_pos)
-        qa.decode(q_d, caches[r], sl, max_len, scale, splits, workspace=ws, out=out)
+        qa.decode_append(q_d, k_d, v_d, caches[r], sl, max_len, scale, splits, workspace=ws, out=out)
         out_h.copy_(out, non_blocking=True)
 
     e2e_val = None
@@ -415,7 +408,7 @@ def run_decode(name, args, device, gpu_index, rank):
 
     peaks, pk_src = measured_peaks()
     achieved = kv_bytes / (dec_ms / 1e3) / 1e9
-    traffic = profiled_traffic(f"decode_{name}_ncu.txt", source_digest("decode.cu", "ptx.cuh", "combine.cu"),
+    traffic = profiled_traffic(f"decode_{name}_ncu.txt", source_digest("decode.cu", "ptx.cuh", "quant_row.cuh"),
                                kv_bytes)
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
@@ -427,7 +420,7 @@ def run_decode(name, args, device, gpu_index, rank):
                   "parallelism": f"replicas x{world}", "timing": "CUDA graphs of the API calls"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                     "traffic": traffic, "kernel": "decode+combine (one qattn_decode call)",
+                     "traffic": traffic, "kernel": "decode with fused append + merge (one qattn_decode_append call)",
                      "peak_source": pk_src, "us_per_launch": round(dec_ms * 1e3, 3)},
         "e2e": {"value": e2e_val, "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},

@@ -95,7 +95,7 @@ struct Cfg {
 template <int D, int W>
 __host__ __device__ constexpr int smem_bytes(int batch) {
   return Cfg<D, W>::kRing + Cfg<D, W>::kQSlot + 2 * W * 8 * 4 + (2 * batch + 1) * 4 +
-         (2 * Cfg<D, W>::kStages + 2) * 8 + Cfg<D, W>::kStages * 4 + 16 + 1024;
+         (2 * Cfg<D, W>::kStages + 3) * 8 + Cfg<D, W>::kStages * 4 + 16 + 1024;
 }
 
 template <int W>
@@ -152,9 +152,11 @@ __device__ __forceinline__ Loc locate(int64_t gs, const int *prefix, int batch, 
 // Fused append (TurboAttention §2.1: a decoding step appends k_t, v_t to the cache
 // and attends over it).  The range holding the last stage of a segment
 // quantizes that segment's new rows (k and v of each kv-head of the group)
-// into the cache at position seq_lens[b] - 1, one warp per row, before its
-// producer issues any load; no other range reads those rows.  A new token
-// beyond the cache (a clamped length) or in a missing page is not written.
+// into the cache at position seq_lens[b] - 1, one consumer warp per row,
+// while its producer streams the earlier stages; the producer loads the
+// stage that holds them only after the consumers' `appended` barrier.  No
+// other range reads those rows.  A new token beyond the cache (a clamped
+// length) or in a missing page is not written.
 template <int D>
 __device__ void append_rows(const DecodeArgs &a, const KvView &cache, int hb, int groups, const int *prefix,
                             int64_t gs0, int64_t gs1, uint32_t *err, int warp, int lane, int nwarps) {
@@ -253,7 +255,8 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
   uint64_t *empty = full + C::kStages;
   uint64_t *qfull = empty + C::kStages;
   uint64_t *qempty = qfull + 1;
-  int *valid = reinterpret_cast<int *>(qempty + 1);                  // [kStages]: 0 = missing page
+  uint64_t *appended = qempty + 1;                                   // fused append done (consumer warps)
+  int *valid = reinterpret_cast<int *>(appended + 1);                // [kStages]: 0 = missing page
   volatile int *abort_flag = valid + C::kStages;                     // set after a timed-out wait
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -267,6 +270,7 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
     }
     mbar_init(smem_u32(qfull), 1);
     mbar_init(smem_u32(qempty), kConsumerWarps);
+    mbar_init(smem_u32(appended), kConsumerWarps);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -311,10 +315,6 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
   const int64_t gs0 = range_start(blockIdx.x, T, gridDim.x);
   const int64_t gs1 = range_start(blockIdx.x + 1, T, gridDim.x);
   if (gs1 <= gs0) return;
-  if (a.k_new) {  // fused append: written before any load of this range is issued
-    append_rows<D>(a, cache, geo.hb, geo.groups, prefix, gs0, gs1, err, warp, lane, kThreads / 32);
-    __syncthreads();
-  }
 
   if (warp >= kConsumerWarps) {
     // ------------------------------------------------------------ producer
@@ -325,6 +325,7 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
       const int rows_per_tok = D / 2;  // code bytes per token
       const uint32_t qbytes = geo.hb * G * D * 2;
       int it = 0, seg = 0;
+      bool rows_in = a.k_new == nullptr;  // the fused append's rows are in the cache
       for (int64_t gs = gs0; gs < gs1; ++seg) {
         const Loc l = locate(gs, prefix, B, geo.groups);
         const int cnt = static_cast<int>(min(static_cast<int64_t>(l.n - l.s), gs1 - gs));
@@ -348,6 +349,13 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
               !mbar_wait(smem_u32(empty + s), ph ^ 1, err, *abort_flag ? kDrainCycles : kWaitCycles)) {
             *abort_flag = 1;  // stop issuing; the consumers drain with short waits
             return;
+          }
+          if (!rows_in && l.s + j == l.n - 1) {  // a segment's last stage holds its new rows
+            rows_in = true;
+            if (!mbar_wait(smem_u32(appended), 0, err, *abort_flag ? kDrainCycles : kWaitCycles)) {
+              *abort_flag = 1;
+              return;
+            }
           }
           const int tok0 = (l.s + j) * geo.tokens;  // first token of the stage in the sequence
           const uint32_t full_s = smem_u32(full + s);
@@ -442,6 +450,14 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
       const int vt = tok_w + t * 16 + ((q & 2) ? 8 : 0) + (lane & 7);
       voff[t][jp] = swz128(kofs + vt * (D / 2) + (2 * jp + (q & 1)) * 16);
     }
+  }
+  if (a.k_new) {
+    // The fused append, while the producer fills the ring: the rows are
+    // fenced to the async proxy, then released to the producer, which
+    // loads no segment's last stage before this barrier completes.
+    append_rows<D>(a, cache, geo.hb, geo.groups, prefix, gs0, gs1, err, warp, lane, kConsumerWarps);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(appended));
   }
   const uint32_t ring = smem_u32(smem);
   int cur = 0;           // ring slot of the next stage
