@@ -686,15 +686,27 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
       const int r = idx / (D / 4), d = (idx - r * (D / 4)) * 4;  // row = kv-head in stage * G + q-head
       const int hh = r / G, h = r - hh * G;
       const int w0 = hh * geo.wph;
-      float M = smm[w0 * 8 + h];
-      for (int w = 1; w < geo.wph; ++w) M = fmaxf(M, smm[(w0 + w) * 8 + h]);
+      // all warps' values are loaded before any is used (W is the bound of wph)
+      float mw[W], lw[W];
+      float4 xw[W];
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        const bool in = w < geo.wph;
+        const int k = (w0 + w) * 8 + h;
+        mw[w] = in ? smm[k] : -INFINITY;
+        lw[w] = in ? sml[k] : 0.f;
+        xw[w] = in ? *reinterpret_cast<const float4 *>(mo + k * C::kMergePitch + d) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      float M = mw[0];
+#pragma unroll
+      for (int w = 1; w < W; ++w) M = fmaxf(M, mw[w]);
       float L = 0.f;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int w = 0; w < geo.wph; ++w) {
-        const float sc = ex2(smm[(w0 + w) * 8 + h] - M);
-        L += sc * sml[(w0 + w) * 8 + h];
-        const float4 x = *reinterpret_cast<const float4 *>(mo + ((w0 + w) * 8 + h) * C::kMergePitch + d);
-        acc.x += sc * x.x, acc.y += sc * x.y, acc.z += sc * x.z, acc.w += sc * x.w;
+#pragma unroll
+      for (int w = 0; w < W; ++w) {
+        const float sc = w < geo.wph ? ex2(mw[w] - M) : 0.f;
+        L += sc * lw[w];
+        acc.x += sc * xw[w].x, acc.y += sc * xw[w].y, acc.z += sc * xw[w].z, acc.w += sc * xw[w].w;
       }
       const bool live = L > 0.f;
       const float inv = live ? 1.f / L : 0.f;
