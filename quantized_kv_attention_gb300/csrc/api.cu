@@ -317,6 +317,7 @@ qattn_status decode_impl(const uint16_t *q, const void *k_new, const void *v_new
   const size_t o_bytes = static_cast<size_t>(2) * ctas * slot_rows * view.head_dim * sizeof(float);
   a.partial_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + (o_bytes + 255) / 256 * 256);
   a.k_new = k_new, a.v_new = v_new, a.new_fp16 = new_fp16 ? 1 : 0;
+  a.max_len = max_seq_len;
   a.batch = batch, a.hq = num_q_heads, a.ctas = ctas, a.warps = warps;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   cudaError_t e = launch_decode(a, view, maps, ds->status, reinterpret_cast<cudaStream_t>(stream));

@@ -280,6 +280,29 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
     prefetch_tmap(&maps.ks);
     prefetch_tmap(&maps.vs);
   }
+  // Speculative L2 prefetch of this range's first stages, as if every
+  // sequence held max_len keys (the common case), issued before the lengths
+  // are known; the real loads follow the lengths.  Byte counts stay inside
+  // the cache (capacity), so a wrong guess only costs bandwidth.
+  if (!paged && threadIdx.x == kConsumerWarps * 32 + 1) {
+    const int64_t per = (static_cast<int64_t>(min(a.max_len, static_cast<int>(cache.capacity))) + geo.tokens - 1) / geo.tokens;
+    const int64_t Tg = static_cast<int64_t>(B) * geo.groups * per;
+    if (per > 0) {
+      const int64_t g0 = range_start(blockIdx.x, Tg, gridDim.x), g1 = range_start(blockIdx.x + 1, Tg, gridDim.x);
+      for (int k = 0; k < 2 && g0 + k < g1; ++k) {
+        const int64_t gs = g0 + k, sg = gs / per;
+        const int64_t tok0 = (gs - sg * per) * geo.tokens;
+        const int64_t head = (sg / geo.groups) * hkv + (sg % geo.groups) * geo.hb;
+        const int64_t ntok = min(static_cast<int64_t>(geo.tokens), cache.capacity - tok0);
+        const int64_t row = head * cache.capacity + tok0;
+        const uint32_t cb = static_cast<uint32_t>(ntok * (D / 2)), sb = static_cast<uint32_t>(ntok * 2);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cache.k_codes + row * (D / 2)), "r"(cb) : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cache.v_codes + row * (D / 2)), "r"(cb) : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cache.k_scales + row), "r"(sb) : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cache.v_scales + row), "r"(sb) : "memory");
+      }
+    }
+  }
   pdl_wait();                // inputs may come from the preceding kernel on the stream
   pdl_launch_dependents();   // the merge kernel may be scheduled as SMs free up
 

@@ -45,6 +45,7 @@ struct DecodeArgs {
   // they are attended; NULL for a plain decode
   const void *k_new, *v_new;
   int new_fp16;
+  int max_len;       // the caller's bound of seq_lens (a guess for early prefetches)
   int batch, hq, ctas;
   int warps;         // CTA layout: 8 or 12 consumer warps (decode_layout)
   float scale_log2;  // softmax_scale * log2(e)
