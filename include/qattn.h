@@ -95,6 +95,7 @@ typedef enum qattn_dtype {
 #define QATTN_FLAG_WAIT_TIMEOUT 1u /* a pipeline wait gave up (kernel returned early) */
 #define QATTN_FLAG_BAD_PAGE 2u     /* a page id or length was out of range; rows skipped */
 #define QATTN_FLAG_TMEM 4u         /* tensor-memory allocation failed */
+#define QATTN_FLAG_BUFFER_FULL 8u  /* qattn_flashq_append met a full buffer; the row was dropped */
 
 /*
  * Where the quantized K and V live.  Passed by host pointer; the struct
@@ -253,6 +254,69 @@ qattn_status qattn_read_device_flags(uint32_t *flags, int32_t clear);
  * pages have no counterpart: this is the library's own failure check.
  */
 qattn_status qattn_check_wait_timeout(uint32_t *flags, int64_t limit_cycles, qattn_stream_t stream);
+
+/*
+ * FlashQ-style decode buffer ([TA] §3.3): decoded K/V rows wait in a buffer
+ * of QATTN_FLASHQ_ROWS rows per (sequence, kv-head) as int8 codes with one
+ * universal scale per (sequence, kv-head) and tensor, outliers clamped, and
+ * a full buffer is compressed into the INT4 cache.  Readings of the page
+ * (which gives no formula for the universal scale):
+ *   R      running max |x^| of the rows already cached for that (sequence,
+ *          kv-head) and tensor = 7 * their largest INT4 scale; while R is 0
+ *          (no or all-zero history) each appended row sets R to its absmax
+ *   u      fp16(fp32(R / 127)), both roundings to nearest even, saturating
+ *   code   clamp(round_half_even(x / u), -127, 127) on the exact quotient
+ *   value  x~ = code * u
+ *   flush  a full buffer's x~ rows go through the INT4 codec into the cache
+ *          at positions cache_lens[b] .. cache_lens[b] + 63; R rises to the
+ *          new rows' 7 * max scale if larger; u follows; the buffer empties
+ * A decode step with the buffer: qattn_decode over the cached rows (with an
+ * lse array), qattn_flashq_append of the step's new rows, qattn_flashq_attend
+ * (merges the buffered rows into out / lse), and every 64 steps
+ * qattn_flashq_flush (then the caller's cached lengths grow by 64).
+ * Sequences advance together: one appended row per sequence per call.
+ */
+#define QATTN_FLASHQ_ROWS 64
+
+typedef struct qattn_flashq_buffer {
+  int8_t *k_codes;     /* [batch, Hkv, 64, D] int8, 16-byte aligned */
+  int8_t *v_codes;     /* [batch, Hkv, 64, D] int8, 16-byte aligned */
+  uint16_t *k_scale;   /* [batch, Hkv] fp16 universal scales u */
+  uint16_t *v_scale;   /* [batch, Hkv] fp16 */
+  float *k_range;      /* [batch, Hkv] R */
+  float *v_range;      /* [batch, Hkv] R */
+  int32_t *count;      /* [batch] rows buffered, 0..64 */
+  int32_t head_dim;    /* D: 64 or 128, as the cache */
+  int32_t num_kv_heads; /* Hkv (1..64), as the cache */
+} qattn_flashq_buffer;
+
+/* R and u from the first cache_lens[b] cached rows of every (sequence,
+ * kv-head); empties the buffers.  cache_lens: device int32 [batch]. */
+qattn_status qattn_flashq_init(const qattn_flashq_buffer *buf, const qattn_kv_cache *cache,
+                               const int32_t *cache_lens, int32_t batch, qattn_stream_t stream);
+
+/* One new K and V row per (sequence, kv-head): k_new, v_new [batch, Hkv, D]
+ * of x_dtype (QATTN_F32 or QATTN_F16), 16-byte aligned.  A full buffer drops
+ * the row and raises QATTN_FLAG_BUFFER_FULL. */
+qattn_status qattn_flashq_append(const void *k_new, const void *v_new, qattn_dtype x_dtype,
+                                 const qattn_flashq_buffer *buf, int32_t batch, qattn_stream_t stream);
+
+/* Merges attention over the buffered rows into out [batch, Hq, D] fp16 and
+ * lse [batch, Hq] fp32 (required), which hold a decode over the cached rows
+ * (lse = -inf where those were empty): L = log(e^lse + e^lse_buf), out =
+ * e^(lse - L) out + e^(lse_buf - L) O_buf.  q [batch, Hq, D] fp16, the same
+ * query; GQA as in qattn_decode.  Sequences with an empty buffer are left as
+ * they are. */
+qattn_status qattn_flashq_attend(const uint16_t *q, const qattn_flashq_buffer *buf, int32_t batch,
+                                 int32_t num_q_heads, float softmax_scale, uint16_t *out, float *lse,
+                                 qattn_stream_t stream);
+
+/* Moves every full buffer into the cache at positions cache_lens[b] ..
+ * cache_lens[b] + 63 (device int32 [batch], the rows already cached); rows
+ * past the cache or in a missing page are not written and raise
+ * QATTN_FLAG_BAD_PAGE.  Buffers that are not full are untouched. */
+qattn_status qattn_flashq_flush(const qattn_flashq_buffer *buf, const qattn_kv_cache *cache,
+                                const int32_t *cache_lens, int32_t batch, qattn_stream_t stream);
 
 /* Bytes of the library-owned scratch behind qattn_decode_noalloc (8 MiB per device). */
 #define QATTN_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)

@@ -30,13 +30,15 @@ QATTN_F32, QATTN_F16 = 0, 1
 PAGE_SIZE = 64
 MAX_GROUP = 8
 MAX_SPLITS = 1024
-FLAG_WAIT_TIMEOUT, FLAG_BAD_PAGE, FLAG_TMEM = 1, 2, 4
+FLAG_WAIT_TIMEOUT, FLAG_BAD_PAGE, FLAG_TMEM, FLAG_BUFFER_FULL = 1, 2, 4, 8
+FLASHQ_ROWS = 64
 
 # Every symbol include/qattn.h declares.
 EXPORTS = (
     "qattn_quantize_kv", "qattn_decode_workspace_size", "qattn_decode", "qattn_prefill",
     "qattn_combine", "qattn_read_device_flags", "qattn_status_string", "qattn_last_error",
     "qattn_version", "qattn_decode_noalloc", "qattn_check_wait_timeout", "qattn_decode_append",
+    "qattn_flashq_init", "qattn_flashq_append", "qattn_flashq_attend", "qattn_flashq_flush",
 )
 
 
@@ -62,6 +64,21 @@ class KvCacheStruct(ctypes.Structure):
         ("page_size", ctypes.c_int32),
         ("capacity", ctypes.c_int64),
         ("num_pages", ctypes.c_int64),
+    ]
+
+
+class FlashqBufferStruct(ctypes.Structure):
+    """Layout of ``qattn_flashq_buffer``."""
+    _fields_ = [
+        ("k_codes", ctypes.c_void_p),
+        ("v_codes", ctypes.c_void_p),
+        ("k_scale", ctypes.c_void_p),
+        ("v_scale", ctypes.c_void_p),
+        ("k_range", ctypes.c_void_p),
+        ("v_range", ctypes.c_void_p),
+        ("count", ctypes.c_void_p),
+        ("head_dim", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
     ]
 
 
@@ -91,6 +108,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qattn_decode_noalloc": (i32, [vp, cache_p, vp, i32, i32, i32, f32, i32, vp, vp, vp]),
         "qattn_check_wait_timeout": (i32, [vp, i64, vp]),
         "qattn_decode_append": (i32, [vp, vp, vp, i32, cache_p, vp, i32, i32, i32, f32, i32, vp, sz, vp, vp, vp]),
+        "qattn_flashq_init": (i32, [ctypes.POINTER(FlashqBufferStruct), cache_p, vp, i32, vp]),
+        "qattn_flashq_append": (i32, [vp, vp, i32, ctypes.POINTER(FlashqBufferStruct), i32, vp]),
+        "qattn_flashq_attend": (i32, [vp, ctypes.POINTER(FlashqBufferStruct), i32, i32, f32, vp, vp, vp]),
+        "qattn_flashq_flush": (i32, [ctypes.POINTER(FlashqBufferStruct), cache_p, vp, i32, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -238,6 +259,76 @@ def decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, cac
                                               _ptr(workspace), ws_bytes, _ptr(out), _ptr(lse), _stream(q.device)),
            "qattn_decode_append")
     return (out, lse) if return_lse else out
+
+
+@dataclass
+class FlashqBuffer:
+    """Caller-owned decode buffer (qattn_flashq_buffer): 64 int8 rows per
+    (sequence, kv-head) for K and V, their universal scales and ranges, and the
+    number of rows buffered per sequence."""
+    k_codes: torch.Tensor   # [B, Hkv, 64, D] int8
+    v_codes: torch.Tensor
+    k_scale: torch.Tensor   # [B, Hkv] fp16
+    v_scale: torch.Tensor
+    k_range: torch.Tensor   # [B, Hkv] fp32
+    v_range: torch.Tensor
+    count: torch.Tensor     # [B] int32
+    head_dim: int
+    num_kv_heads: int
+
+    @staticmethod
+    def create(batch, num_kv_heads, head_dim, device="cuda"):
+        codes = lambda: torch.zeros(batch, num_kv_heads, FLASHQ_ROWS, head_dim, dtype=torch.int8, device=device)
+        half = lambda: torch.zeros(batch, num_kv_heads, dtype=torch.float16, device=device)
+        f32 = lambda: torch.zeros(batch, num_kv_heads, dtype=torch.float32, device=device)
+        return FlashqBuffer(codes(), codes(), half(), half(), f32(), f32(),
+                            torch.zeros(batch, dtype=torch.int32, device=device), head_dim, num_kv_heads)
+
+    def struct(self) -> FlashqBufferStruct:
+        s = FlashqBufferStruct()
+        s.k_codes, s.v_codes = self.k_codes.data_ptr(), self.v_codes.data_ptr()
+        s.k_scale, s.v_scale = self.k_scale.data_ptr(), self.v_scale.data_ptr()
+        s.k_range, s.v_range = self.k_range.data_ptr(), self.v_range.data_ptr()
+        s.count = self.count.data_ptr()
+        s.head_dim, s.num_kv_heads = self.head_dim, self.num_kv_heads
+        return s
+
+
+def flashq_init(buf: FlashqBuffer, cache: KvCache, cache_lens: torch.Tensor) -> None:
+    """Universal scales from the first cache_lens[b] cached rows; empty buffers."""
+    cl = cache_lens.to(device=buf.count.device, dtype=torch.int32).contiguous()
+    bs, cs = buf.struct(), cache.struct()
+    _check(load_library().qattn_flashq_init(ctypes.byref(bs), ctypes.byref(cs), _ptr(cl), cl.numel(),
+                                            _stream(buf.count.device)), "qattn_flashq_init")
+
+
+def flashq_append(k_new: torch.Tensor, v_new: torch.Tensor, buf: FlashqBuffer) -> None:
+    """One new K and V row per (sequence, kv-head), [B, Hkv, D] fp32 or fp16."""
+    if k_new.dtype != v_new.dtype or k_new.dtype not in (torch.float32, torch.float16):
+        raise ValueError("k_new and v_new must both be float32 or both float16")
+    k_new, v_new = k_new.contiguous(), v_new.contiguous()
+    dt = QATTN_F16 if k_new.dtype == torch.float16 else QATTN_F32
+    bs = buf.struct()
+    _check(load_library().qattn_flashq_append(_ptr(k_new), _ptr(v_new), dt, ctypes.byref(bs), k_new.shape[0],
+                                              _stream(k_new.device)), "qattn_flashq_append")
+
+
+def flashq_attend(q: torch.Tensor, buf: FlashqBuffer, softmax_scale: float, out: torch.Tensor,
+                  lse: torch.Tensor) -> None:
+    """Merge attention over the buffered rows into out / lse (a decode over the cached rows)."""
+    q = q.contiguous()
+    B, Hq, _ = q.shape
+    bs = buf.struct()
+    _check(load_library().qattn_flashq_attend(_ptr(q), ctypes.byref(bs), B, Hq, float(softmax_scale), _ptr(out),
+                                              _ptr(lse), _stream(q.device)), "qattn_flashq_attend")
+
+
+def flashq_flush(buf: FlashqBuffer, cache: KvCache, cache_lens: torch.Tensor) -> None:
+    """Full buffers -> 64 INT4 rows each at positions cache_lens[b] .. + 63."""
+    cl = cache_lens.to(device=buf.count.device, dtype=torch.int32).contiguous()
+    bs, cs = buf.struct(), cache.struct()
+    _check(load_library().qattn_flashq_flush(ctypes.byref(bs), ctypes.byref(cs), _ptr(cl), cl.numel(),
+                                             _stream(buf.count.device)), "qattn_flashq_flush")
 
 
 def prefill(q: torch.Tensor, cache: KvCache, nk: int, softmax_scale: float, causal: bool = True,

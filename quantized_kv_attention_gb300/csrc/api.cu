@@ -348,6 +348,105 @@ qattn_status qattn_decode_append(const uint16_t *q, const void *k_new, const voi
                      softmax_scale, num_splits, workspace, workspace_size, out, lse, stream);
 }
 
+}  // extern "C"
+
+namespace qattn {
+namespace {
+
+// Validates a decode buffer (and, when given, that it matches the cache).
+qattn_status check_flashq(const qattn_flashq_buffer *b, int batch, FlashqView *v) {
+  if (!b) return fail(QATTN_ERR_INVALID_ARG, "flashq buffer is NULL");
+  if (batch < 0 || batch > QATTN_MAX_BATCH) return fail(QATTN_ERR_INVALID_ARG, "batch %d", batch);
+  if (b->head_dim != 64 && b->head_dim != 128) return fail(QATTN_ERR_UNSUPPORTED, "head_dim %d", b->head_dim);
+  if (b->num_kv_heads < 1 || b->num_kv_heads > 64)
+    return fail(QATTN_ERR_INVALID_ARG, "num_kv_heads %d (1..64)", b->num_kv_heads);
+  if (!b->k_codes || !b->v_codes || !b->k_scale || !b->v_scale || !b->k_range || !b->v_range || !b->count)
+    return fail(QATTN_ERR_INVALID_ARG, "a flashq buffer pointer is NULL");
+  if (!aligned16(b->k_codes) || !aligned16(b->v_codes))
+    return fail(QATTN_ERR_INVALID_ARG, "flashq codes must be 16-byte aligned");
+  v->k_codes = b->k_codes, v->v_codes = b->v_codes, v->k_scale = b->k_scale, v->v_scale = b->v_scale;
+  v->k_range = b->k_range, v->v_range = b->v_range, v->count = b->count;
+  v->hkv = b->num_kv_heads, v->head_dim = b->head_dim;
+  return QATTN_OK;
+}
+
+qattn_status check_flashq_cache(const qattn_flashq_buffer *b, const qattn_kv_cache *cache,
+                                const int32_t *cache_lens, int batch, FlashqView *fv, KvView *kv) {
+  qattn_status st = check_flashq(b, batch, fv);
+  if (st != QATTN_OK) return st;
+  uint64_t code_bytes = 0;
+  if ((st = check_cache(cache, batch, kv, &code_bytes)) != QATTN_OK) return st;
+  if (kv->head_dim != fv->head_dim || kv->hkv != fv->hkv)
+    return fail(QATTN_ERR_INVALID_ARG, "buffer (D %d, Hkv %d) and cache (D %d, Hkv %d) differ", fv->head_dim,
+                fv->hkv, kv->head_dim, kv->hkv);
+  if (batch > 0 && !cache_lens) return fail(QATTN_ERR_INVALID_ARG, "cache_lens is NULL");
+  return QATTN_OK;
+}
+
+}  // namespace
+}  // namespace qattn
+
+extern "C" {
+
+qattn_status qattn_flashq_init(const qattn_flashq_buffer *buf, const qattn_kv_cache *cache,
+                               const int32_t *cache_lens, int32_t batch, qattn_stream_t stream) {
+  FlashqView fv;
+  KvView kv;
+  qattn_status st = check_flashq_cache(buf, cache, cache_lens, batch, &fv, &kv);
+  if (st != QATTN_OK || batch == 0) return st;
+  DeviceState *ds;
+  if ((st = device_state(&ds)) != QATTN_OK) return st;
+  cudaError_t e = launch_flashq_init(fv, kv, cache_lens, batch, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "flashq init launch");
+}
+
+qattn_status qattn_flashq_append(const void *k_new, const void *v_new, qattn_dtype x_dtype,
+                                 const qattn_flashq_buffer *buf, int32_t batch, qattn_stream_t stream) {
+  if (x_dtype != QATTN_F32 && x_dtype != QATTN_F16) return fail(QATTN_ERR_INVALID_ARG, "x_dtype %d", (int)x_dtype);
+  FlashqView fv;
+  qattn_status st = check_flashq(buf, batch, &fv);
+  if (st != QATTN_OK || batch == 0) return st;
+  if (!k_new || !v_new) return fail(QATTN_ERR_INVALID_ARG, "k_new or v_new is NULL");
+  if (!aligned16(k_new) || !aligned16(v_new)) return fail(QATTN_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+  DeviceState *ds;
+  if ((st = device_state(&ds)) != QATTN_OK) return st;
+  cudaError_t e = launch_flashq_append(k_new, v_new, x_dtype == QATTN_F16, fv, batch, ds->status,
+                                       reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "flashq append launch");
+}
+
+qattn_status qattn_flashq_attend(const uint16_t *q, const qattn_flashq_buffer *buf, int32_t batch,
+                                 int32_t num_q_heads, float softmax_scale, uint16_t *out, float *lse,
+                                 qattn_stream_t stream) {
+  FlashqView fv;
+  qattn_status st = check_flashq(buf, batch, &fv);
+  if (st != QATTN_OK) return st;
+  if (num_q_heads <= 0 || num_q_heads % fv.hkv)
+    return fail(QATTN_ERR_INVALID_ARG, "Hq %d is not a positive multiple of Hkv %d", num_q_heads, fv.hkv);
+  if (num_q_heads / fv.hkv > QATTN_MAX_GROUP)
+    return fail(QATTN_ERR_UNSUPPORTED, "group size %d > %d", num_q_heads / fv.hkv, QATTN_MAX_GROUP);
+  if (batch == 0) return QATTN_OK;
+  if (!q || !out || !lse) return fail(QATTN_ERR_INVALID_ARG, "q, out or lse is NULL");
+  if (!aligned16(q) || !aligned16(out)) return fail(QATTN_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+  DeviceState *ds;
+  if ((st = device_state(&ds)) != QATTN_OK) return st;
+  cudaError_t e = launch_flashq_attend(q, fv, batch, num_q_heads, softmax_scale * 1.4426950408889634f, out, lse,
+                                       reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "flashq attend launch");
+}
+
+qattn_status qattn_flashq_flush(const qattn_flashq_buffer *buf, const qattn_kv_cache *cache,
+                                const int32_t *cache_lens, int32_t batch, qattn_stream_t stream) {
+  FlashqView fv;
+  KvView kv;
+  qattn_status st = check_flashq_cache(buf, cache, cache_lens, batch, &fv, &kv);
+  if (st != QATTN_OK || batch == 0) return st;
+  DeviceState *ds;
+  if ((st = device_state(&ds)) != QATTN_OK) return st;
+  cudaError_t e = launch_flashq_flush(fv, kv, cache_lens, batch, ds->status, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "flashq flush launch");
+}
+
 qattn_status qattn_prefill(const uint16_t *q, const qattn_kv_cache *cache, int32_t batch,
                            int32_t num_q_heads, int32_t nq, int32_t nk, float softmax_scale,
                            int32_t causal, uint16_t *out, float *lse, qattn_stream_t stream) {

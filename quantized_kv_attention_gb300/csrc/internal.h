@@ -63,6 +63,23 @@ DecodeGeometry decode_geometry(int head_dim, int hkv, bool paged, int warps);
 struct DecodeMaps {
   CUtensorMap k, v, ks, vs;  // codes 3-D [heads][rows][128 B], scales 2-D [heads][tokens]
 };
+// The decode buffer of qattn_flashq_* (see include/qattn.h).
+struct FlashqView {
+  int8_t *k_codes, *v_codes;    // [batch, Hkv, 64, D] int8 codes
+  uint16_t *k_scale, *v_scale;  // [batch, Hkv] fp16 universal scales
+  float *k_range, *v_range;     // [batch, Hkv] running max |x^| of the cached rows
+  int32_t *count;               // [batch] rows buffered
+  int hkv, head_dim;
+};
+cudaError_t launch_flashq_init(const FlashqView &f, const KvView &c, const int32_t *cache_lens, int batch,
+                               cudaStream_t stream);
+cudaError_t launch_flashq_append(const void *k, const void *v, bool fp16_in, const FlashqView &f, int batch,
+                                 uint32_t *err, cudaStream_t stream);
+cudaError_t launch_flashq_attend(const uint16_t *q, const FlashqView &f, int batch, int hq, float scale_log2,
+                                 uint16_t *out, float *lse, cudaStream_t stream);
+cudaError_t launch_flashq_flush(const FlashqView &f, const KvView &c, const int32_t *cache_lens, int batch,
+                                uint32_t *err, cudaStream_t stream);
+
 cudaError_t launch_decode(const DecodeArgs &a, const KvView &cache, const DecodeMaps &maps, uint32_t *err,
                           cudaStream_t stream);
 

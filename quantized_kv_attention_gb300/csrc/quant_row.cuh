@@ -61,16 +61,15 @@ __device__ __forceinline__ int code_of(float x, float s) {
   return x < 0.f ? -m : m;
 }
 
-// Quantizes row `src` (D values of type T) with the 32 lanes of a warp: lane
-// i covers elements 4i..4i+3 (D = 128) or 2i, 2i+1 (D = 64) and writes their
-// packed nibbles (low nibble = even element) to dst_codes + i * D / 64; lane
-// 0 writes the fp16 scale.  Every lane of the warp must call it.
-template <typename T, int D>
-__device__ __forceinline__ void quantize_row_warp(const T *src, uint8_t *dst_codes, uint16_t *dst_scale,
-                                                  int lane) {
+// Quantizes one row of D values held by the 32 lanes of a warp: lane i
+// holds elements 4i..4i+3 (D = 128) or 2i, 2i+1 (D = 64) in x and writes
+// their packed nibbles (low nibble = even element) to dst_codes + i * D / 64;
+// lane 0 writes the fp16 scale, which every lane gets back.  Every lane of
+// the warp must call it.
+template <int D>
+__device__ __forceinline__ __half quantize_vals_warp(const float (&x)[D / 32], uint8_t *dst_codes,
+                                                     uint16_t *dst_scale, int lane) {
   constexpr int VPL = D / 32;  // values per lane
-  float x[VPL];
-  RowLoad<T, VPL>::load(src + lane * VPL, x);
   float am = 0.f;
 #pragma unroll
   for (int j = 0; j < VPL; ++j) am = fmaxf(am, fabsf(x[j]));
@@ -92,6 +91,17 @@ __device__ __forceinline__ void quantize_row_warp(const T *src, uint8_t *dst_cod
   else
     *dst = static_cast<uint8_t>(packed);
   if (lane == 0) *dst_scale = __half_as_ushort(hs);
+  return hs;
+}
+
+// quantize_vals_warp of row `src` (D values of type T, lane i reading its
+// elements as above).
+template <typename T, int D>
+__device__ __forceinline__ void quantize_row_warp(const T *src, uint8_t *dst_codes, uint16_t *dst_scale,
+                                                  int lane) {
+  float x[D / 32];
+  RowLoad<T, D / 32>::load(src + lane * (D / 32), x);
+  quantize_vals_warp<D>(x, dst_codes, dst_scale, lane);
 }
 
 }  // namespace qattn

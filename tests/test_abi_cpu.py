@@ -137,3 +137,36 @@ def test_decode_append_rejects_bad_arguments():
     assert da(k=FAKE + 4) == qa.QATTN_ERR_INVALID_ARG   # misaligned
     assert da(v=FAKE + 8) == qa.QATTN_ERR_INVALID_ARG
     assert da(batch=0) == qa.QATTN_OK                   # nothing to do
+
+
+def _fq(**kw):
+    s = qa.FlashqBufferStruct()
+    s.k_codes = s.v_codes = s.k_scale = s.v_scale = s.k_range = s.v_range = s.count = FAKE
+    s.head_dim, s.num_kv_heads = 128, 2
+    for k, v in kw.items():
+        setattr(s, k, v)
+    return s
+
+
+def test_flashq_rejects_bad_arguments():
+    c = _cache()
+    init = lambda b, cache=c, batch=1: lib.qattn_flashq_init(ctypes.byref(b), ctypes.byref(cache), FAKE, batch, None)
+    assert lib.qattn_flashq_init(None, ctypes.byref(c), FAKE, 1, None) == qa.QATTN_ERR_INVALID_ARG
+    assert init(_fq(head_dim=96)) == qa.QATTN_ERR_UNSUPPORTED
+    assert init(_fq(num_kv_heads=0)) == qa.QATTN_ERR_INVALID_ARG
+    assert init(_fq(count=0)) == qa.QATTN_ERR_INVALID_ARG
+    assert init(_fq(k_codes=FAKE + 4)) == qa.QATTN_ERR_INVALID_ARG             # misaligned
+    assert init(_fq(num_kv_heads=4)) == qa.QATTN_ERR_INVALID_ARG               # cache has Hkv 2
+    assert init(_fq(head_dim=64)) == qa.QATTN_ERR_INVALID_ARG                  # cache has D 128
+    assert lib.qattn_flashq_init(ctypes.byref(_fq()), ctypes.byref(c), None, 1, None) == qa.QATTN_ERR_INVALID_ARG
+    assert init(_fq(), batch=0) == qa.QATTN_OK
+    b = _fq()
+    assert lib.qattn_flashq_append(FAKE, FAKE, 7, ctypes.byref(b), 1, None) == qa.QATTN_ERR_INVALID_ARG
+    assert lib.qattn_flashq_append(None, FAKE, 0, ctypes.byref(b), 1, None) == qa.QATTN_ERR_INVALID_ARG
+    assert lib.qattn_flashq_append(FAKE + 8, FAKE, 0, ctypes.byref(b), 1, None) == qa.QATTN_ERR_INVALID_ARG
+    att = lambda hq=4, lse=FAKE, batch=1: lib.qattn_flashq_attend(FAKE, ctypes.byref(b), batch, hq, 1.0, FAKE, lse, None)
+    assert att(lse=None) == qa.QATTN_ERR_INVALID_ARG                           # lse is required
+    assert att(hq=3) == qa.QATTN_ERR_INVALID_ARG
+    assert att(hq=2 * 9) == qa.QATTN_ERR_UNSUPPORTED                           # group of 9
+    assert att(batch=0) == qa.QATTN_OK
+    assert lib.qattn_flashq_flush(ctypes.byref(_fq(head_dim=64)), ctypes.byref(c), FAKE, 1, None) == qa.QATTN_ERR_INVALID_ARG
