@@ -442,6 +442,89 @@ def prefill_flops(B, Hq, Nq, Nk, D, causal=True):
     return 4.0 * D * B * Hq * pairs
 
 
+def run_decode_flashq(name, args, device, gpu_index, rank):
+    """A decode workload's shape with the decode buffer (qattn_flashq_*):
+    the INT4 cache holds Nk - 64 rows, and a cycle of 64 steps appends one
+    K/V row per (sequence, kv-head) into the int8 buffer, decodes over the
+    cached rows, merges the buffered rows in, and finally flushes the buffer
+    into the cache (every replay rewrites the same 64 cache rows, so replays
+    are identical).  Timed per step over whole cycles, CUDA graphs of the API
+    calls, rotating cache copies larger than 4x L2."""
+    import torch
+    import quantized_kv_attention_gb300 as qa
+    from quantized_kv_attention_gb300 import workloads as wl
+    cfg = dict(wl.WORKLOADS[name])
+    B, Hq, Hkv, D, Nk = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["Nk"]
+    splits = 152 if name == "long_decode" else 0
+    nb = qa.FLASHQ_ROWS
+    Lc = Nk - nb
+    seed = cfg["seed"] + 1000 * rank
+    scale = 1.0 / math.sqrt(D)
+    cached_bytes = B * Hkv * Lc * (D + 4)
+    buf_bytes = B * Hkv * (nb + 1) / 2 * (2 * D + 4)  # mean rows buffered at a step, int8 K and V
+    kv_bytes = cached_bytes + buf_bytes
+    copies = max(1, math.ceil(4 * _l2_bytes(torch, device) / cached_bytes))
+    caches, bufs = [], []
+    lens = torch.full((B,), Lc, dtype=torch.int32, device=device)
+    for r in range(copies):
+        c = qa.KvCache.contiguous(B, Hkv, Nk, D, device=device)
+        oc = wl.outlier_channels(cfg["seed"], Hkv, D, cfg["outliers"]) if cfg.get("outliers") else None
+        _fill_contiguous(qa, torch, c, B, Hkv, Lc, D, seed * 31 + r, device, oc, cfg.get("outlier_scale", 1.0))
+        f = qa.FlashqBuffer.create(B, Hkv, D, device=device)
+        qa.flashq_init(f, c, lens)
+        caches.append(c)
+        bufs.append(f)
+    torch.cuda.synchronize()
+    q = torch.randn(B, Hq, D, device=device).half()
+    new_k = torch.randn(B, Hkv, D, device=device)
+    new_v = torch.randn(B, Hkv, D, device=device)
+    out = torch.empty(B, Hq, D, dtype=torch.float16, device=device)
+    lse = torch.empty(B, Hq, dtype=torch.float32, device=device)
+    ws = torch.empty(max(qa.decode_workspace_size(B, Hq, Hkv, D, Lc, splits), 16), dtype=torch.uint8, device=device)
+
+    def cycle(r):
+        for _ in range(nb):
+            qa.flashq_append(new_k, new_v, bufs[r])
+            qa.decode(q, caches[r], lens, Lc, scale, splits, workspace=ws, out=out, lse=lse)
+            qa.flashq_attend(q, bufs[r], scale, out, lse)
+        qa.flashq_flush(bufs[r], caches[r], lens)
+
+    for r in range(copies):
+        cycle(r)
+    torch.cuda.synchronize()
+    g = _graph(torch, lambda: [cycle(r) for r in range(copies)])
+    reps = max(1, args.steps // (nb * copies))
+    sampler = ClockSampler(gpu_index)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with sampler:
+        g.replay()
+        torch.cuda.synchronize()
+        barrier()
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        barrier()
+    steps = reps * nb * copies
+    value, tmax, world = aggregate(kv_bytes * steps / 1e9, e0.elapsed_time(e1) / 1e3, device)
+    res = {
+        "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(tmax * 1e3 / steps, 5), "steps": steps,
+        "config": {"workload": f"{name}_flashq", "B": B, "Hq": Hq, "Hkv": Hkv, "D": D, "Nk": Nk,
+                   "cached_rows": Lc, "buffer_rows": nb, "seed": cfg["seed"], "softmax_scale": scale,
+                   "kv_bytes_per_step": int(kv_bytes),
+                   "l2": "rotating KV-cache copies totalling more than 4x L2",
+                   "step": "append one K/V row per sequence into the int8 buffer + split-KV decode over the "
+                           "cached rows + merge of the buffered rows; a flush into the INT4 cache every 64 steps"},
+        "setup": {"cache_copies": copies, "parallelism": f"replicas x{world}",
+                  "timing": "CUDA graphs of whole 64-step cycles of the API calls"},
+        "clocks": sampler.summary(),
+    }
+    del caches, bufs
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_prefill(name, args, device, gpu_index, rank, steps=None):
     import torch
     import quantized_kv_attention_gb300 as qa
@@ -661,6 +744,7 @@ def main(argv=None):
     if args.secondary and world == 1 and args.workload == "gqa_decode":
         res["secondary"] = {
             "long_decode": compact(run_decode("long_decode", args, device, gpu_index, rank)),
+            "long_decode_flashq": compact(run_decode_flashq("long_decode", args, device, gpu_index, rank)),
             "causal_prefill": compact(run_prefill("causal_prefill", args, device, gpu_index, rank,
                                                   steps=min(args.steps, 50))),
         }

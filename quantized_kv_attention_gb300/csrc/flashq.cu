@@ -165,15 +165,24 @@ __global__ void __launch_bounds__(256) flashq_attend_kernel(const uint16_t *__re
     reinterpret_cast<uint4 *>(&cv[0][0])[i] = reinterpret_cast<const uint4 *>(f.v_codes + bh * kNb * D)[i];
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < G * n; i += blockDim.x) {  // scores
-    const int g = i / n, t = i % n;
-    float acc = 0.f;
-#pragma unroll 8
-    for (int d = 0; d < D; ++d) acc = fmaf(qs[g][d], static_cast<float>(ck[t][d]), acc);
-    ps[g][t] = acc * uk * scale_log2;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  {  // scores: a warp per buffered row t, lane i over d = VPL i .. VPL i + VPL - 1, all G heads
+    constexpr int VPL = D / 32;
+    for (int t = warp; t < n; t += blockDim.x >> 5) {
+      float c[VPL];
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) c[j] = static_cast<float>(ck[t][VPL * lane + j]);
+      for (int g = 0; g < G; ++g) {
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) acc = fmaf(qs[g][VPL * lane + j], c[j], acc);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) ps[g][t] = acc * uk * scale_log2;
+      }
+    }
   }
   __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int g = warp; g < G; g += blockDim.x >> 5) {  // softmax of row g
     float m = -INFINITY;
     for (int t = lane; t < n; t += 32) m = fmaxf(m, ps[g][t]);
