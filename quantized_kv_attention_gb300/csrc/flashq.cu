@@ -142,78 +142,69 @@ __global__ void __launch_bounds__(1024) flashq_append_kernel(const T *__restrict
   if (threadIdx.x == 0) f.count[b] = slot + 1;
 }
 
-// Grid (batch * Hkv), 256 threads.  For the G query heads of kv-head h:
-// S = q . x~_K * scale (log2 units), p = 2^(S - m_b), O_b = sum p x~_V / l_b,
-// lse_b = (m_b + log2 l_b) ln 2; then merged with the (O_c, lse_c) already
-// in out / lse: L = log(e^lse_c + e^lse_b), O = e^(lse_c - L) O_c + e^(lse_b - L) O_b.
+// Grid (batch * Hq), 128 threads: one query row (sequence b, query head g of
+// kv-head h = g / G).  S_t = q . x~_K,t * scale (log2 units) over the n
+// buffered rows, p = 2^(S - m_b), O_b = sum p x~_V / l_b, lse_b =
+// (m_b + log2 l_b) ln 2; then merged with the (O_c, lse_c) already in out /
+// lse: L = log(e^lse_c + e^lse_b), O = e^(lse_c - L) O_c + e^(lse_b - L) O_b.
 template <int D>
-__global__ void __launch_bounds__(256) flashq_attend_kernel(const uint16_t *__restrict__ q, FlashqView f, int batch,
+__global__ void __launch_bounds__(128) flashq_attend_kernel(const uint16_t *__restrict__ q, FlashqView f, int batch,
                                                             int hq, float scale_log2, uint16_t *out, float *lse) {
-  const int bh = blockIdx.x, b = bh / f.hkv, h = bh % f.hkv, G = hq / f.hkv;
+  constexpr int VPL = D / 32;
+  const int64_t row = blockIdx.x;  // b * hq + query head
+  const int b = static_cast<int>(row / hq), G = hq / f.hkv;
+  const int64_t bh = static_cast<int64_t>(b) * f.hkv + static_cast<int>(row % hq) / G;
   const int n = min(f.count[b], kNb);
   if (n <= 0) return;
-  __shared__ float qs[QATTN_MAX_GROUP][D];
-  __shared__ float ps[QATTN_MAX_GROUP][kNb];
+  __shared__ float qs[D];
+  __shared__ float ps[kNb];
   __shared__ int8_t ck[kNb][D], cv[kNb][D];
-  __shared__ float mls[QATTN_MAX_GROUP][3];  // m_b, l_b, lse_c
+  __shared__ float mls[3];  // m_b, l_b, lse_c
   const float uk = __half2float(__ushort_as_half(f.k_scale[bh])), uv = __half2float(__ushort_as_half(f.v_scale[bh]));
-  const int64_t row0 = static_cast<int64_t>(b) * hq + static_cast<int64_t>(h) * G;  // first query row
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x)
-    qs[i / D][i % D] = __half2float(__ushort_as_half(q[row0 * D + i]));
+  for (int i = threadIdx.x; i < D; i += blockDim.x) qs[i] = __half2float(__ushort_as_half(q[row * D + i]));
   for (int i = threadIdx.x; i < n * D / 16; i += blockDim.x) {
     reinterpret_cast<uint4 *>(&ck[0][0])[i] = reinterpret_cast<const uint4 *>(f.k_codes + bh * kNb * D)[i];
     reinterpret_cast<uint4 *>(&cv[0][0])[i] = reinterpret_cast<const uint4 *>(f.v_codes + bh * kNb * D)[i];
   }
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  {  // scores: a warp per buffered row t, lane i over d = VPL i .. VPL i + VPL - 1, all G heads
-    constexpr int VPL = D / 32;
-    for (int t = warp; t < n; t += blockDim.x >> 5) {
-      float c[VPL];
+  for (int t = warp; t < n; t += blockDim.x >> 5) {  // scores: a warp per buffered row
+    float acc = 0.f;
 #pragma unroll
-      for (int j = 0; j < VPL; ++j) c[j] = static_cast<float>(ck[t][VPL * lane + j]);
-      for (int g = 0; g < G; ++g) {
-        float acc = 0.f;
+    for (int j = 0; j < VPL; ++j) acc = fmaf(qs[VPL * lane + j], static_cast<float>(ck[t][VPL * lane + j]), acc);
 #pragma unroll
-        for (int j = 0; j < VPL; ++j) acc = fmaf(qs[g][VPL * lane + j], c[j], acc);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) ps[g][t] = acc * uk * scale_log2;
-      }
-    }
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) ps[t] = acc * uk * scale_log2;
   }
   __syncthreads();
-  for (int g = warp; g < G; g += blockDim.x >> 5) {  // softmax of row g
+  if (warp == 0) {  // softmax of the row
     float m = -INFINITY;
-    for (int t = lane; t < n; t += 32) m = fmaxf(m, ps[g][t]);
+    for (int t = lane; t < n; t += 32) m = fmaxf(m, ps[t]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
     float l = 0.f;
     for (int t = lane; t < n; t += 32) {
-      const float p = exp2f(ps[g][t] - m);
-      ps[g][t] = p;
+      const float p = exp2f(ps[t] - m);
+      ps[t] = p;
       l += p;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-    if (lane == 0) mls[g][0] = m, mls[g][1] = l, mls[g][2] = lse[row0 + g];
+    if (lane == 0) mls[0] = m, mls[1] = l, mls[2] = lse[row];
   }
-  __syncthreads();  // lse_c of every row is read before any row's lse is written
-  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {  // O_b and the merge
-    const int g = i / D, d = i % D;
+  __syncthreads();  // lse_c is read before it is overwritten below
+  const float lse_b = (mls[0] + log2f(mls[1])) * 0.69314718055994531f, lse_c = mls[2];
+  const float mx = fmaxf(lse_c, lse_b);
+  const float wc = expf(lse_c - mx), wb = expf(lse_b - mx);  // e^-inf = 0 for an empty cache part
+  const float z = wc + wb;
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {  // O_b and the merge
     float acc = 0.f;
-    for (int t = 0; t < n; ++t) acc = fmaf(ps[g][t], static_cast<float>(cv[t][d]), acc);
-    const float ob = acc * uv / mls[g][1];
-    const float lse_b = (mls[g][0] + log2f(mls[g][1])) * 0.69314718055994531f;
-    const int64_t row = row0 + g;
-    const float lse_c = mls[g][2];
-    const float mx = fmaxf(lse_c, lse_b);
-    const float wc = expf(lse_c - mx), wb = expf(lse_b - mx);  // e^-inf = 0 for an empty cache part
-    const float z = wc + wb;
+    for (int t = 0; t < n; ++t) acc = fmaf(ps[t], static_cast<float>(cv[t][d]), acc);
+    const float ob = acc * uv / mls[1];
     const float oc = __half2float(__ushort_as_half(out[row * D + d]));
     out[row * D + d] = __half_as_ushort(__float2half_rn((wc * oc + wb * ob) / z));
-    if (d == 0) lse[row] = mx + logf(z);
   }
+  if (threadIdx.x == 0) lse[row] = mx + logf(z);
 }
 
 // Grid batch, 512 threads: a sequence whose buffer is full moves its 64 rows
@@ -292,10 +283,11 @@ cudaError_t launch_flashq_append(const void *k, const void *v, bool fp16_in, con
 cudaError_t launch_flashq_attend(const uint16_t *q, const FlashqView &f, int batch, int hq, float scale_log2,
                                  uint16_t *out, float *lse, cudaStream_t stream) {
   if (batch == 0) return cudaSuccess;
+  const unsigned rows = static_cast<unsigned>(batch) * static_cast<unsigned>(hq);
   if (f.head_dim == 128)
-    flashq_attend_kernel<128><<<batch * f.hkv, 256, 0, stream>>>(q, f, batch, hq, scale_log2, out, lse);
+    flashq_attend_kernel<128><<<rows, 128, 0, stream>>>(q, f, batch, hq, scale_log2, out, lse);
   else
-    flashq_attend_kernel<64><<<batch * f.hkv, 256, 0, stream>>>(q, f, batch, hq, scale_log2, out, lse);
+    flashq_attend_kernel<64><<<rows, 128, 0, stream>>>(q, f, batch, hq, scale_log2, out, lse);
   return cudaGetLastError();
 }
 

@@ -129,3 +129,8 @@ def test_flashq_full_buffer_is_flagged():
     qa.flashq_append(row, row, buf)
     assert qa.read_device_flags(clear=True) & qa.FLAG_BUFFER_FULL
     assert buf.count.item() == fq.NB
+
+
+def test_flashq_group_of_eight():
+    """G = 8, as in the long-context shape the bench times."""
+    _replay(53, 1, 16, 2, 128, 200, 66)
