@@ -219,9 +219,10 @@ def decode(q: torch.Tensor, cache: KvCache, seq_lens: torch.Tensor, max_seq_len:
         out = torch.empty_like(q)
     if lse is None and return_lse:
         lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
-    need = decode_workspace_size(B, Hq, cache.num_kv_heads, D, max_seq_len, num_splits)
-    if workspace is None and need:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if workspace is None:  # a given workspace is checked by the library itself
+        need = decode_workspace_size(B, Hq, cache.num_kv_heads, D, max_seq_len, num_splits)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     sl = seq_lens.to(device=q.device, dtype=torch.int32).contiguous()
     st = cache.struct()
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -248,9 +249,10 @@ def decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, cac
         out = torch.empty_like(q)
     if lse is None and return_lse:
         lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
-    need = decode_workspace_size(B, Hq, cache.num_kv_heads, D, max_seq_len, num_splits)
-    if workspace is None and need:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if workspace is None:  # a given workspace is checked by the library itself
+        need = decode_workspace_size(B, Hq, cache.num_kv_heads, D, max_seq_len, num_splits)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     sl = seq_lens.to(device=q.device, dtype=torch.int32).contiguous()
     st = cache.struct()
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
