@@ -109,6 +109,14 @@ typedef enum qattn_dtype {
  *                    must be a positive multiple of 64
  *   page_size        paged layout: must be QATTN_PAGE_SIZE
  *   num_pages        paged layout: pages in the pool
+ *   code_bits        0 or 4: the INT4 format above.  3: INT3 ([QCA] §3.3: ten
+ *                    3-bit values per little-endian 32-bit word, element j in
+ *                    word j / 10 at bits 3 (j % 10), two's complement, unused
+ *                    fields zero; 52 bytes per row at D = 128; scale
+ *                    fp16(fp32(absmax / 3)), codes clamp(RNE(x / s), -3, 3)).
+ *                    INT3 is supported by qattn_quantize_kv and qattn_decode
+ *                    for a contiguous cache with D = 128; other calls return
+ *                    QATTN_ERR_UNSUPPORTED for it.
  */
 typedef struct qattn_kv_cache {
   uint8_t *k_codes;
@@ -122,6 +130,7 @@ typedef struct qattn_kv_cache {
   int32_t page_size;
   int64_t capacity;
   int64_t num_pages;
+  int32_t code_bits;
 } qattn_kv_cache;
 
 /*

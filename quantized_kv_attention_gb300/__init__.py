@@ -64,6 +64,7 @@ class KvCacheStruct(ctypes.Structure):
         ("page_size", ctypes.c_int32),
         ("capacity", ctypes.c_int64),
         ("num_pages", ctypes.c_int64),
+        ("code_bits", ctypes.c_int32),
     ]
 
 
@@ -138,11 +139,13 @@ def _stream(device) -> ctypes.c_void_p:
 
 @dataclass
 class KvCache:
-    """Caller-owned INT4 KV cache (contiguous or paged) as torch tensors.
+    """Caller-owned INT4 (or INT3) KV cache (contiguous or paged) as torch tensors.
 
     contiguous: codes [B, Hkv, capacity, D/2] uint8, scales [B, Hkv, capacity] fp16
     paged:      codes [P, Hkv, 64, D/2] uint8, scales [P, Hkv, 64] fp16,
                 page_table [B, max_pages] int32 (-1 = no page)
+    code_bits = 3: INT3 rows of 13 little-endian 32-bit words (52 bytes) at D = 128,
+                contiguous only (codes [B, Hkv, capacity, 52] uint8)
     """
     k_codes: torch.Tensor
     k_scales: torch.Tensor
@@ -153,13 +156,16 @@ class KvCache:
     capacity: int = 0
     page_table: Optional[torch.Tensor] = None
     num_pages: int = 0
+    code_bits: int = 4
 
     @staticmethod
-    def contiguous(batch, num_kv_heads, capacity, head_dim, device="cuda"):
+    def contiguous(batch, num_kv_heads, capacity, head_dim, device="cuda", code_bits=4):
         cap = -(-capacity // PAGE_SIZE) * PAGE_SIZE
-        codes = lambda: torch.zeros(batch, num_kv_heads, cap, head_dim // 2, dtype=torch.uint8, device=device)
+        row = 4 * (-(-head_dim // 10)) if code_bits == 3 else head_dim // 2
+        codes = lambda: torch.zeros(batch, num_kv_heads, cap, row, dtype=torch.uint8, device=device)
         scales = lambda: torch.zeros(batch, num_kv_heads, cap, dtype=torch.float16, device=device)
-        return KvCache(codes(), scales(), codes(), scales(), head_dim, num_kv_heads, capacity=cap)
+        return KvCache(codes(), scales(), codes(), scales(), head_dim, num_kv_heads, capacity=cap,
+                       code_bits=code_bits)
 
     @staticmethod
     def paged(num_pages, num_kv_heads, head_dim, page_table, device="cuda"):
@@ -178,6 +184,7 @@ class KvCache:
         s.k_codes, s.k_scales = self.k_codes.data_ptr(), self.k_scales.data_ptr()
         s.v_codes, s.v_scales = self.v_codes.data_ptr(), self.v_scales.data_ptr()
         s.head_dim, s.num_kv_heads = self.head_dim, self.num_kv_heads
+        s.code_bits = self.code_bits
         if self.page_table is not None:
             s.page_table = self.page_table.data_ptr()
             s.max_pages_per_seq = self.page_table.shape[1]

@@ -114,7 +114,12 @@ qattn_status decode_maps(DecodeMaps *m, const KvView &v, int batch, int warps) {
   const DecodeGeometry geo = decode_geometry(v.head_dim, v.hkv, paged, warps);
   const uint64_t heads = paged ? static_cast<uint64_t>(v.num_pages) * v.hkv : static_cast<uint64_t>(batch) * v.hkv;
   const uint64_t tokens = paged ? kPage : static_cast<uint64_t>(v.capacity);
-  const uint64_t rows = tokens * v.head_dim / 256;
+  // code bytes per token: D/2 (INT4) or 52 (INT3, D = 128); INT3 stages are
+  // read with plain word loads, so their boxes are not swizzled
+  const uint64_t tok_bytes = v.bits == 3 ? 52 : static_cast<uint64_t>(v.head_dim / 2);
+  const uint64_t rows = tokens * tok_bytes / 128;
+  const cuuint32_t box_rows = v.bits == 3 ? static_cast<cuuint32_t>(geo.tokens_per_stage * tok_bytes / 128)
+                                          : static_cast<cuuint32_t>(geo.box_rows);
   if (heads > 0x7fffffffull || rows > 0x7fffffffull) return fail(QATTN_ERR_UNSUPPORTED, "cache too large");
   const void *bases[4] = {v.k_codes, v.v_codes, v.k_scales, v.v_scales};
   CUtensorMap *outs[4] = {&m->k, &m->v, &m->ks, &m->vs};
@@ -123,11 +128,11 @@ qattn_status decode_maps(DecodeMaps *m, const KvView &v, int batch, int warps) {
     if (i < 2) {
       cuuint64_t dims[3] = {128, rows, heads};
       cuuint64_t strides[2] = {128, rows * 128};
-      cuuint32_t box[3] = {128, static_cast<cuuint32_t>(geo.box_rows), static_cast<cuuint32_t>(geo.box_heads)};
+      cuuint32_t box[3] = {128, box_rows, static_cast<cuuint32_t>(geo.box_heads)};
       cuuint32_t es[3] = {1, 1, 1};
       r = enc(outs[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(bases[i]), dims, strides, box, es,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+              CU_TENSOR_MAP_INTERLEAVE_NONE, v.bits == 3 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     } else {
       cuuint64_t dims[2] = {tokens, heads};
       cuuint64_t strides[1] = {tokens * 2};
@@ -158,6 +163,12 @@ qattn_status check_cache(const qattn_kv_cache *c, int batch, KvView *v, uint64_t
   v->page_table = c->page_table;
   v->hkv = c->num_kv_heads;
   v->head_dim = c->head_dim;
+  if (c->code_bits != 0 && c->code_bits != 4 && c->code_bits != 3)
+    return fail(QATTN_ERR_INVALID_ARG, "code_bits %d (0 or 4: INT4, 3: INT3)", c->code_bits);
+  v->bits = c->code_bits == 3 ? 3 : 4;
+  if (v->bits == 3 && (c->page_table || c->head_dim != 128))
+    return fail(QATTN_ERR_UNSUPPORTED, "INT3 needs a contiguous cache with head_dim 128");
+  const uint64_t row_bytes = v->bits == 3 ? 52 : static_cast<uint64_t>(c->head_dim / 2);
   v->capacity = 0, v->num_pages = 0, v->max_pages = 0;
   if (c->page_table) {
     if (c->page_size != QATTN_PAGE_SIZE)
@@ -166,13 +177,13 @@ qattn_status check_cache(const qattn_kv_cache *c, int batch, KvView *v, uint64_t
       return fail(QATTN_ERR_INVALID_ARG, "paged cache needs num_pages > 0 and max_pages_per_seq > 0");
     v->num_pages = c->num_pages;
     v->max_pages = c->max_pages_per_seq;
-    *code_bytes = static_cast<uint64_t>(c->num_pages) * c->num_kv_heads * kPage * (c->head_dim / 2);
+    *code_bytes = static_cast<uint64_t>(c->num_pages) * c->num_kv_heads * kPage * row_bytes;
   } else {
     if (c->capacity <= 0 || c->capacity % kPage)
       return fail(QATTN_ERR_UNSUPPORTED, "capacity %lld must be a positive multiple of %d",
                   (long long)c->capacity, kPage);
     v->capacity = c->capacity;
-    *code_bytes = static_cast<uint64_t>(batch) * c->num_kv_heads * c->capacity * (c->head_dim / 2);
+    *code_bytes = static_cast<uint64_t>(batch) * c->num_kv_heads * c->capacity * row_bytes;
   }
   return QATTN_OK;
 }
@@ -291,6 +302,7 @@ qattn_status decode_impl(const uint16_t *q, const void *k_new, const void *v_new
   if (!q || !seq_lens || !out) return fail(QATTN_ERR_INVALID_ARG, "q, seq_lens or out is NULL");
   if (!aligned16(q) || !aligned16(out)) return fail(QATTN_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
   if ((k_new == nullptr) != (v_new == nullptr)) return fail(QATTN_ERR_INVALID_ARG, "k_new and v_new: both or neither");
+  if (view.bits == 3 && k_new) return fail(QATTN_ERR_UNSUPPORTED, "qattn_decode_append on an INT3 cache");
   if (k_new && (!aligned16(k_new) || !aligned16(v_new)))
     return fail(QATTN_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
   DeviceState *ds;
@@ -300,7 +312,8 @@ qattn_status decode_impl(const uint16_t *q, const void *k_new, const void *v_new
   if (static_cast<int64_t>(batch) * view.hkv * stage_limit >= (int64_t(1) << 31))
     return fail(QATTN_ERR_UNSUPPORTED, "batch * Hkv * cached stages exceeds 2^31");
   const bool paged = view.page_table != nullptr;
-  const int warps = decode_layout(batch, view.hkv, max_seq_len, paged, num_splits > 0 ? num_splits : ds->sms);
+  const int warps = view.bits == 3 ? 8 : decode_layout(batch, view.hkv, max_seq_len, paged,
+                                                        num_splits > 0 ? num_splits : ds->sms);
   const int ctas = plan_ctas(batch, view.hkv, view.head_dim, max_seq_len, num_splits, ds->sms, paged, warps);
   const DecodeGeometry geo = decode_geometry(view.head_dim, view.hkv, paged, warps);
   const int slot_rows = geo.heads_per_stage * G;
@@ -376,6 +389,7 @@ qattn_status check_flashq_cache(const qattn_flashq_buffer *b, const qattn_kv_cac
   if (st != QATTN_OK) return st;
   uint64_t code_bytes = 0;
   if ((st = check_cache(cache, batch, kv, &code_bytes)) != QATTN_OK) return st;
+  if (kv->bits == 3) return fail(QATTN_ERR_UNSUPPORTED, "the decode buffer on an INT3 cache");
   if (kv->head_dim != fv->head_dim || kv->hkv != fv->hkv)
     return fail(QATTN_ERR_INVALID_ARG, "buffer (D %d, Hkv %d) and cache (D %d, Hkv %d) differ", fv->head_dim,
                 fv->hkv, kv->head_dim, kv->hkv);
@@ -456,6 +470,7 @@ qattn_status qattn_prefill(const uint16_t *q, const qattn_kv_cache *cache, int32
   uint64_t code_bytes = 0;
   qattn_status st = check_cache(cache, batch, &view, &code_bytes);
   if (st != QATTN_OK) return st;
+  if (view.bits == 3) return fail(QATTN_ERR_UNSUPPORTED, "qattn_prefill on an INT3 cache");
 
   if (num_q_heads % view.hkv) return fail(QATTN_ERR_INVALID_ARG, "Hq %d is not a multiple of Hkv %d", num_q_heads, view.hkv);
   if (nq > nk) return fail(QATTN_ERR_INVALID_ARG, "nq %d > nk %d", nq, nk);

@@ -70,12 +70,18 @@ struct Layout {
   static constexpr int kRegsConsumer = 160, kRegsProducer = 32;
 };
 
-template <int D, int W>
+// BITS = 4: the INT4 rows (D/2 bytes); BITS = 3: INT3 rows of ten 3-bit
+// values per 32-bit word (D = 128: 13 words, 52 bytes), read unswizzled.
+template <int D, int W, int BITS = 4>
 struct Cfg {
   static constexpr int kRows = Layout<W>::kRows;
-  static constexpr int kCodeBytes = kRows * D / 2;  // per tensor per stage
+  static constexpr int kTokBytes = BITS == 3 ? 52 : D / 2;  // code bytes per (token, kv-head)
+  static constexpr int kCodeBytes = kRows * kTokBytes;      // per tensor per stage
   static constexpr int kScaleBytes = kRows * 2;
-  static constexpr int kStageBytes = (2 * kCodeBytes + 2 * kScaleBytes + 1023) / 1024 * 1024;
+  // the last stage of a segment also hosts the cross-warp merge area
+  static constexpr int kDataBytes = (2 * kCodeBytes + 2 * kScaleBytes + 1023) / 1024 * 1024;
+  static constexpr int kMergeBytes = (W * 8 * (D + 4) * 4 + 1023) / 1024 * 1024;
+  static constexpr int kStageBytes = kDataBytes > kMergeBytes ? kDataBytes : kMergeBytes;
   static constexpr int kStages = D == 128 ? (W == 8 ? 6 : 4) : (W == 8 ? 12 : 8);
   static constexpr int kQSlot = 4 * QATTN_MAX_GROUP * D * 2;  // Q rows of one segment (<= 4 kv-heads)
   // fp32 row pitch of the cross-warp merge area laid over the last stage's
@@ -88,14 +94,18 @@ struct Cfg {
   static constexpr int kKBytes = D / 8;  // K code bytes per lane per token
   static constexpr int kWords = kKBytes / 4;
   static constexpr int kMt = D / 16;     // m-tiles of O^T, k-steps of S
+  // INT3: k-steps of S (10 words' pairs per lane), m-tiles of O^T (5 pairs of
+  // each of a lane's 2 words)
+  static constexpr int kKs3 = 10, kMt3 = 10;
+  static constexpr int kOt = BITS == 3 ? kMt3 : kMt;
 };
 
 // Dynamic shared memory: ring | Q slot | m, l per (warp, q-head) | prefix |
 // lengths | barriers, flags.  The cross-warp merge reuses a ring slot.
-template <int D, int W>
+template <int D, int W, int BITS = 4>
 __host__ __device__ constexpr int smem_bytes(int batch) {
-  return Cfg<D, W>::kRing + Cfg<D, W>::kQSlot + 2 * W * 8 * 4 + (2 * batch + 1) * 4 +
-         (2 * Cfg<D, W>::kStages + 3) * 8 + Cfg<D, W>::kStages * 4 + 16 + 1024;
+  return Cfg<D, W, BITS>::kRing + Cfg<D, W, BITS>::kQSlot + 2 * W * 8 * 4 + (2 * batch + 1) * 4 +
+         (2 * Cfg<D, W, BITS>::kStages + 3) * 8 + Cfg<D, W, BITS>::kStages * 4 + 16 + 1024;
 }
 
 template <int W>
@@ -112,6 +122,21 @@ __device__ __forceinline__ void decode_sub(uint32_t w, uint32_t (&out)[4]) {
   out[1] = lop3_and_xor(w, 0x00F000F0u, 0x00800080u);
   out[2] = lop3_and_xor(w8, 0x000F000Fu, 0x00080008u);
   out[3] = lop3_and_xor(w8, 0x00F000F0u, 0x00800080u);
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
+// INT3 word -> one MMA register of fp16 subnormals: fields p and p + 5 (15
+// bits apart) land at bits 1..3 and 16..18, i.e. (2 u_p, u_{p+5}) * 2^-24
+// with u = code + 4 (the XOR flips each field's sign bit).  p is a constant
+// after unrolling.
+__device__ __forceinline__ uint32_t ext3(uint32_t w, int p) {
+  const uint32_t sh = p == 0 ? (w << 1) : (w >> (3 * p - 1));
+  return lop3_and_xor(sh, 0x0007000Eu, 0x00040008u);
 }
 
 __device__ __forceinline__ __half lds_f16(uint32_t addr) {
@@ -232,10 +257,10 @@ struct Maps {
   CUtensorMap k, v, ks, vs;
 };
 
-template <int D, int W>
+template <int D, int W, int BITS = 4>
 __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
     decode_kernel(DecodeArgs a, KvView cache, const __grid_constant__ Maps maps, uint32_t *err) {
-  using C = Cfg<D, W>;
+  using C = Cfg<D, W, BITS>;
   constexpr int kConsumerWarps = W;
   constexpr int kThreads = Layout<W>::kThreads;
   constexpr int kRowsPerStage = Layout<W>::kRows;
@@ -295,9 +320,9 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
         const int64_t head = (sg / geo.groups) * hkv + (sg % geo.groups) * geo.hb;
         const int64_t ntok = min(static_cast<int64_t>(geo.tokens), cache.capacity - tok0);
         const int64_t row = head * cache.capacity + tok0;
-        const uint32_t cb = static_cast<uint32_t>(ntok * (D / 2)), sb = static_cast<uint32_t>(ntok * 2);
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cache.k_codes + row * (D / 2)), "r"(cb) : "memory");
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cache.v_codes + row * (D / 2)), "r"(cb) : "memory");
+        const uint32_t cb = static_cast<uint32_t>(ntok * C::kTokBytes), sb = static_cast<uint32_t>(ntok * 2);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cache.k_codes + row * C::kTokBytes), "r"(cb) : "memory");
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cache.v_codes + row * C::kTokBytes), "r"(cb) : "memory");
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cache.k_scales + row), "r"(sb) : "memory");
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cache.v_scales + row), "r"(sb) : "memory");
       }
@@ -345,7 +370,7 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
     // thread of its first warp issues the loads)
     if constexpr (Layout<W>::kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Layout<W>::kRegsProducer));
     if (warp == kConsumerWarps && lane == 0) {
-      const int rows_per_tok = D / 2;  // code bytes per token
+      const int rows_per_tok = C::kTokBytes;  // code bytes per token
       const uint32_t qbytes = geo.hb * G * D * 2;
       int it = 0, seg = 0;
       bool rows_in = a.k_new == nullptr;  // the fused append's rows are in the cache
@@ -455,7 +480,7 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
   const int g = lane >> 2, c = lane & 3;
   const int hbw = warp / geo.wph;              // this warp's kv-head within the stage
   const int tok_w = (warp % geo.wph) * 32;     // its 32 tokens within that head's stage tokens
-  const int kofs = hbw * geo.tokens * (D / 2); // byte offset of the head's codes in a stage
+  const int kofs = hbw * geo.tokens * C::kTokBytes;  // byte offset of the head's codes in a stage
   const int sofs = hbw * geo.tokens;           // element offset of the head's scales
   const float kf = a.scale_log2 * kTwo24;      // folds the 2^-24 of the subnormal codes
   // Stage-relative swizzled offsets of this lane's K rows (tile t, rows g / g+8)
@@ -474,11 +499,11 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
       voff[t][jp] = swz128(kofs + vt * (D / 2) + (2 * jp + (q & 1)) * 16);
     }
   }
-  if (a.k_new) {
+  if (BITS == 4 && a.k_new) {
     // The fused append, while the producer fills the ring: the rows are
     // fenced to the async proxy, then released to the producer, which
     // loads no segment's last stage before this barrier completes.
-    append_rows<D>(a, cache, geo.hb, geo.groups, prefix, gs0, gs1, err, warp, lane, kConsumerWarps);
+    if constexpr (BITS == 4) append_rows<D>(a, cache, geo.hb, geo.groups, prefix, gs0, gs1, err, warp, lane, kConsumerWarps);
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(appended));
   }
@@ -495,9 +520,31 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
     // memory.  Lane c covers d = c*D/4 + 8i + {0..7} (word i of its K code
     // bytes); the decoder pairs (e, e+4), and nibble positions 1 and 3 come
     // out 16x larger, so those columns carry q / 16.
-    uint32_t qb[C::kMt][2];
+    uint32_t qb[BITS == 3 ? C::kKs3 : C::kMt][2];
     float qsum = 0.f;
-    {
+    if constexpr (BITS == 3) {
+      // INT3: register r of lane c takes field pair p = r % 5 of its word
+      // slot r / 5 (words c, c + 4, c + 8, and 12 for lane 0): d = 10 w + p
+      // (low half, which came out 2x larger: q / 2) and 10 w + p + 5
+      if (!mbar_wait(smem_u32(qfull), seg & 1, err, *abort_flag ? kDrainCycles : kWaitCycles))
+        *abort_flag = 1;
+      const uint32_t qrow = smem_u32(qslot) + (hbw * G + min(g, G - 1)) * D * 2;
+#pragma unroll
+      for (int r = 0; r < 2 * C::kKs3; ++r) {
+        const int jw = r / 5, p = r % 5;
+        const int w = jw < 3 ? c + 4 * jw : (c == 0 ? 12 : -1);
+        const int dlo = 10 * w + p, dhi = dlo + 5;
+        float qlo = 0.f, qhi = 0.f;
+        if (g < G && w >= 0) {
+          if (dlo < D) qlo = __half2float(lds_f16(qrow + 2 * dlo));
+          if (dhi < D) qhi = __half2float(lds_f16(qrow + 2 * dhi));
+        }
+        const __half2 h = __halves2half2(__float2half_rn(0.5f * qlo), __float2half_rn(qhi));
+        qb[r >> 1][r & 1] = *reinterpret_cast<const uint32_t *>(&h);
+        const float2 f = __half22float2(h);
+        qsum += 2.f * f.x + f.y;  // the bias uses exactly the values the MMA multiplies
+      }
+    } else {
       if (!mbar_wait(smem_u32(qfull), seg & 1, err, *abort_flag ? kDrainCycles : kWaitCycles))
         *abort_flag = 1;
       const int dbase = c * (D / 4);
@@ -525,14 +572,16 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
     if (lane == 0) mbar_arrive(smem_u32(qempty));  // Q now lives in registers
     qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
     qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
-    // raw-unit bias 8 * sum(q) * 2^-24 for the lane's q-heads 2c and 2c+1
-    const float bq0 = 8.f / kTwo24 * __shfl_sync(0xffffffffu, qsum, (2 * c) << 2);
-    const float bq1 = 8.f / kTwo24 * __shfl_sync(0xffffffffu, qsum, (2 * c + 1) << 2);
+    // raw-unit bias (code offset) * sum(q) * 2^-24 for the lane's q-heads 2c
+    // and 2c+1; the offset is 8 for INT4 codes, 4 for INT3
+    constexpr float kOff = BITS == 3 ? 4.f : 8.f;
+    const float bq0 = kOff / kTwo24 * __shfl_sync(0xffffffffu, qsum, (2 * c) << 2);
+    const float bq1 = kOff / kTwo24 * __shfl_sync(0xffffffffu, qsum, (2 * c + 1) << 2);
 
     float m0 = -1e30f, m1 = -1e30f, l0 = 0.f, l1 = 0.f, ps0 = 0.f, ps1 = 0.f;
-    float o[C::kMt][4];
+    float o[C::kOt][4];
 #pragma unroll
-    for (int mt = 0; mt < C::kMt; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    for (int mt = 0; mt < C::kOt; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
 
     int last = 0;  // slot of the segment's last stage: its buffer hosts the merge
     for (int j = 0; j < cnt; ++j) {
@@ -549,6 +598,37 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
         const uint32_t svs = sks + 2 * kRowsPerStage;
         // S^T of the warp's 32 tokens: two 16-token tiles, two accumulation
         // chains each (even / odd code words)
+        float sacc[2][4], so[2][4];
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sacc[t][e] = so[t][e] = 0.f;
+        if constexpr (BITS == 3) {
+          // words c, c + 4, c + 8 (and 12 for lane 0) of rows g and g + 8 of each tile
+          uint32_t kw3[2][2][4];
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t rb = kb + kofs + (tok_w + 16 * t + g + 8 * h) * C::kTokBytes + 4 * c;
+              kw3[t][h][0] = lds32(rb);
+              kw3[t][h][1] = lds32(rb + 16);
+              kw3[t][h][2] = lds32(rb + 32);
+              kw3[t][h][3] = c == 0 ? lds32(rb + 48) : 0u;
+            }
+#pragma unroll
+          for (int ks = 0; ks < C::kKs3; ++ks)
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              const int r0 = 2 * ks, r1 = 2 * ks + 1;
+              const uint32_t a0 = ext3(kw3[t][0][r0 / 5], r0 % 5), a1 = ext3(kw3[t][1][r0 / 5], r0 % 5);
+              const uint32_t a2 = ext3(kw3[t][0][r1 / 5], r1 % 5), a3 = ext3(kw3[t][1][r1 / 5], r1 % 5);
+              if (ks & 1)
+                mma_16816(so[t], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+              else
+                mma_16816(sacc[t], a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+            }
+        } else {
         uint32_t kw[2][2][C::kWords];
 #pragma unroll
         for (int t = 0; t < 2; ++t)
@@ -562,11 +642,6 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
               kw[t][h][0] = u.x, kw[t][h][1] = u.y;
             }
           }
-        float sacc[2][4], so[2][4];
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) sacc[t][e] = so[t][e] = 0.f;
 #pragma unroll
         for (int i = 0; i < C::kWords; ++i)
 #pragma unroll
@@ -582,6 +657,7 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
               mma_16816(sacc[t], x0[2], x1[2], x0[3], x1[3], qb[2 * i + 1][0], qb[2 * i + 1][1]);
             }
           }
+        }
         float ts[2][4], fv[2][2];
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
@@ -619,7 +695,7 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
           m0 = n0, m1 = n1;
           l0 *= al0, l1 *= al1, ps0 *= al0, ps1 *= al1;
 #pragma unroll
-          for (int mt = 0; mt < C::kMt; ++mt) {
+          for (int mt = 0; mt < C::kOt; ++mt) {
             o[mt][0] *= al0, o[mt][1] *= al1, o[mt][2] *= al0, o[mt][3] *= al1;
           }
         }
@@ -640,6 +716,34 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
           pb[t][1] = movmatrix_trans(r1);
         }
         // O^T += V codes^T . P'^T
+        if constexpr (BITS == 3) {
+          // lane g owns words g and g + 8 of the V rows: m-tile 5 jj + p, row
+          // g is d = 10 (g + 8 jj) + p (2x larger), row g + 8 is d + 5; the
+          // two tokens of each A register come from two words, paired by
+          // byte permutes of the two extractions
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            uint32_t vw[2][4];
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+              const int w = g + 8 * jj;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const int tk = tok_w + 16 * t + 2 * c + (k & 1) + (k & 2 ? 8 : 0);
+                vw[jj][k] = w < 13 ? lds32(vb + kofs + tk * C::kTokBytes + 4 * w) : 0u;
+              }
+            }
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj)
+#pragma unroll
+              for (int pp = 0; pp < 5; ++pp) {
+                const uint32_t y0 = ext3(vw[jj][0], pp), y1 = ext3(vw[jj][1], pp);
+                const uint32_t y2 = ext3(vw[jj][2], pp), y3 = ext3(vw[jj][3], pp);
+                mma_16816(o[5 * jj + pp], __byte_perm(y0, y1, 0x5410), __byte_perm(y0, y1, 0x7632),
+                          __byte_perm(y2, y3, 0x5410), __byte_perm(y2, y3, 0x7632), pb[t][0], pb[t][1]);
+              }
+          }
+        } else {
 #pragma unroll
         for (int t = 0; t < 2; ++t)
 #pragma unroll
@@ -655,6 +759,7 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
             for (int k = 0; k < 4; ++k)
               mma_16816(o[jp * 4 + k], d0[k], d1[k], d2[k], d3[k], pb[t][0], pb[t][1]);
           }
+        }
       }
       __syncwarp();
       if (j + 1 < cnt) {
@@ -677,6 +782,27 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
     }
     consumer_sync<W>();  // every warp has read its last stage
     float *mo = reinterpret_cast<float *>(smem + last * C::kStageBytes);
+    if constexpr (BITS == 3) {
+      // O^T m-tile 5 jj + p: row g holds d = 10 (g + 8 jj) + p (2x larger),
+      // row g + 8 holds d + 5; code offset 4; P' carried 2^-8
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const int w = g + 8 * jj;
+#pragma unroll
+        for (int pp = 0; pp < 5; ++pp) {
+          const int mt = 5 * jj + pp, dlo = 10 * w + pp, dhi = dlo + 5;
+          if (w < 13 && dlo < D) {
+            if (2 * c < G) mo[(warp * 8 + 2 * c) * C::kMergePitch + dlo] = (o[mt][0] * (kTwo24 / 2.f) - 4.f * ps0) * 256.f;
+            if (2 * c + 1 < G)
+              mo[(warp * 8 + 2 * c + 1) * C::kMergePitch + dlo] = (o[mt][1] * (kTwo24 / 2.f) - 4.f * ps1) * 256.f;
+          }
+          if (w < 13 && dhi < D) {
+            if (2 * c < G) mo[(warp * 8 + 2 * c) * C::kMergePitch + dhi] = (o[mt][2] * kTwo24 - 4.f * ps0) * 256.f;
+            if (2 * c + 1 < G) mo[(warp * 8 + 2 * c + 1) * C::kMergePitch + dhi] = (o[mt][3] * kTwo24 - 4.f * ps1) * 256.f;
+          }
+        }
+      }
+    } else {
     // O^T m-tile jp*4+k holds d = 64 jp + 4 g + k (rows g) and +32 (rows g+8);
     // nibble positions 1 and 3 (odd k) came out 16x larger; P' carried 2^-8.
 #pragma unroll
@@ -694,6 +820,7 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
       const int d = 32 * jq + 4 * g;
       if (2 * c < G) *reinterpret_cast<float4 *>(mo + (warp * 8 + 2 * c) * C::kMergePitch + d) = v0;
       if (2 * c + 1 < G) *reinterpret_cast<float4 *>(mo + (warp * 8 + 2 * c + 1) * C::kMergePitch + d) = v1;
+    }
     }
     if (g == 0) {
       smm[warp * 8 + 2 * c] = m0, smm[warp * 8 + 2 * c + 1] = m1;
@@ -878,13 +1005,13 @@ cudaLaunchAttribute pdl_attr() {
   return attr;
 }
 
-template <int D, int W>
+template <int D, int W, int BITS = 4>
 cudaError_t launch_d(const DecodeArgs &a, const KvView &cache, const DecodeMaps &dm, uint32_t *err,
                      cudaStream_t stream) {
   static bool configured = false;  // per-function attribute, set once per process
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         smem_bytes<D, W>(QATTN_MAX_BATCH));
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, W, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         smem_bytes<D, W, BITS>(QATTN_MAX_BATCH));
     if (e != cudaSuccess) return e;
     configured = true;
   }
@@ -897,11 +1024,11 @@ cudaError_t launch_d(const DecodeArgs &a, const KvView &cache, const DecodeMaps 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.ctas);
   cfg.blockDim = dim3(Layout<W>::kThreads);
-  cfg.dynamicSmemBytes = smem_bytes<D, W>(a.batch);
+  cfg.dynamicSmemBytes = smem_bytes<D, W, BITS>(a.batch);
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<D, W>, a, cache, maps, err);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<D, W, BITS>, a, cache, maps, err);
   if (e != cudaSuccess) return e;
   const int64_t limit = cache.page_table ? static_cast<int64_t>(cache.max_pages) * kPage : cache.capacity;
   cudaLaunchConfig_t mc = {};
@@ -942,6 +1069,7 @@ DecodeGeometry decode_geometry(int head_dim, int hkv, bool paged, int warps) {
 cudaError_t launch_decode(const DecodeArgs &a, const KvView &cache, const DecodeMaps &maps, uint32_t *err,
                           cudaStream_t stream) {
   if (a.batch == 0 || a.ctas <= 0) return cudaSuccess;
+  if (cache.bits == 3) return launch_d<128, 8, 3>(a, cache, maps, err, stream);  // contiguous, D = 128
   if (cache.page_table || a.warps == 8)
     return cache.head_dim == 128 ? launch_d<128, 8>(a, cache, maps, err, stream)
                                  : launch_d<64, 8>(a, cache, maps, err, stream);

@@ -19,6 +19,7 @@ struct KvView {
   int32_t max_pages;          // paged: page-table row length
   int32_t hkv;
   int32_t head_dim;
+  int32_t bits;               // 4 (INT4) or 3 (INT3: contiguous, D = 128)
 };
 
 constexpr int kPage = 64;  // tokens per page and per decode pipeline stage

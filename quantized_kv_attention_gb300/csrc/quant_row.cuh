@@ -104,4 +104,44 @@ __device__ __forceinline__ void quantize_row_warp(const T *src, uint8_t *dst_cod
   quantize_vals_warp<D>(x, dst_codes, dst_scale, lane);
 }
 
+// INT3 ("Quantized Cross-Attention ... In-SRAM Dequantization" §3.3: ten
+// 3-bit values per 32-bit word) of one D = 128 row: s = fp16(fp32(absmax /
+// 3)), code = clamp(RNE(x / s), -3, 3) decided against the exact half-way
+// points s/2, 3s/2, 5s/2; element j goes to word j / 10 at bits 3 (j % 10)
+// as a 3-bit two's-complement field.  Lane i holds elements 4i..4i+3; lanes
+// 0..12 each gather the ten codes of one word by shuffles and store it.
+__device__ __forceinline__ int code_of3(float x, float s) {
+  const float ax = fabsf(x);
+  const float h = 0.5f * s;
+  const int m = (ax > h) + (ax >= 3.f * h) + (ax > 5.f * h);
+  return x < 0.f ? -m : m;
+}
+
+template <typename T>
+__device__ __forceinline__ void quantize_row3_warp(const T *src, uint32_t *dst_words, uint16_t *dst_scale,
+                                                   int lane) {
+  float x[4];
+  RowLoad<T, 4>::load(src + lane * 4, x);
+  float am = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+  __half hs = __float2half_rn(__fdiv_rn(am, 3.0f));
+  if (__hisinf(hs)) hs = __ushort_as_half(0x7BFF);
+  const float s = __half2float(hs);
+  uint32_t bytes = 0;  // the lane's four 3-bit fields, one per byte
+  if (s > 0.f) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) bytes |= (static_cast<uint32_t>(code_of3(x[j], s)) & 7u) << (8 * j);
+  }
+  uint32_t word = 0;
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    const int e = 10 * lane + i;  // element of this lane's word (lanes 0..12 only)
+    const uint32_t v = __shfl_sync(0xffffffffu, bytes, (e >> 2) & 31);
+    if (e < 128) word |= ((v >> (8 * (e & 3))) & 7u) << (3 * i);
+  }
+  if (lane < 13) dst_words[lane] = word;
+  if (lane == 0) *dst_scale = __half_as_ushort(hs);
+}
+
 }  // namespace qattn

@@ -45,6 +45,12 @@ __global__ void __launch_bounds__(256)
 
   uint8_t *codes = is_v ? cache.v_codes : cache.k_codes;
   uint16_t *scales = is_v ? cache.v_scales : cache.k_scales;
+  if constexpr (D == 128) {
+    if (cache.bits == 3) {  // 13 words per row
+      quantize_row3_warp<T>(src, reinterpret_cast<uint32_t *>(codes + dst_row * 52), scales + dst_row, lane);
+      return;
+    }
+  }
   quantize_row_warp<T, D>(src, codes + dst_row * (D / 2), scales + dst_row, lane);
 }
 

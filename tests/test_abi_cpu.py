@@ -170,3 +170,15 @@ def test_flashq_rejects_bad_arguments():
     assert att(hq=2 * 9) == qa.QATTN_ERR_UNSUPPORTED                           # group of 9
     assert att(batch=0) == qa.QATTN_OK
     assert lib.qattn_flashq_flush(ctypes.byref(_fq(head_dim=64)), ctypes.byref(c), FAKE, 1, None) == qa.QATTN_ERR_INVALID_ARG
+
+
+def test_int3_cache_checks():
+    assert _decode(_cache(code_bits=5)) == qa.QATTN_ERR_INVALID_ARG
+    assert _decode(_cache(code_bits=3, head_dim=64)) == qa.QATTN_ERR_UNSUPPORTED
+    paged3 = _cache(code_bits=3, page_table=FAKE, page_size=64, num_pages=4, max_pages_per_seq=2)
+    assert _decode(paged3) == qa.QATTN_ERR_UNSUPPORTED
+    c3 = _cache(code_bits=3)
+    assert lib.qattn_prefill(FAKE, ctypes.byref(c3), 1, 4, 8, 8, 1.0, 1, FAKE, None, None) == qa.QATTN_ERR_UNSUPPORTED
+    assert lib.qattn_decode_append(FAKE, FAKE, FAKE, qa.QATTN_F32, ctypes.byref(c3), FAKE, 1, 4, 100, 1.0, 0, None, 0,
+                                   FAKE, None, None) == qa.QATTN_ERR_UNSUPPORTED
+    assert lib.qattn_flashq_init(ctypes.byref(_fq()), ctypes.byref(c3), FAKE, 1, None) == qa.QATTN_ERR_UNSUPPORTED
