@@ -442,6 +442,84 @@ def prefill_flops(B, Hq, Nq, Nk, D, causal=True):
     return 4.0 * D * B * Hq * pairs
 
 
+def run_decode_int3(name, args, device, gpu_index, rank):
+    """A contiguous decode workload's shape with an INT3 cache (ten 3-bit
+    values per 32-bit word, 52 + 52 + 2 + 2 bytes per (token, kv-head) at
+    D = 128).  A step appends one K/V row per sequence (qattn_quantize_kv at
+    position seq_lens[b] - 1) and runs one qattn_decode; CUDA graphs of the
+    API calls, rotating cache copies larger than 4x L2; the roofline times the
+    decode call alone."""
+    import torch
+    import quantized_kv_attention_gb300 as qa
+    from quantized_kv_attention_gb300 import workloads as wl
+    cfg = dict(wl.WORKLOADS[name])
+    B, Hq, Hkv, D, Nk = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["Nk"]
+    splits = 152 if name == "long_decode" else 0
+    seed = cfg["seed"] + 1000 * rank
+    scale = 1.0 / math.sqrt(D)
+    row_bytes = 2 * 52 + 4
+    kv_bytes = B * Hkv * Nk * row_bytes
+    copies = max(1, math.ceil(4 * _l2_bytes(torch, device) / kv_bytes))
+    caches = []
+    g = torch.Generator(device=device)
+    for r in range(copies):
+        c = qa.KvCache.contiguous(B, Hkv, Nk, D, device=device, code_bits=3)
+        g.manual_seed(seed * 31 + r)
+        for b in range(B):
+            sub = qa.KvCache(c.k_codes[b:b + 1], c.k_scales[b:b + 1], c.v_codes[b:b + 1], c.v_scales[b:b + 1], D,
+                             Hkv, capacity=c.capacity, code_bits=3)
+            qa.quantize_kv(torch.randn(1, Hkv, Nk, D, device=device, generator=g),
+                           torch.randn(1, Hkv, Nk, D, device=device, generator=g), sub)
+        caches.append(c)
+    torch.cuda.synchronize()
+    sl = torch.full((B,), Nk, dtype=torch.int32, device=device)
+    start_pos = sl - 1
+    q = torch.randn(B, Hq, D, device=device).half()
+    new_k = torch.randn(B, Hkv, 1, D, device=device)
+    new_v = torch.randn(B, Hkv, 1, D, device=device)
+    out = torch.empty(B, Hq, D, dtype=torch.float16, device=device)
+    ws = torch.empty(max(qa.decode_workspace_size(B, Hq, Hkv, D, Nk, splits), 16), dtype=torch.uint8, device=device)
+
+    def attend(r):
+        qa.decode(q, caches[r], sl, Nk, scale, splits, workspace=ws, out=out)
+
+    def enqueue_steps(n):
+        for i in range(n):
+            qa.quantize_kv(new_k, new_v, caches[i % copies], start_pos)
+            attend(i % copies)
+
+    def enqueue_inner(n):
+        for i in range(n):
+            attend(i % copies)
+
+    enqueue_steps(max(args.warmup, 1))
+    torch.cuda.synchronize()
+    inner_count = max(copies, 64 // copies * copies)
+    total_ms, dec_ms, clocks = _timed_graphs(torch, args.steps, enqueue_steps, enqueue_inner, inner_count,
+                                             gpu_index, period=copies, soak_s=args.soak)
+    value, tmax, world = aggregate(kv_bytes * args.steps / 1e9, total_ms / 1e3, device)
+    peaks, pk_src = measured_peaks()
+    achieved = kv_bytes / (dec_ms / 1e3) / 1e9
+    res = {
+        "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(tmax * 1e3 / args.steps, 5),
+        "steps": args.steps,
+        "config": {"workload": f"{name}_int3", "B": B, "Hq": Hq, "Hkv": Hkv, "D": D, "Nk": Nk, "code_bits": 3,
+                   "splits": splits, "seed": cfg["seed"], "softmax_scale": scale, "kv_bytes_per_step": kv_bytes,
+                   "l2": "rotating KV-cache copies totalling more than 4x L2",
+                   "step": "append one K/V row per sequence (INT3 quantize) + split-KV decode + combine"},
+        "setup": {"cache_copies": copies, "parallelism": f"replicas x{world}",
+                  "timing": "CUDA graphs of the API calls"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "kernel": "decode+combine (one qattn_decode call, INT3 cache)", "peak_source": pk_src,
+                     "us_per_launch": round(dec_ms * 1e3, 3)},
+        "clocks": clocks,
+    }
+    del caches
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_decode_flashq(name, args, device, gpu_index, rank):
     """A decode workload's shape with the decode buffer (qattn_flashq_*):
     the INT4 cache holds Nk - 64 rows, and a cycle of 64 steps appends one
@@ -745,6 +823,7 @@ def main(argv=None):
         res["secondary"] = {
             "long_decode": compact(run_decode("long_decode", args, device, gpu_index, rank)),
             "long_decode_flashq": compact(run_decode_flashq("long_decode", args, device, gpu_index, rank)),
+            "long_decode_int3": compact(run_decode_int3("long_decode", args, device, gpu_index, rank)),
             "causal_prefill": compact(run_prefill("causal_prefill", args, device, gpu_index, rank,
                                                   steps=min(args.steps, 50))),
         }
