@@ -50,6 +50,7 @@ def test_int3_append_is_bit_exact(dt):
     (2, 4, 4, [129, 300], 2, 1 / math.sqrt(128)),        # G = 1
     (2, 12, 4, [300, 200], 2, 0.1),                      # G = 3
     (1, 64, 8, [4096], 64, 1 / math.sqrt(128)),          # long-context shape, many splits
+    (2, 16, 2, [20000, 9001], 4, 1 / math.sqrt(128)),    # long ranges, few splits
 ])
 def test_int3_decode(case):
     qa = require_gpu()
