@@ -907,6 +907,10 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4)
   const int b = blockIdx.x / geo.groups, hg = blockIdx.x % geo.groups;
   const int r = blockIdx.y;  // row within the segment: kv-head r / G, q-head r % G
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // A programmatic dependent (the next decode on the stream) may be scheduled
+  // now: it writes nothing before its own wait, which ends only once this
+  // grid has completed, so its set-up and L2 prefetch overlap this merge.
+  pdl_launch_dependents();
   // The decode kernel triggers this launch only after its own wait on the
   // inputs, so the lengths are final here; its partials are read after pdl_wait.
   auto stages = [&](int bb) {

@@ -44,6 +44,7 @@ def _run_contiguous(seed, B, Hq, Hkv, D, lens, splits, scale, outliers=False):
     (2, 4, 4, 64, [129, 65], 3, 1 / 8),                   # G = 1, D = 64
     (2, 12, 4, 128, [300, 200], 2, 0.1),                  # G = 3
     (1, 64, 8, 128, [4096], 64, 1 / math.sqrt(128)),      # long-context shape, many splits
+    (1, 8, 1, 128, [40000], 64, 1.0),                     # one segment over 64 splits: two merge batches
     # long ranges (>= 12 stages of 384 tokens per range): the 12-warp layout
     (3, 16, 4, 128, [20000, 0, 9001], 4, 1 / math.sqrt(128)),
     (2, 8, 2, 64, [16000, 15999], 2, 1 / 8),
