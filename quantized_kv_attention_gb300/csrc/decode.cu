@@ -101,10 +101,11 @@ struct Cfg {
 };
 
 // Dynamic shared memory: ring | Q slot | m, l per (warp, q-head) | prefix |
-// lengths | barriers, flags.  The cross-warp merge reuses a ring slot.
+// lengths | non-empty prefix | barriers, flags.  The cross-warp merge reuses a
+// ring slot.
 template <int D, int W, int BITS = 4>
 __host__ __device__ constexpr int smem_bytes(int batch) {
-  return Cfg<D, W, BITS>::kRing + Cfg<D, W, BITS>::kQSlot + 2 * W * 8 * 4 + (2 * batch + 1) * 4 +
+  return Cfg<D, W, BITS>::kRing + Cfg<D, W, BITS>::kQSlot + 2 * W * 8 * 4 + (3 * batch + 2) * 4 +
          (2 * Cfg<D, W, BITS>::kStages + 3) * 8 + Cfg<D, W, BITS>::kStages * 4 + 16 + 1024;
 }
 
@@ -145,13 +146,49 @@ __device__ __forceinline__ __half lds_f16(uint32_t addr) {
   return __ushort_as_half(v);
 }
 
-// Range of the flattened stage list owned by CTA i of n: [i*T/n, (i+1)*T/n).
-__host__ __device__ __forceinline__ int64_t range_start(int64_t i, int64_t T, int64_t n) {
-  return i * T / n;
+// Cost-balanced ranges of the flattened stage list.  A stage costs kUnit;
+// the first stage of each segment (sequence, head group) costs kSegCost<W>
+// more, for the segment's own fixed work (its Q rows, the cross-warp merge,
+// the partial or output write), so a range that a segment boundary cuts gets
+// fewer stages.  With C(gs) the summed cost of the stages before gs and
+// Wc = C(T), CTA i of n owns the stages with t_i <= C(gs) < t_{i+1},
+// t_i = floor(i * Wc / n); a range may be empty.
+constexpr int64_t kUnit = 16;
+template <int W>
+constexpr int64_t kSegCost = W == 12 ? 14 : 12;
+
+__host__ __device__ __forceinline__ int64_t cost_target(int64_t i, int64_t Wc, int64_t n) {
+  return i * Wc / n;
 }
-// CTA owning global stage gs (inverse of range_start).
-__host__ __device__ __forceinline__ int64_t owner_cta(int64_t gs, int64_t T, int64_t n) {
-  return ((gs + 1) * n + T - 1) / T - 1;
+// CTA owning the stage whose cost offset is x: the largest i with t_i <= x.
+__host__ __device__ __forceinline__ int64_t cost_owner(int64_t x, int64_t Wc, int64_t n) {
+  const int64_t i = ((x + 1) * n + Wc - 1) / Wc - 1;
+  return i < n - 1 ? i : n - 1;
+}
+// Inside a segment the cost offset of stage g is 0 (g = 0), else sc + kUnit*g:
+// the first stage g whose offset reaches rr.
+__host__ __device__ __forceinline__ int64_t stage_at(int64_t rr, int64_t sc) {
+  if (rr <= 0) return 0;
+  if (rr <= sc + kUnit) return 1;
+  return (rr - sc + kUnit - 1) / kUnit;
+}
+// First stage of CTA i: prefix[b] = groups * (stages of sequences before b),
+// nzp[b] = non-empty sequences before b, so the cost before sequence b is
+// kUnit * prefix[b] + sc * groups * nzp[b].
+__device__ __forceinline__ int64_t cost_start(int64_t i, int64_t n, int64_t Wc, const int *prefix, const int *nzp,
+                                              int batch, int groups, int64_t sc) {
+  const int64_t t = cost_target(i, Wc, n);
+  if (t >= Wc) return prefix[batch];
+  auto P = [&](int b) { return kUnit * prefix[b] + sc * groups * nzp[b]; };
+  int lo = 0, hi = batch - 1;  // largest b with P(b) <= t: always a non-empty sequence
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (P(mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  const int64_t nb = (prefix[lo + 1] - prefix[lo]) / groups;
+  const int64_t L = sc + kUnit * nb;  // cost of one segment of sequence lo
+  const int64_t r = t - P(lo), h = r / L;
+  return prefix[lo] + h * nb + stage_at(r - h * L, sc);
 }
 
 struct Loc {
@@ -275,8 +312,9 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
   float *sml = smm + kConsumerWarps * 8;                              // [warp][8]
   int *prefix = reinterpret_cast<int *>(sml + kConsumerWarps * 8);    // [B + 1]
   int *lens = prefix + B + 1;                                         // [B], clamped
+  int *nzp = lens + B;                                                // [B + 1], non-empty sequences before b
   uint64_t *full = reinterpret_cast<uint64_t *>(
-      (reinterpret_cast<uintptr_t>(lens + B) + 7) & ~static_cast<uintptr_t>(7));
+      (reinterpret_cast<uintptr_t>(nzp + B + 1) + 7) & ~static_cast<uintptr_t>(7));
   uint64_t *empty = full + C::kStages;
   uint64_t *qfull = empty + C::kStages;
   uint64_t *qempty = qfull + 1;
@@ -311,9 +349,14 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
   // the cache (capacity), so a wrong guess only costs bandwidth.
   if (!paged && threadIdx.x == kConsumerWarps * 32 + 1) {
     const int64_t per = (static_cast<int64_t>(min(a.max_len, static_cast<int>(cache.capacity))) + geo.tokens - 1) / geo.tokens;
-    const int64_t Tg = static_cast<int64_t>(B) * geo.groups * per;
     if (per > 0) {
-      const int64_t g0 = range_start(blockIdx.x, Tg, gridDim.x), g1 = range_start(blockIdx.x + 1, Tg, gridDim.x);
+      // the cost-balanced ranges of B * groups segments of `per` stages
+      const int64_t sc = kSegCost<W>, L = sc + kUnit * per, Wg = static_cast<int64_t>(B) * geo.groups * L;
+      auto start = [&](int64_t i) {
+        const int64_t t = cost_target(i, Wg, gridDim.x), sg = t / L;
+        return t >= Wg ? static_cast<int64_t>(B) * geo.groups * per : sg * per + stage_at(t - sg * L, sc);
+      };
+      const int64_t g0 = start(blockIdx.x), g1 = start(blockIdx.x + 1);
       for (int k = 0; k < 2 && g0 + k < g1; ++k) {
         const int64_t gs = g0 + k, sg = gs / per;
         const int64_t tok0 = (gs - sg * per) * geo.tokens;
@@ -341,27 +384,33 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
     if (len < 0) len = 0;
     lens[b] = len;
     prefix[b + 1] = len > 0 ? geo.groups * ((len + geo.tokens - 1) / geo.tokens) : 0;
+    nzp[b + 1] = len > 0;
   }
   __syncthreads();
   if (warp == 0) {
-    int carry = 0;
+    int carry = 0, carry_nz = 0;
     for (int base = 0; base < B; base += 32) {
       int v = base + lane < B ? prefix[base + lane + 1] : 0;
+      int vn = base + lane < B ? nzp[base + lane + 1] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int u = __shfl_up_sync(0xffffffffu, v, o);
-        if (lane >= o) v += u;
+        const int un = __shfl_up_sync(0xffffffffu, vn, o);
+        if (lane >= o) v += u, vn += un;
       }
-      if (base + lane < B) prefix[base + lane + 1] = carry + v;
+      if (base + lane < B) prefix[base + lane + 1] = carry + v, nzp[base + lane + 1] = carry_nz + vn;
       carry += __shfl_sync(0xffffffffu, v, 31);
+      carry_nz += __shfl_sync(0xffffffffu, vn, 31);
     }
-    if (lane == 0) prefix[0] = 0;
+    if (lane == 0) prefix[0] = 0, nzp[0] = 0;
   }
   __syncthreads();
 
   const int64_t T = prefix[B];
-  const int64_t gs0 = range_start(blockIdx.x, T, gridDim.x);
-  const int64_t gs1 = range_start(blockIdx.x + 1, T, gridDim.x);
+  const int64_t sc = kSegCost<W>;
+  const int64_t Wc = kUnit * T + sc * geo.groups * nzp[B];
+  const int64_t gs0 = cost_start(blockIdx.x, gridDim.x, Wc, prefix, nzp, B, geo.groups, sc);
+  const int64_t gs1 = cost_start(blockIdx.x + 1, gridDim.x, Wc, prefix, nzp, B, geo.groups, sc);
   if (gs1 <= gs0) return;
 
   if (warp >= kConsumerWarps) {
@@ -902,7 +951,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4)
   constexpr int VPL = D / 32;
   __shared__ float accs[kMergeWarps][D];
   __shared__ float wm[kMergeWarps], wz[kMergeWarps];
-  __shared__ int redi[2][kMergeWarps];
+  __shared__ int redi[4][kMergeWarps];
   const StageGeo geo = stage_geo<W>(hkv, paged != 0);
   const int b = blockIdx.x / geo.groups, hg = blockIdx.x % geo.groups;
   const int r = blockIdx.y;  // row within the segment: kv-head r / G, q-head r % G
@@ -917,21 +966,24 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4)
     const int64_t len = min(static_cast<int64_t>(__ldg(seq_lens + bb)), limit);
     return len > 0 ? static_cast<int>((len + geo.tokens - 1) / geo.tokens) : 0;
   };
-  int tot = 0, pre = 0;
+  // stages and non-empty sequences: in all, and before sequence b
+  int tot = 0, pre = 0, nzt = 0, nzb = 0;
   for (int bb = threadIdx.x; bb < batch; bb += kMergeWarps * 32) {
     const int n = stages(bb);
-    tot += n;
-    if (bb < b) pre += n;
+    tot += n, nzt += n > 0;
+    if (bb < b) pre += n, nzb += n > 0;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     tot += __shfl_xor_sync(0xffffffffu, tot, o);
     pre += __shfl_xor_sync(0xffffffffu, pre, o);
+    nzt += __shfl_xor_sync(0xffffffffu, nzt, o);
+    nzb += __shfl_xor_sync(0xffffffffu, nzb, o);
   }
-  if (lane == 0) redi[0][warp] = tot, redi[1][warp] = pre;
+  if (lane == 0) redi[0][warp] = tot, redi[1][warp] = pre, redi[2][warp] = nzt, redi[3][warp] = nzb;
   __syncthreads();
-  tot = pre = 0;
-  for (int w = 0; w < kMergeWarps; ++w) tot += redi[0][w], pre += redi[1][w];
+  tot = pre = nzt = nzb = 0;
+  for (int w = 0; w < kMergeWarps; ++w) tot += redi[0][w], pre += redi[1][w], nzt += redi[2][w], nzb += redi[3][w];
   const int rows = geo.hb * G;
   const int64_t row = static_cast<int64_t>(b) * hkv * G + static_cast<int64_t>(hg) * rows + r;
   const int n = stages(b);
@@ -941,9 +993,14 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4)
     if (threadIdx.x == 0 && lse) lse[row] = -INFINITY;
     return;
   }
-  const int64_t T = static_cast<int64_t>(geo.groups) * tot;
+  // the decode kernel's cost-balanced ranges: cost offsets of the segment's
+  // first and last stages
+  const int64_t sc = kSegCost<W>;
+  const int64_t Wc = kUnit * geo.groups * tot + sc * geo.groups * nzt;
   const int64_t first = static_cast<int64_t>(geo.groups) * pre + static_cast<int64_t>(hg) * n;
-  const int64_t c0 = owner_cta(first, T, ctas), c1 = owner_cta(first + n - 1, T, ctas);
+  const int64_t cf = kUnit * geo.groups * pre + sc * geo.groups * nzb + hg * (sc + kUnit * n);
+  const int64_t cl = n > 1 ? cf + sc + kUnit * (n - 1) : cf;
+  const int64_t c0 = cost_owner(cf, Wc, ctas), c1 = cost_owner(cl, Wc, ctas);
   if (c0 == c1) return;  // finished inside one CTA
   const int np = static_cast<int>(c1 - c0 + 1);
   pdl_wait();
@@ -952,15 +1009,18 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4)
   for (int j = 0; j < VPL; ++j) acc[j] = 0.f;
   // A warp folds partials k = warp, warp + 8, ... in batches of 4 whose loads
   // are all issued before any is used.  Empty ranges (two 64-bit divisions
-  // to detect) exist only when there are fewer stages than CTAs.
-  const bool may_be_empty = T < ctas;
+  // to detect) exist only when a CTA's share of the cost is below that of a
+  // segment's first stage; the starts of CTAs c0 < c <= c1 + 1 are found
+  // from the segment's own cost offsets.
+  const bool may_be_empty = Wc < (kUnit + sc) * ctas;
+  auto start_in = [&](int64_t c) { return first + stage_at(cost_target(c, Wc, ctas) - cf, sc); };
   for (int k0 = warp; k0 < np; k0 += 4 * kMergeWarps) {
     float lv[4], x[4][VPL];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int k = k0 + i * kMergeWarps;
       const int64_t c = c0 + k;
-      const bool ok = k < np && (k == 0 || !may_be_empty || range_start(c, T, ctas) != range_start(c + 1, T, ctas));
+      const bool ok = k < np && (k == 0 || !may_be_empty || start_in(c) != start_in(c + 1));
       const int64_t slot = k == 0 ? 2 * c0 + 1 : 2 * c;
       lv[i] = ok ? pl[slot * rows + r] : -INFINITY;
       const float *src = po + (slot * rows + r) * D + lane * VPL;
