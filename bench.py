@@ -442,10 +442,11 @@ def prefill_flops(B, Hq, Nq, Nk, D, causal=True):
     return 4.0 * D * B * Hq * pairs
 
 
-def run_decode_int3(name, args, device, gpu_index, rank):
+def run_decode_lowbit(name, args, device, gpu_index, rank, bits=3):
     """A contiguous decode workload's shape with an INT3 cache (ten 3-bit
     values per 32-bit word, 52 + 52 + 2 + 2 bytes per (token, kv-head) at
-    D = 128).  A step appends one K/V row per sequence (qattn_quantize_kv at
+    D = 128) or an INT2 cache (sixteen 2-bit values per word, 32 + 32 + 2 + 2
+    bytes).  A step appends one K/V row per sequence (qattn_quantize_kv at
     position seq_lens[b] - 1) and runs one qattn_decode; CUDA graphs of the
     API calls, rotating cache copies larger than 4x L2; the roofline times the
     decode call alone."""
@@ -457,17 +458,18 @@ def run_decode_int3(name, args, device, gpu_index, rank):
     splits = 152 if name == "long_decode" else 0
     seed = cfg["seed"] + 1000 * rank
     scale = 1.0 / math.sqrt(D)
-    row_bytes = 2 * 52 + 4
+    tok_bytes = 52 if bits == 3 else D * bits // 8
+    row_bytes = 2 * tok_bytes + 4
     kv_bytes = B * Hkv * Nk * row_bytes
     copies = max(1, math.ceil(4 * _l2_bytes(torch, device) / kv_bytes))
     caches = []
     g = torch.Generator(device=device)
     for r in range(copies):
-        c = qa.KvCache.contiguous(B, Hkv, Nk, D, device=device, code_bits=3)
+        c = qa.KvCache.contiguous(B, Hkv, Nk, D, device=device, code_bits=bits)
         g.manual_seed(seed * 31 + r)
         for b in range(B):
             sub = qa.KvCache(c.k_codes[b:b + 1], c.k_scales[b:b + 1], c.v_codes[b:b + 1], c.v_scales[b:b + 1], D,
-                             Hkv, capacity=c.capacity, code_bits=3)
+                             Hkv, capacity=c.capacity, code_bits=bits)
             qa.quantize_kv(torch.randn(1, Hkv, Nk, D, device=device, generator=g),
                            torch.randn(1, Hkv, Nk, D, device=device, generator=g), sub)
         caches.append(c)
@@ -503,15 +505,15 @@ def run_decode_int3(name, args, device, gpu_index, rank):
     res = {
         "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(tmax * 1e3 / args.steps, 5),
         "steps": args.steps,
-        "config": {"workload": f"{name}_int3", "B": B, "Hq": Hq, "Hkv": Hkv, "D": D, "Nk": Nk, "code_bits": 3,
+        "config": {"workload": f"{name}_int{bits}", "B": B, "Hq": Hq, "Hkv": Hkv, "D": D, "Nk": Nk, "code_bits": bits,
                    "splits": splits, "seed": cfg["seed"], "softmax_scale": scale, "kv_bytes_per_step": kv_bytes,
                    "l2": "rotating KV-cache copies totalling more than 4x L2",
-                   "step": "append one K/V row per sequence (INT3 quantize) + split-KV decode + combine"},
+                   "step": f"append one K/V row per sequence (INT{bits} quantize) + split-KV decode + merge"},
         "setup": {"cache_copies": copies, "parallelism": f"replicas x{world}",
                   "timing": "CUDA graphs of the API calls"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
-                     "kernel": "decode+combine (one qattn_decode call, INT3 cache)", "peak_source": pk_src,
+                     "kernel": f"decode + merge (one qattn_decode call, INT{bits} cache)", "peak_source": pk_src,
                      "us_per_launch": round(dec_ms * 1e3, 3)},
         "clocks": clocks,
     }
@@ -823,7 +825,8 @@ def main(argv=None):
         res["secondary"] = {
             "long_decode": compact(run_decode("long_decode", args, device, gpu_index, rank)),
             "long_decode_flashq": compact(run_decode_flashq("long_decode", args, device, gpu_index, rank)),
-            "long_decode_int3": compact(run_decode_int3("long_decode", args, device, gpu_index, rank)),
+            "long_decode_int3": compact(run_decode_lowbit("long_decode", args, device, gpu_index, rank, 3)),
+            "long_decode_int2": compact(run_decode_lowbit("long_decode", args, device, gpu_index, rank, 2)),
             "causal_prefill": compact(run_prefill("causal_prefill", args, device, gpu_index, rank,
                                                   steps=min(args.steps, 50))),
         }

@@ -96,6 +96,7 @@ typedef enum qattn_dtype {
 #define QATTN_FLAG_BAD_PAGE 2u     /* a page id or length was out of range; rows skipped */
 #define QATTN_FLAG_TMEM 4u         /* tensor-memory allocation failed */
 #define QATTN_FLAG_BUFFER_FULL 8u  /* qattn_flashq_append met a full buffer; the row was dropped */
+#define QATTN_FLAG_BAD_HEAD 16u    /* a cache's kv_head_index named no head of the model; rows skipped */
 
 /*
  * Where the quantized K and V live.  Passed by host pointer; the struct
@@ -117,6 +118,27 @@ typedef enum qattn_dtype {
  *                    INT3 is supported by qattn_quantize_kv and qattn_decode
  *                    for a contiguous cache with D = 128; other calls return
  *                    QATTN_ERR_UNSUPPORTED for it.
+ *                    2: INT2 ([TA] §3.2's 2-bit heads, read as this per-row
+ *                    symmetric codec at 2 bits: sixteen 2-bit values per
+ *                    little-endian 32-bit word, element j in word j / 16 at
+ *                    bits 2 (j % 16), two's complement; 32 bytes per row at
+ *                    D = 128; scale fp16(absmax), codes clamp(RNE(x / s),
+ *                    -1, 1)).  Supported like INT3.
+ *   kv_head_index    NULL: the cache holds every kv-head of the model.
+ *                    Otherwise a device int32 array [num_kv_heads]: cache
+ *                    head h is the model's kv-head kv_head_index[h] (one of
+ *                    model_kv_heads), as in a headwise mixed-precision layout
+ *                    ([TA] §3.2) that keeps the 2-bit and the 4-bit heads in
+ *                    two caches.  qattn_quantize_kv then reads k, v as
+ *                    [batch, model_kv_heads, n, D] and stores the listed
+ *                    heads; qattn_decode attends q-heads kv_head_index[h] * G
+ *                    .. + G - 1 (G = Hq / model_kv_heads) with cache head h
+ *                    and writes only those rows of out and lse.  An entry
+ *                    outside [0, model_kv_heads) raises QATTN_FLAG_BAD_HEAD
+ *                    and its rows are skipped.  Contiguous caches only; the
+ *                    other calls return QATTN_ERR_UNSUPPORTED for a listed
+ *                    cache.
+ *   model_kv_heads   kv-heads of the model (read when kv_head_index is set)
  */
 typedef struct qattn_kv_cache {
   uint8_t *k_codes;
@@ -131,6 +153,8 @@ typedef struct qattn_kv_cache {
   int64_t capacity;
   int64_t num_pages;
   int32_t code_bits;
+  const int32_t *kv_head_index;
+  int32_t model_kv_heads;
 } qattn_kv_cache;
 
 /*
@@ -352,6 +376,34 @@ qattn_status qattn_decode_noalloc(const uint16_t *q, const qattn_kv_cache *cache
                                   const int32_t *seq_lens, int32_t batch, int32_t num_q_heads,
                                   int32_t max_seq_len, float softmax_scale, int32_t num_splits,
                                   uint16_t *out, float *lse, qattn_stream_t stream);
+
+/*
+ * qattn_headwise_plan -- the headwise mixed-precision plan of [TA] §3.2:
+ * one priority per kv-head from a prompt's keys and values, and 2 bits for
+ * the num_low heads of lowest priority, 4 bits for the others.
+ *
+ *   k, v       [batch, Hkv, n, D] of x_dtype (fp32 or fp16), finite values;
+ *              the layout qattn_quantize_kv reads
+ *   lens       [batch] int32 (device) rows of each sequence that count
+ *              (clamped to [0, n]); NULL = all n
+ *   num_low    n_h, 0 <= num_low <= Hkv
+ *   bits       [Hkv] int32 (device), written: 2 or 4
+ *   priority   [Hkv] float64 (device), written when not NULL
+ *
+ * The page names the two statistics and omits the equation that combines
+ * them; this library's reading: per head and tensor, with mx_j and mn_j the
+ * largest and smallest value of channel j over the counted rows,
+ * gap = max_j mx_j - min_j mn_j, std = the population standard deviation of
+ * the channel gaps mx_j - mn_j, priority = gap * std; a kv-head's priority
+ * is the larger of its key and value priorities (its K and V share one bit
+ * width); ties go to the lower head index.  The statistics are binary64,
+ * summed in channel order without fused multiply-adds, so they are
+ * reproducible bit for bit.  Hkv <= 256.  Calls that overlap on the GPU
+ * race (they share one device scratch array).
+ */
+qattn_status qattn_headwise_plan(const void *k, const void *v, qattn_dtype x_dtype, int32_t batch,
+                                 int32_t num_kv_heads, int32_t n, int32_t head_dim, const int32_t *lens,
+                                 int32_t num_low, int32_t *bits, double *priority, qattn_stream_t stream);
 
 /* Static description of a status code (never NULL). */
 const char *qattn_status_string(qattn_status status);

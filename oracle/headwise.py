@@ -69,7 +69,7 @@ def priorities(k, v, lens=None) -> np.ndarray:
     k = np.asarray(k, dtype=np.float32)
     v = np.asarray(v, dtype=np.float32)
     B, H, n, _ = k.shape
-    ln = [n] * B if lens is None else [min(int(x), n) for x in lens]
+    ln = [n] * B if lens is None else [max(0, min(int(x), n)) for x in lens]
     out = np.zeros(H, dtype=np.float64)
     for h in range(H):
         kr = np.concatenate([k[b, h, :ln[b]] for b in range(B)])

@@ -30,7 +30,7 @@ QATTN_F32, QATTN_F16 = 0, 1
 PAGE_SIZE = 64
 MAX_GROUP = 8
 MAX_SPLITS = 1024
-FLAG_WAIT_TIMEOUT, FLAG_BAD_PAGE, FLAG_TMEM, FLAG_BUFFER_FULL = 1, 2, 4, 8
+FLAG_WAIT_TIMEOUT, FLAG_BAD_PAGE, FLAG_TMEM, FLAG_BUFFER_FULL, FLAG_BAD_HEAD = 1, 2, 4, 8, 16
 FLASHQ_ROWS = 64
 
 # Every symbol include/qattn.h declares.
@@ -39,6 +39,7 @@ EXPORTS = (
     "qattn_combine", "qattn_read_device_flags", "qattn_status_string", "qattn_last_error",
     "qattn_version", "qattn_decode_noalloc", "qattn_check_wait_timeout", "qattn_decode_append",
     "qattn_flashq_init", "qattn_flashq_append", "qattn_flashq_attend", "qattn_flashq_flush",
+    "qattn_headwise_plan",
 )
 
 
@@ -65,6 +66,8 @@ class KvCacheStruct(ctypes.Structure):
         ("capacity", ctypes.c_int64),
         ("num_pages", ctypes.c_int64),
         ("code_bits", ctypes.c_int32),
+        ("kv_head_index", ctypes.c_void_p),
+        ("model_kv_heads", ctypes.c_int32),
     ]
 
 
@@ -113,6 +116,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qattn_flashq_append": (i32, [vp, vp, i32, ctypes.POINTER(FlashqBufferStruct), i32, vp]),
         "qattn_flashq_attend": (i32, [vp, ctypes.POINTER(FlashqBufferStruct), i32, i32, f32, vp, vp, vp]),
         "qattn_flashq_flush": (i32, [ctypes.POINTER(FlashqBufferStruct), cache_p, vp, i32, vp]),
+        "qattn_headwise_plan": (i32, [vp, vp, i32, i32, i32, i32, i32, vp, i32, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -139,13 +143,16 @@ def _stream(device) -> ctypes.c_void_p:
 
 @dataclass
 class KvCache:
-    """Caller-owned INT4 (or INT3) KV cache (contiguous or paged) as torch tensors.
+    """Caller-owned INT4 (or INT3, INT2) KV cache (contiguous or paged) as torch tensors.
 
     contiguous: codes [B, Hkv, capacity, D/2] uint8, scales [B, Hkv, capacity] fp16
     paged:      codes [P, Hkv, 64, D/2] uint8, scales [P, Hkv, 64] fp16,
                 page_table [B, max_pages] int32 (-1 = no page)
     code_bits = 3: INT3 rows of 13 little-endian 32-bit words (52 bytes) at D = 128,
                 contiguous only (codes [B, Hkv, capacity, 52] uint8)
+    code_bits = 2: INT2 rows of 8 words (32 bytes) at D = 128, contiguous only
+    kv_head_index: int32 [Hkv] (device): cache head h is the model's kv-head
+                kv_head_index[h] of model_kv_heads (headwise mixed precision)
     """
     k_codes: torch.Tensor
     k_scales: torch.Tensor
@@ -157,11 +164,13 @@ class KvCache:
     page_table: Optional[torch.Tensor] = None
     num_pages: int = 0
     code_bits: int = 4
+    kv_head_index: Optional[torch.Tensor] = None
+    model_kv_heads: int = 0
 
     @staticmethod
     def contiguous(batch, num_kv_heads, capacity, head_dim, device="cuda", code_bits=4):
         cap = -(-capacity // PAGE_SIZE) * PAGE_SIZE
-        row = 4 * (-(-head_dim // 10)) if code_bits == 3 else head_dim // 2
+        row = 4 * (-(-head_dim // 10)) if code_bits == 3 else head_dim * code_bits // 8
         codes = lambda: torch.zeros(batch, num_kv_heads, cap, row, dtype=torch.uint8, device=device)
         scales = lambda: torch.zeros(batch, num_kv_heads, cap, dtype=torch.float16, device=device)
         return KvCache(codes(), scales(), codes(), scales(), head_dim, num_kv_heads, capacity=cap,
@@ -176,6 +185,11 @@ class KvCache:
                        page_table=pt, num_pages=num_pages)
 
     @property
+    def workspace_kv_heads(self) -> int:
+        """The kv-head count that sizes a decode workspace (the model's for a listed cache)."""
+        return self.model_kv_heads if self.kv_head_index is not None else self.num_kv_heads
+
+    @property
     def paged_layout(self) -> bool:
         return self.page_table is not None
 
@@ -185,6 +199,9 @@ class KvCache:
         s.v_codes, s.v_scales = self.v_codes.data_ptr(), self.v_scales.data_ptr()
         s.head_dim, s.num_kv_heads = self.head_dim, self.num_kv_heads
         s.code_bits = self.code_bits
+        if self.kv_head_index is not None:
+            s.kv_head_index = self.kv_head_index.data_ptr()
+            s.model_kv_heads = self.model_kv_heads
         if self.page_table is not None:
             s.page_table = self.page_table.data_ptr()
             s.max_pages_per_seq = self.page_table.shape[1]
@@ -227,7 +244,7 @@ def decode(q: torch.Tensor, cache: KvCache, seq_lens: torch.Tensor, max_seq_len:
     if lse is None and return_lse:
         lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
     if workspace is None:  # a given workspace is checked by the library itself
-        need = decode_workspace_size(B, Hq, cache.num_kv_heads, D, max_seq_len, num_splits)
+        need = decode_workspace_size(B, Hq, cache.workspace_kv_heads, D, max_seq_len, num_splits)
         if need:
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     sl = seq_lens.to(device=q.device, dtype=torch.int32).contiguous()
@@ -257,7 +274,7 @@ def decode_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, cac
     if lse is None and return_lse:
         lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
     if workspace is None:  # a given workspace is checked by the library itself
-        need = decode_workspace_size(B, Hq, cache.num_kv_heads, D, max_seq_len, num_splits)
+        need = decode_workspace_size(B, Hq, cache.workspace_kv_heads, D, max_seq_len, num_splits)
         if need:
             workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     sl = seq_lens.to(device=q.device, dtype=torch.int32).contiguous()
@@ -385,3 +402,49 @@ def read_device_flags(clear: bool = True) -> int:
     f = ctypes.c_uint32(0)
     _check(load_library().qattn_read_device_flags(ctypes.byref(f), int(clear)), "qattn_read_device_flags")
     return int(f.value)
+
+
+def headwise_plan(k: torch.Tensor, v: torch.Tensor, num_low: int, lens: Optional[torch.Tensor] = None):
+    """Headwise mixed precision (qattn_headwise_plan): priorities of the kv-heads of a
+    prompt's k, v [B, Hkv, n, D] (fp32 or fp16) and bits [Hkv] int32, 2 for the num_low
+    lowest-priority heads and 4 for the others.  Returns (bits, priority float64)."""
+    if k.dtype not in (torch.float32, torch.float16) or v.dtype != k.dtype:
+        raise TypeError("k and v must both be float32 or float16")
+    k, v = k.contiguous(), v.contiguous()
+    B, H, n, D = k.shape
+    bits = torch.empty(H, dtype=torch.int32, device=k.device)
+    prio = torch.empty(H, dtype=torch.float64, device=k.device)
+    ln = None if lens is None else lens.to(device=k.device, dtype=torch.int32).contiguous()
+    dt = QATTN_F16 if k.dtype == torch.float16 else QATTN_F32
+    _check(load_library().qattn_headwise_plan(_ptr(k), _ptr(v), dt, B, H, n, D, _ptr(ln), num_low, _ptr(bits),
+                                              _ptr(prio), _stream(k.device)), "qattn_headwise_plan")
+    return bits, prio
+
+
+def mixed_caches(bits, batch: int, capacity: int, head_dim: int, device="cuda"):
+    """The two caches of a headwise plan: (4-bit heads, 2-bit heads), each listing its
+    heads' model indices in kv_head_index (None when a width has no head)."""
+    b = [int(x) for x in (bits.tolist() if torch.is_tensor(bits) else bits)]
+    caches = []
+    for width in (4, 2):
+        idx = [h for h, x in enumerate(b) if x == width]
+        if not idx:
+            caches.append(None)
+            continue
+        c = KvCache.contiguous(batch, len(idx), capacity, head_dim, device, code_bits=width)
+        c.kv_head_index = torch.tensor(idx, dtype=torch.int32, device=device)
+        c.model_kv_heads = len(b)
+        caches.append(c)
+    return tuple(caches)
+
+
+def decode_mixed(q: torch.Tensor, caches, seq_lens: torch.Tensor, max_seq_len: int, softmax_scale: float,
+                 num_splits: int = 0, return_lse: bool = False):
+    """Decode over the caches of a headwise plan: each writes the rows of its own heads."""
+    q = q.contiguous()
+    out = torch.empty_like(q)
+    lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=q.device) if return_lse else None
+    for c in caches:
+        if c is not None:
+            decode(q, c, seq_lens, max_seq_len, softmax_scale, num_splits, out=out, lse=lse)
+    return (out, lse) if return_lse else out

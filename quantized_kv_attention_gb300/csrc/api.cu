@@ -116,9 +116,9 @@ qattn_status decode_maps(DecodeMaps *m, const KvView &v, int batch, int warps) {
   const uint64_t tokens = paged ? kPage : static_cast<uint64_t>(v.capacity);
   // code bytes per token: D/2 (INT4) or 52 (INT3, D = 128); INT3 stages are
   // read with plain word loads, so their boxes are not swizzled
-  const uint64_t tok_bytes = v.bits == 3 ? 52 : static_cast<uint64_t>(v.head_dim / 2);
+  const uint64_t tok_bytes = v.bits == 3 ? 52 : static_cast<uint64_t>(v.head_dim * v.bits / 8);
   const uint64_t rows = tokens * tok_bytes / 128;
-  const cuuint32_t box_rows = v.bits == 3 ? static_cast<cuuint32_t>(geo.tokens_per_stage * tok_bytes / 128)
+  const cuuint32_t box_rows = v.bits != 4 ? static_cast<cuuint32_t>(geo.tokens_per_stage * tok_bytes / 128)
                                           : static_cast<cuuint32_t>(geo.box_rows);
   if (heads > 0x7fffffffull || rows > 0x7fffffffull) return fail(QATTN_ERR_UNSUPPORTED, "cache too large");
   const void *bases[4] = {v.k_codes, v.v_codes, v.k_scales, v.v_scales};
@@ -163,12 +163,20 @@ qattn_status check_cache(const qattn_kv_cache *c, int batch, KvView *v, uint64_t
   v->page_table = c->page_table;
   v->hkv = c->num_kv_heads;
   v->head_dim = c->head_dim;
-  if (c->code_bits != 0 && c->code_bits != 4 && c->code_bits != 3)
-    return fail(QATTN_ERR_INVALID_ARG, "code_bits %d (0 or 4: INT4, 3: INT3)", c->code_bits);
-  v->bits = c->code_bits == 3 ? 3 : 4;
-  if (v->bits == 3 && (c->page_table || c->head_dim != 128))
-    return fail(QATTN_ERR_UNSUPPORTED, "INT3 needs a contiguous cache with head_dim 128");
-  const uint64_t row_bytes = v->bits == 3 ? 52 : static_cast<uint64_t>(c->head_dim / 2);
+  if (c->code_bits != 0 && c->code_bits != 4 && c->code_bits != 3 && c->code_bits != 2)
+    return fail(QATTN_ERR_INVALID_ARG, "code_bits %d (0 or 4: INT4, 3: INT3, 2: INT2)", c->code_bits);
+  v->bits = c->code_bits == 0 ? 4 : c->code_bits;
+  if (v->bits != 4 && (c->page_table || c->head_dim != 128))
+    return fail(QATTN_ERR_UNSUPPORTED, "INT%d needs a contiguous cache with head_dim 128", v->bits);
+  v->head_map = c->kv_head_index;
+  v->model_hkv = c->num_kv_heads;
+  if (c->kv_head_index) {
+    if (c->page_table) return fail(QATTN_ERR_UNSUPPORTED, "kv_head_index with a paged cache");
+    if (c->model_kv_heads < c->num_kv_heads)
+      return fail(QATTN_ERR_INVALID_ARG, "model_kv_heads %d < num_kv_heads %d", c->model_kv_heads, c->num_kv_heads);
+    v->model_hkv = c->model_kv_heads;
+  }
+  const uint64_t row_bytes = v->bits == 3 ? 52 : static_cast<uint64_t>(c->head_dim * v->bits / 8);
   v->capacity = 0, v->num_pages = 0, v->max_pages = 0;
   if (c->page_table) {
     if (c->page_size != QATTN_PAGE_SIZE)
@@ -244,6 +252,32 @@ qattn_status qattn_quantize_kv(const void *k, const void *v, qattn_dtype x_dtype
   return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "quantize launch");
 }
 
+qattn_status qattn_headwise_plan(const void *k, const void *v, qattn_dtype x_dtype, int32_t batch,
+                                 int32_t num_kv_heads, int32_t n, int32_t head_dim, const int32_t *lens,
+                                 int32_t num_low, int32_t *bits, double *priority, qattn_stream_t stream) {
+  if (batch < 0 || batch > QATTN_MAX_BATCH || n < 0)
+    return fail(QATTN_ERR_INVALID_ARG, "batch %d, n %d", batch, n);
+  if (x_dtype != QATTN_F32 && x_dtype != QATTN_F16) return fail(QATTN_ERR_INVALID_ARG, "x_dtype %d", (int)x_dtype);
+  if (head_dim != 64 && head_dim != 128) return fail(QATTN_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", head_dim);
+  if (num_kv_heads <= 0 || num_kv_heads > headwise_max_heads())
+    return fail(QATTN_ERR_UNSUPPORTED, "num_kv_heads %d (1..%d)", num_kv_heads, headwise_max_heads());
+  if (num_low < 0 || num_low > num_kv_heads)
+    return fail(QATTN_ERR_INVALID_ARG, "num_low %d (0..%d)", num_low, num_kv_heads);
+  if (!bits) return fail(QATTN_ERR_INVALID_ARG, "bits is NULL");
+  if (batch > 0 && n > 0) {
+    if (!k || !v) return fail(QATTN_ERR_INVALID_ARG, "k or v is NULL");
+    if (static_cast<int64_t>((n + 255) / 256) * batch * num_kv_heads > 0x7fffffffLL)
+      return fail(QATTN_ERR_UNSUPPORTED, "batch * Hkv * n too large");
+  }
+  DeviceState *ds;
+  qattn_status st = device_state(&ds);
+  if (st != QATTN_OK) return st;
+  cudaError_t e = launch_headwise_plan(k, v, x_dtype == QATTN_F16, batch, num_kv_heads, batch > 0 ? n : 0,
+                                       head_dim, lens, num_low, bits, priority,
+                                       reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "headwise plan launch");
+}
+
 size_t qattn_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                    int32_t head_dim, int32_t max_seq_len, int32_t num_splits) {
   if (batch <= 0 || batch > QATTN_MAX_BATCH || num_q_heads <= 0 || num_kv_heads <= 0 ||
@@ -293,26 +327,28 @@ qattn_status decode_impl(const uint16_t *q, const void *k_new, const void *v_new
   uint64_t code_bytes = 0;
   qattn_status st = check_cache(cache, batch, &view, &code_bytes);
   if (st != QATTN_OK) return st;
-  if (num_q_heads % view.hkv) return fail(QATTN_ERR_INVALID_ARG, "Hq %d is not a multiple of Hkv %d", num_q_heads, view.hkv);
-  if (num_q_heads / view.hkv > QATTN_MAX_GROUP)
-    return fail(QATTN_ERR_UNSUPPORTED, "group size %d > %d", num_q_heads / view.hkv, QATTN_MAX_GROUP);
+  if (num_q_heads % view.model_hkv)
+    return fail(QATTN_ERR_INVALID_ARG, "Hq %d is not a multiple of the model's Hkv %d", num_q_heads, view.model_hkv);
+  if (num_q_heads / view.model_hkv > QATTN_MAX_GROUP)
+    return fail(QATTN_ERR_UNSUPPORTED, "group size %d > %d", num_q_heads / view.model_hkv, QATTN_MAX_GROUP);
   if (!hkv_supported(view.hkv, view.page_table != nullptr))
     return fail(QATTN_ERR_UNSUPPORTED, "paged num_kv_heads %d (supported: 1, 2 or a multiple of 4)", view.hkv);
   if (batch == 0) return QATTN_OK;
   if (!q || !seq_lens || !out) return fail(QATTN_ERR_INVALID_ARG, "q, seq_lens or out is NULL");
   if (!aligned16(q) || !aligned16(out)) return fail(QATTN_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
   if ((k_new == nullptr) != (v_new == nullptr)) return fail(QATTN_ERR_INVALID_ARG, "k_new and v_new: both or neither");
-  if (view.bits == 3 && k_new) return fail(QATTN_ERR_UNSUPPORTED, "qattn_decode_append on an INT3 cache");
+  if (view.bits != 4 && k_new) return fail(QATTN_ERR_UNSUPPORTED, "qattn_decode_append on an INT%d cache", view.bits);
+  if (view.head_map && k_new) return fail(QATTN_ERR_UNSUPPORTED, "qattn_decode_append with kv_head_index");
   if (k_new && (!aligned16(k_new) || !aligned16(v_new)))
     return fail(QATTN_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
   DeviceState *ds;
   if ((st = device_state(&ds)) != QATTN_OK) return st;
-  const int G = num_q_heads / view.hkv;
+  const int G = num_q_heads / view.model_hkv;
   const int64_t stage_limit = view.page_table ? view.max_pages : view.capacity / kPage;
   if (static_cast<int64_t>(batch) * view.hkv * stage_limit >= (int64_t(1) << 31))
     return fail(QATTN_ERR_UNSUPPORTED, "batch * Hkv * cached stages exceeds 2^31");
   const bool paged = view.page_table != nullptr;
-  const int warps = view.bits == 3 ? 8 : decode_layout(batch, view.hkv, max_seq_len, paged,
+  const int warps = view.bits != 4 ? 8 : decode_layout(batch, view.hkv, max_seq_len, paged,
                                                         num_splits > 0 ? num_splits : ds->sms);
   const int ctas = plan_ctas(batch, view.hkv, view.head_dim, max_seq_len, num_splits, ds->sms, paged, warps);
   const DecodeGeometry geo = decode_geometry(view.head_dim, view.hkv, paged, warps);
@@ -389,7 +425,8 @@ qattn_status check_flashq_cache(const qattn_flashq_buffer *b, const qattn_kv_cac
   if (st != QATTN_OK) return st;
   uint64_t code_bytes = 0;
   if ((st = check_cache(cache, batch, kv, &code_bytes)) != QATTN_OK) return st;
-  if (kv->bits == 3) return fail(QATTN_ERR_UNSUPPORTED, "the decode buffer on an INT3 cache");
+  if (kv->bits != 4) return fail(QATTN_ERR_UNSUPPORTED, "the decode buffer on an INT%d cache", kv->bits);
+  if (kv->head_map) return fail(QATTN_ERR_UNSUPPORTED, "the decode buffer with kv_head_index");
   if (kv->head_dim != fv->head_dim || kv->hkv != fv->hkv)
     return fail(QATTN_ERR_INVALID_ARG, "buffer (D %d, Hkv %d) and cache (D %d, Hkv %d) differ", fv->head_dim,
                 fv->hkv, kv->head_dim, kv->hkv);
@@ -470,7 +507,8 @@ qattn_status qattn_prefill(const uint16_t *q, const qattn_kv_cache *cache, int32
   uint64_t code_bytes = 0;
   qattn_status st = check_cache(cache, batch, &view, &code_bytes);
   if (st != QATTN_OK) return st;
-  if (view.bits == 3) return fail(QATTN_ERR_UNSUPPORTED, "qattn_prefill on an INT3 cache");
+  if (view.bits != 4) return fail(QATTN_ERR_UNSUPPORTED, "qattn_prefill on an INT%d cache", view.bits);
+  if (view.head_map) return fail(QATTN_ERR_UNSUPPORTED, "qattn_prefill with kv_head_index");
 
   if (num_q_heads % view.hkv) return fail(QATTN_ERR_INVALID_ARG, "Hq %d is not a multiple of Hkv %d", num_q_heads, view.hkv);
   if (nq > nk) return fail(QATTN_ERR_INVALID_ARG, "nq %d > nk %d", nq, nk);

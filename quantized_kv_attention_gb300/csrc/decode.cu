@@ -71,11 +71,12 @@ struct Layout {
 };
 
 // BITS = 4: the INT4 rows (D/2 bytes); BITS = 3: INT3 rows of ten 3-bit
-// values per 32-bit word (D = 128: 13 words, 52 bytes), read unswizzled.
+// values per 32-bit word (D = 128: 13 words, 52 bytes), read unswizzled;
+// BITS = 2: INT2 rows of sixteen 2-bit values per word (D = 128: 32 bytes).
 template <int D, int W, int BITS = 4>
 struct Cfg {
   static constexpr int kRows = Layout<W>::kRows;
-  static constexpr int kTokBytes = BITS == 3 ? 52 : D / 2;  // code bytes per (token, kv-head)
+  static constexpr int kTokBytes = BITS == 3 ? 52 : BITS == 2 ? D / 4 : D / 2;  // code bytes per (token, kv-head)
   static constexpr int kCodeBytes = kRows * kTokBytes;      // per tensor per stage
   static constexpr int kScaleBytes = kRows * 2;
   // the last stage of a segment also hosts the cross-warp merge area
@@ -91,7 +92,7 @@ struct Cfg {
   static constexpr int kMergePitch = D + 4;
   static_assert(W * 8 * kMergePitch * 4 <= kStageBytes, "merge area fits a stage");
   static constexpr int kRing = kStages * kStageBytes;
-  static constexpr int kKBytes = D / 8;  // K code bytes per lane per token
+  static constexpr int kKBytes = kTokBytes / 4;  // K code bytes per lane per token (INT4, INT2)
   static constexpr int kWords = kKBytes / 4;
   static constexpr int kMt = D / 16;     // m-tiles of O^T, k-steps of S
   // INT3: k-steps of S (10 words' pairs per lane), m-tiles of O^T (5 pairs of
@@ -123,6 +124,24 @@ __device__ __forceinline__ void decode_sub(uint32_t w, uint32_t (&out)[4]) {
   out[1] = lop3_and_xor(w, 0x00F000F0u, 0x00800080u);
   out[2] = lop3_and_xor(w8, 0x000F000Fu, 0x00080008u);
   out[3] = lop3_and_xor(w8, 0x00F000F0u, 0x00800080u);
+}
+
+// INT2 word -> eight MMA registers of fp16 subnormals: out[e] = (field e,
+// field e + 8) * 4^(e & 3) * 2^-24 as u = code + 2 (the XOR flips each
+// 2-bit field's sign bit); fields 4..7 of each half are read after a shift
+// by 8, so no field reaches the exponent bits.  For a K word the two fields
+// are elements e and e + 8 of one row; for an ldmatrix.trans word of V they
+// are element e of two tokens.
+__device__ __forceinline__ void decode_sub2(uint32_t w, uint32_t (&out)[8]) {
+  const uint32_t w8 = w >> 8;
+  out[0] = lop3_and_xor(w, 0x00030003u, 0x00020002u);
+  out[1] = lop3_and_xor(w, 0x000C000Cu, 0x00080008u);
+  out[2] = lop3_and_xor(w, 0x00300030u, 0x00200020u);
+  out[3] = lop3_and_xor(w, 0x00C000C0u, 0x00800080u);
+  out[4] = lop3_and_xor(w8, 0x00030003u, 0x00020002u);
+  out[5] = lop3_and_xor(w8, 0x000C000Cu, 0x00080008u);
+  out[6] = lop3_and_xor(w8, 0x00300030u, 0x00200020u);
+  out[7] = lop3_and_xor(w8, 0x00C000C0u, 0x00800080u);
 }
 
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
@@ -301,7 +320,7 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
   constexpr int kConsumerWarps = W;
   constexpr int kThreads = Layout<W>::kThreads;
   constexpr int kRowsPerStage = Layout<W>::kRows;
-  const int G = a.hq / cache.hkv;
+  const int G = a.hq / cache.model_hkv;
   const int B = a.batch, hkv = cache.hkv;
   const StageGeo geo = stage_geo<W>(hkv, cache.page_table != nullptr);
   extern __shared__ uint8_t smem_raw[];
@@ -435,9 +454,13 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
             return;
           }
           const uint32_t qf = smem_u32(qfull);
+          int mh = model_head(cache.head_map, cache.model_hkv, l.hg * geo.hb);
+          if (mh < 0) {  // no such model head: a harmless load; its rows are not written
+            atomicOr(err, kFlagBadHead);
+            mh = 0;
+          }
           mbar_arrive_expect_tx(qf, qbytes);
-          bulk_g2s(smem_u32(qslot),
-                   a.q + (static_cast<int64_t>(l.b) * a.hq + static_cast<int64_t>(l.hg) * geo.hb * G) * D, qbytes, qf);
+          bulk_g2s(smem_u32(qslot), a.q + (static_cast<int64_t>(l.b) * a.hq + static_cast<int64_t>(mh) * G) * D, qbytes, qf);
         }
         for (int j = 0; j < cnt; ++j, ++it) {
           const int s = it % C::kStages;
@@ -540,12 +563,12 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
   for (int t = 0; t < 2; ++t) {
 #pragma unroll
     for (int h = 0; h < 2; ++h)
-      koff[t][h] = swz128(kofs + (tok_w + t * 16 + g + 8 * h) * (D / 2) + c * C::kKBytes);
+      koff[t][h] = swz128(kofs + (tok_w + t * 16 + g + 8 * h) * C::kTokBytes + c * C::kKBytes);
 #pragma unroll
     for (int jp = 0; jp < D / 64; ++jp) {
       const int q = lane >> 3;
       const int vt = tok_w + t * 16 + ((q & 2) ? 8 : 0) + (lane & 7);
-      voff[t][jp] = swz128(kofs + vt * (D / 2) + (2 * jp + (q & 1)) * 16);
+      voff[t][jp] = swz128(kofs + vt * C::kTokBytes + (2 * jp + (q & 1)) * 16);  // INT2: jp = 0 only
     }
   }
   if (BITS == 4 && a.k_new) {
@@ -571,7 +594,32 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
     // out 16x larger, so those columns carry q / 16.
     uint32_t qb[BITS == 3 ? C::kKs3 : C::kMt][2];
     float qsum = 0.f;
-    if constexpr (BITS == 3) {
+    if constexpr (BITS == 2) {
+      // INT2: lane c covers d = 32 c + 16 i + {0..15} (word i of its K code
+      // bytes); k-step 4 i + j multiplies fields (2j, 2j + 8) and (2j + 1,
+      // 2j + 9) of the word, which come out 4^(e & 3) larger, so those
+      // columns carry q / 4^(e & 3)
+      if (!mbar_wait(smem_u32(qfull), seg & 1, err, *abort_flag ? kDrainCycles : kWaitCycles))
+        *abort_flag = 1;
+      const uint32_t qrow = smem_u32(qslot) + ((hbw * G + min(g, G - 1)) * D + c * (D / 4)) * 2;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const uint4 u = g < G ? lds128(qrow + 32 * i) : make_uint4(0, 0, 0, 0);
+        const uint4 v = g < G ? lds128(qrow + 32 * i + 16) : make_uint4(0, 0, 0, 0);
+        const uint32_t uu[4] = {u.x, u.y, u.z, u.w}, vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float s0 = (j & 1) ? 16.f : 1.f, s1 = (j & 1) ? 64.f : 4.f;
+          const uint32_t e0 = __byte_perm(uu[j], vv[j], 0x5410), e1 = __byte_perm(uu[j], vv[j], 0x7632);
+          const __half2 h0 = __hmul2(*reinterpret_cast<const __half2 *>(&e0), __float2half2_rn(1.f / s0));
+          const __half2 h1 = __hmul2(*reinterpret_cast<const __half2 *>(&e1), __float2half2_rn(1.f / s1));
+          qb[4 * i + j][0] = *reinterpret_cast<const uint32_t *>(&h0);
+          qb[4 * i + j][1] = *reinterpret_cast<const uint32_t *>(&h1);
+          const float2 f0 = __half22float2(h0), f1 = __half22float2(h1);
+          qsum += s0 * (f0.x + f0.y) + s1 * (f1.x + f1.y);  // the values the MMA multiplies
+        }
+      }
+    } else if constexpr (BITS == 3) {
       // INT3: register r of lane c takes field pair p = r % 5 of its word
       // slot r / 5 (words c, c + 4, c + 8, and 12 for lane 0): d = 10 w + p
       // (low half, which came out 2x larger: q / 2) and 10 w + p + 5
@@ -622,8 +670,8 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
     qsum += __shfl_xor_sync(0xffffffffu, qsum, 1);
     qsum += __shfl_xor_sync(0xffffffffu, qsum, 2);
     // raw-unit bias (code offset) * sum(q) * 2^-24 for the lane's q-heads 2c
-    // and 2c+1; the offset is 8 for INT4 codes, 4 for INT3
-    constexpr float kOff = BITS == 3 ? 4.f : 8.f;
+    // and 2c+1; the offset is 8 for INT4 codes, 4 for INT3, 2 for INT2
+    constexpr float kOff = BITS == 3 ? 4.f : BITS == 2 ? 2.f : 8.f;
     const float bq0 = kOff / kTwo24 * __shfl_sync(0xffffffffu, qsum, (2 * c) << 2);
     const float bq1 = kOff / kTwo24 * __shfl_sync(0xffffffffu, qsum, (2 * c + 1) << 2);
 
@@ -652,7 +700,32 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
         for (int t = 0; t < 2; ++t)
 #pragma unroll
           for (int e = 0; e < 4; ++e) sacc[t][e] = so[t][e] = 0.f;
-        if constexpr (BITS == 3) {
+        if constexpr (BITS == 2) {
+          // words 2c, 2c + 1 of rows g and g + 8 of each tile
+          uint32_t kw[2][2][2];
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint2 u = lds64(kb + koff[t][h]);
+              kw[t][h][0] = u.x, kw[t][h][1] = u.y;
+            }
+#pragma unroll
+          for (int i = 0; i < 2; ++i)
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              uint32_t x0[8], x1[8];
+              decode_sub2(kw[t][0][i], x0);
+              decode_sub2(kw[t][1][i], x1);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                if (j & 1)
+                  mma_16816(so[t], x0[2 * j], x1[2 * j], x0[2 * j + 1], x1[2 * j + 1], qb[4 * i + j][0], qb[4 * i + j][1]);
+                else
+                  mma_16816(sacc[t], x0[2 * j], x1[2 * j], x0[2 * j + 1], x1[2 * j + 1], qb[4 * i + j][0], qb[4 * i + j][1]);
+              }
+            }
+        } else if constexpr (BITS == 3) {
           // words c, c + 4, c + 8 (and 12 for lane 0) of rows g and g + 8 of each tile
           uint32_t kw3[2][2][4];
 #pragma unroll
@@ -765,7 +838,23 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
           pb[t][1] = movmatrix_trans(r1);
         }
         // O^T += V codes^T . P'^T
-        if constexpr (BITS == 3) {
+        if constexpr (BITS == 2) {
+          // one ldmatrix.x4.trans per tile: matrix q holds tokens (q & 2 ? 8 :
+          // 0) + 0..7 at 16-byte chunk q & 1 (64 dimensions); m-tile k row g
+          // is d = 8 g + k, row g + 8 is d = 64 + 8 g + k (4^(k & 3) larger)
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4_trans(vb + voff[t][0], r0, r1, r2, r3);
+            uint32_t d0[8], d1[8], d2[8], d3[8];
+            decode_sub2(r0, d0);
+            decode_sub2(r1, d1);
+            decode_sub2(r2, d2);
+            decode_sub2(r3, d3);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mma_16816(o[k], d0[k], d1[k], d2[k], d3[k], pb[t][0], pb[t][1]);
+          }
+        } else if constexpr (BITS == 3) {
           // lane g owns words g and g + 8 of the V rows: m-tile 5 jj + p, row
           // g is d = 10 (g + 8 jj) + p (2x larger), row g + 8 is d + 5; the
           // two tokens of each A register come from two words, paired by
@@ -831,7 +920,28 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
     }
     consumer_sync<W>();  // every warp has read its last stage
     float *mo = reinterpret_cast<float *>(smem + last * C::kStageBytes);
-    if constexpr (BITS == 3) {
+    if constexpr (BITS == 2) {
+      // O^T m-tile k: row g holds d = 8 g + k, row g + 8 holds d = 64 + 8 g + k,
+      // 4^(k & 3) larger; code offset 2; P' carried 2^-8.  Float4 runs along d.
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int kg = 0; kg < 2; ++kg) {
+          float v0[4], v1[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int k = 4 * kg + e;
+            const float f = kTwo24 / static_cast<float>(1 << (2 * (k & 3)));
+            v0[e] = (o[k][2 * hh] * f - 2.f * ps0) * 256.f;
+            v1[e] = (o[k][2 * hh + 1] * f - 2.f * ps1) * 256.f;
+          }
+          const int d = 64 * hh + 8 * g + 4 * kg;
+          if (2 * c < G)
+            *reinterpret_cast<float4 *>(mo + (warp * 8 + 2 * c) * C::kMergePitch + d) = make_float4(v0[0], v0[1], v0[2], v0[3]);
+          if (2 * c + 1 < G)
+            *reinterpret_cast<float4 *>(mo + (warp * 8 + 2 * c + 1) * C::kMergePitch + d) = make_float4(v1[0], v1[1], v1[2], v1[3]);
+        }
+    } else if constexpr (BITS == 3) {
       // O^T m-tile 5 jj + p: row g holds d = 10 (g + 8 jj) + p (2x larger),
       // row g + 8 holds d + 5; code offset 4; P' carried 2^-8
 #pragma unroll
@@ -911,7 +1021,9 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
       const float inv = live ? 1.f / L : 0.f;
       const float lse_v = live ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
       if (complete) {
-        const int64_t row = static_cast<int64_t>(l.b) * a.hq + (l.hg * geo.hb + hh) * G + h;
+        const int mh = model_head(cache.head_map, cache.model_hkv, l.hg * geo.hb + hh);
+        if (mh < 0) continue;  // flagged by the producer
+        const int64_t row = static_cast<int64_t>(l.b) * a.hq + mh * G + h;
         const uint32_t h01 = pack_half2(acc.x * inv, acc.y * inv), h23 = pack_half2(acc.z * inv, acc.w * inv);
         *reinterpret_cast<uint2 *>(a.out + row * D + d) = make_uint2(h01, h23);
         if (d == 0 && a.lse) a.lse[row] = lse_v;
@@ -945,7 +1057,8 @@ constexpr int kMergeWarps = 8;
 template <int D, int W>
 __global__ void __launch_bounds__(kMergeWarps * 32, 4)
     decode_merge_kernel(const int32_t *__restrict__ seq_lens, int batch, int hkv, int G, int ctas,
-                        int64_t limit, int paged, const float *__restrict__ po,
+                        int64_t limit, int paged, const int32_t *__restrict__ head_map, int model_hkv,
+                        const float *__restrict__ po,
                         const float *__restrict__ pl, uint16_t *__restrict__ out,
                         float *__restrict__ lse) {
   constexpr int VPL = D / 32;
@@ -985,7 +1098,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4)
   tot = pre = nzt = nzb = 0;
   for (int w = 0; w < kMergeWarps; ++w) tot += redi[0][w], pre += redi[1][w], nzt += redi[2][w], nzb += redi[3][w];
   const int rows = geo.hb * G;
-  const int64_t row = static_cast<int64_t>(b) * hkv * G + static_cast<int64_t>(hg) * rows + r;
+  const int mh = model_head(head_map, model_hkv, hg * geo.hb + r / G);
+  if (mh < 0) return;  // flagged by the decode kernel
+  const int64_t row = (static_cast<int64_t>(b) * model_hkv + mh) * G + r % G;
   const int n = stages(b);
   if (n == 0) {  // no decode CTA touches this row
     pdl_wait();
@@ -1079,7 +1194,7 @@ cudaError_t launch_d(const DecodeArgs &a, const KvView &cache, const DecodeMaps 
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int G = a.hq / cache.hkv;
+  const int G = a.hq / cache.model_hkv;
   const bool paged = cache.page_table != nullptr;
   const StageGeo geo = stage_geo<W>(cache.hkv, paged);
   Maps maps;
@@ -1102,7 +1217,8 @@ cudaError_t launch_d(const DecodeArgs &a, const KvView &cache, const DecodeMaps 
   mc.attrs = attr;
   mc.numAttrs = 1;
   return cudaLaunchKernelEx(&mc, decode_merge_kernel<D, W>, a.seq_lens, a.batch, cache.hkv, G, a.ctas, limit,
-                            static_cast<int>(paged), static_cast<const float *>(a.partial_o), static_cast<const float *>(a.partial_lse),
+                            static_cast<int>(paged), cache.head_map, static_cast<int>(cache.model_hkv),
+                            static_cast<const float *>(a.partial_o), static_cast<const float *>(a.partial_lse),
                             a.out, a.lse);
 }
 
@@ -1134,6 +1250,7 @@ cudaError_t launch_decode(const DecodeArgs &a, const KvView &cache, const Decode
                           cudaStream_t stream) {
   if (a.batch == 0 || a.ctas <= 0) return cudaSuccess;
   if (cache.bits == 3) return launch_d<128, 8, 3>(a, cache, maps, err, stream);  // contiguous, D = 128
+  if (cache.bits == 2) return launch_d<128, 8, 2>(a, cache, maps, err, stream);  // contiguous, D = 128
   if (cache.page_table || a.warps == 8)
     return cache.head_dim == 128 ? launch_d<128, 8>(a, cache, maps, err, stream)
                                  : launch_d<64, 8>(a, cache, maps, err, stream);

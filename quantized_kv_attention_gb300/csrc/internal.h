@@ -19,10 +19,26 @@ struct KvView {
   int32_t max_pages;          // paged: page-table row length
   int32_t hkv;
   int32_t head_dim;
-  int32_t bits;               // 4 (INT4) or 3 (INT3: contiguous, D = 128)
+  int32_t bits;               // 4 (INT4), 3 (INT3) or 2 (INT2); INT3 and INT2: contiguous, D = 128
+  // A cache holding some of a model's kv-heads: cache head h is the model's
+  // kv-head head_map[h] of model_hkv (nullptr: h itself, model_hkv = hkv).
+  const int32_t *head_map;
+  int32_t model_hkv;
 };
 
 constexpr int kPage = 64;  // tokens per page and per decode pipeline stage
+
+// Status bit QATTN_FLAG_BAD_HEAD: a cache's head map named no head of the
+// model (its rows were skipped).
+constexpr uint32_t kFlagBadHead = 16u;
+
+// The model's kv-head of cache head h (KvView::head_map); -1 when the map
+// names no head of the model.
+__device__ __forceinline__ int model_head(const int32_t *head_map, int model_hkv, int h) {
+  if (!head_map) return h;
+  const int m = __ldg(head_map + h);
+  return m >= 0 && m < model_hkv ? m : -1;
+}
 
 // quantize.cu
 cudaError_t launch_quantize(const void *k, const void *v, bool fp16_in, int batch, int n,
@@ -83,6 +99,13 @@ cudaError_t launch_flashq_flush(const FlashqView &f, const KvView &c, const int3
 
 cudaError_t launch_decode(const DecodeArgs &a, const KvView &cache, const DecodeMaps &maps, uint32_t *err,
                           cudaStream_t stream);
+
+// headwise.cu: priorities of the kv-heads of k, v [batch, Hkv, n, D] and
+// bits[h] = 2 for the n_low lowest, else 4 (see include/qattn.h).
+int headwise_max_heads();
+cudaError_t launch_headwise_plan(const void *k, const void *v, bool fp16_in, int batch, int hkv, int n,
+                                 int head_dim, const int32_t *lens, int n_low, int32_t *bits, double *priority,
+                                 cudaStream_t stream);
 
 // combine.cu (pdl: launched as a programmatic dependent of the previous kernel)
 cudaError_t launch_combine(const float *partial_o, const float *partial_lse, int splits,

@@ -144,4 +144,38 @@ __device__ __forceinline__ void quantize_row3_warp(const T *src, uint32_t *dst_w
   if (lane == 0) *dst_scale = __half_as_ushort(hs);
 }
 
+// INT2 (TurboAttention, arXiv 2412.08585, §3.2's 2-bit heads, in this
+// library's per-row symmetric layout) of one D = 128 row: s = fp16(absmax)
+// (fp32(absmax / 1) is exact; saturating at 65504), code = clamp(RNE(x / s),
+// -1, 1), i.e. +-1 when |x| > s / 2 (a tie at s / 2 goes to the even 0);
+// element j goes to word j / 16 at bits 2 (j % 16) as a 2-bit two's-
+// complement field.  Lane i holds elements 4i..4i+3, one byte of word i / 4;
+// lanes 4k gather the four bytes of word k by shuffles and store it.
+template <typename T>
+__device__ __forceinline__ void quantize_row2_warp(const T *src, uint32_t *dst_words, uint16_t *dst_scale,
+                                                   int lane) {
+  float x[4];
+  RowLoad<T, 4>::load(src + lane * 4, x);
+  float am = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+  __half hs = __float2half_rn(am);
+  if (__hisinf(hs)) hs = __ushort_as_half(0x7BFF);
+  const float s = __half2float(hs);
+  const float h = 0.5f * s;
+  uint32_t byte = 0;  // the lane's four 2-bit fields
+  if (s > 0.f) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t f = fabsf(x[j]) > h ? (x[j] < 0.f ? 3u : 1u) : 0u;
+      byte |= f << (2 * j);
+    }
+  }
+  const uint32_t b1 = __shfl_down_sync(0xffffffffu, byte, 1);
+  const uint32_t b2 = __shfl_down_sync(0xffffffffu, byte, 2);
+  const uint32_t b3 = __shfl_down_sync(0xffffffffu, byte, 3);
+  if ((lane & 3) == 0) dst_words[lane >> 2] = byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
+  if (lane == 0) *dst_scale = __half_as_ushort(hs);
+}
+
 }  // namespace qattn

@@ -1,4 +1,4 @@
-// quantize.cu -- quantize-on-append: new K/V rows -> INT4 codes + fp16 scales.
+// quantize.cu -- quantize-on-append: new K/V rows -> INT4 (INT3, INT2) codes + fp16 scales.
 //
 // TurboAttention (arXiv 2412.08585) §2.1: each decoding step appends k_t, v_t
 // to the cache (prefill appends all prompt rows at once); §2.3: symmetric
@@ -23,12 +23,18 @@ __global__ void __launch_bounds__(256)
   const int64_t rows = static_cast<int64_t>(batch) * cache.hkv * n;
   if (row >= rows) return;
   const bool is_v = blockIdx.y != 0;
-  const T *src = (is_v ? v : k) + row * D;
 
   const int i = static_cast<int>(row % n);
   const int64_t bh = row / n;
   const int h = static_cast<int>(bh % cache.hkv);
   const int b = static_cast<int>(bh / cache.hkv);
+  // the source rows are the model's: cache head h reads model head head_map[h]
+  const int mh = model_head(cache.head_map, cache.model_hkv, h);
+  if (mh < 0) {  // warp-uniform
+    if (lane == 0 && err) atomicOr(err, kFlagBadHead);
+    return;
+  }
+  const T *src = (is_v ? v : k) + ((static_cast<int64_t>(b) * cache.model_hkv + mh) * n + i) * D;
   const int64_t pos = static_cast<int64_t>(start_pos ? __ldg(start_pos + b) : 0) + i;
 
   int64_t dst_row = -1;  // row index in the destination cache
@@ -48,6 +54,10 @@ __global__ void __launch_bounds__(256)
   if constexpr (D == 128) {
     if (cache.bits == 3) {  // 13 words per row
       quantize_row3_warp<T>(src, reinterpret_cast<uint32_t *>(codes + dst_row * 52), scales + dst_row, lane);
+      return;
+    }
+    if (cache.bits == 2) {  // 8 words per row
+      quantize_row2_warp<T>(src, reinterpret_cast<uint32_t *>(codes + dst_row * 32), scales + dst_row, lane);
       return;
     }
   }

@@ -182,3 +182,50 @@ def test_int3_cache_checks():
     assert lib.qattn_decode_append(FAKE, FAKE, FAKE, qa.QATTN_F32, ctypes.byref(c3), FAKE, 1, 4, 100, 1.0, 0, None, 0,
                                    FAKE, None, None) == qa.QATTN_ERR_UNSUPPORTED
     assert lib.qattn_flashq_init(ctypes.byref(_fq()), ctypes.byref(c3), FAKE, 1, None) == qa.QATTN_ERR_UNSUPPORTED
+
+
+def test_int2_cache_checks():
+    assert _decode(_cache(code_bits=1)) == qa.QATTN_ERR_INVALID_ARG
+    assert _decode(_cache(code_bits=2, head_dim=64)) == qa.QATTN_ERR_UNSUPPORTED
+    paged2 = _cache(code_bits=2, page_table=FAKE, page_size=64, num_pages=4, max_pages_per_seq=2)
+    assert _decode(paged2) == qa.QATTN_ERR_UNSUPPORTED
+    c2 = _cache(code_bits=2)
+    assert lib.qattn_prefill(FAKE, ctypes.byref(c2), 1, 4, 8, 8, 1.0, 1, FAKE, None, None) == qa.QATTN_ERR_UNSUPPORTED
+    assert lib.qattn_decode_append(FAKE, FAKE, FAKE, qa.QATTN_F32, ctypes.byref(c2), FAKE, 1, 4, 100, 1.0, 0, None, 0,
+                                   FAKE, None, None) == qa.QATTN_ERR_UNSUPPORTED
+    assert lib.qattn_flashq_init(ctypes.byref(_fq()), ctypes.byref(c2), FAKE, 1, None) == qa.QATTN_ERR_UNSUPPORTED
+
+
+def test_kv_head_index_checks():
+    # a cache holding 2 of a model's 4 kv-heads
+    listed = _cache(kv_head_index=FAKE, model_kv_heads=4)
+    assert _decode(_cache(kv_head_index=FAKE, model_kv_heads=1)) == qa.QATTN_ERR_INVALID_ARG  # fewer than it holds
+    paged = _cache(kv_head_index=FAKE, model_kv_heads=4, page_table=FAKE, page_size=64, num_pages=4,
+                   max_pages_per_seq=2)
+    assert _decode(paged) == qa.QATTN_ERR_UNSUPPORTED
+    assert _decode(listed, hq=6) == qa.QATTN_ERR_INVALID_ARG      # Hq must divide by the model's 4 heads
+    assert _decode(listed, hq=4 * 65) == qa.QATTN_ERR_UNSUPPORTED  # group size above the limit
+    assert lib.qattn_prefill(FAKE, ctypes.byref(listed), 1, 4, 8, 8, 1.0, 1, FAKE, None, None) == \
+        qa.QATTN_ERR_UNSUPPORTED
+    assert lib.qattn_decode_append(FAKE, FAKE, FAKE, qa.QATTN_F32, ctypes.byref(listed), FAKE, 1, 8, 100, 1.0, 0,
+                                   None, 0, FAKE, None, None) == qa.QATTN_ERR_UNSUPPORTED
+    assert lib.qattn_flashq_init(ctypes.byref(_fq()), ctypes.byref(listed), FAKE, 1, None) == qa.QATTN_ERR_UNSUPPORTED
+
+
+def _plan(**kw):
+    a = dict(k=FAKE, v=FAKE, dt=qa.QATTN_F32, batch=1, hkv=4, n=16, d=128, lens=None, low=1, bits=FAKE, prio=None)
+    a.update(kw)
+    return lib.qattn_headwise_plan(a["k"], a["v"], a["dt"], a["batch"], a["hkv"], a["n"], a["d"], a["lens"],
+                                   a["low"], a["bits"], a["prio"], None)
+
+
+def test_headwise_plan_rejects_bad_arguments():
+    assert _plan(low=-1) == qa.QATTN_ERR_INVALID_ARG
+    assert _plan(low=5) == qa.QATTN_ERR_INVALID_ARG
+    assert _plan(hkv=0) == qa.QATTN_ERR_UNSUPPORTED
+    assert _plan(hkv=257, low=0) == qa.QATTN_ERR_UNSUPPORTED
+    assert _plan(d=96) == qa.QATTN_ERR_UNSUPPORTED
+    assert _plan(bits=None) == qa.QATTN_ERR_INVALID_ARG
+    assert _plan(k=None) == qa.QATTN_ERR_INVALID_ARG
+    assert _plan(dt=7) == qa.QATTN_ERR_INVALID_ARG
+    assert _plan(batch=-1) == qa.QATTN_ERR_INVALID_ARG
