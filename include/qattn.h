@@ -178,7 +178,8 @@ qattn_status qattn_quantize_kv(const void *k, const void *v, qattn_dtype x_dtype
 /*
  * qattn_decode_workspace_size -- bytes of workspace qattn_decode needs for
  * `num_splits` key ranges (0 = the automatic choice for these sizes on the
- * current device).  Host-only; returns 0 for invalid sizes.
+ * current device).  Host-only; returns 0 for invalid sizes.  For a cache
+ * with a kv_head_index pass the model's kv-head count (model_kv_heads).
  */
 size_t qattn_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                    int32_t head_dim, int32_t max_seq_len, int32_t num_splits);

@@ -51,8 +51,10 @@ extern "C" qattn_status qattn_decode_noalloc(const uint16_t *q, const qattn_kv_c
   char msg[256];
   // Size first: a request whose partials do not fit is refused before any
   // device work (qattn_decode validates everything else).
-  const size_t need = qattn_decode_workspace_size(batch, num_q_heads, cache ? cache->num_kv_heads : 0,
-                                                  cache ? cache->head_dim : 0, max_seq_len, num_splits);
+  // a listed cache's split rows follow the model's group size
+  const int32_t ws_hkv = cache ? (cache->kv_head_index ? cache->model_kv_heads : cache->num_kv_heads) : 0;
+  const size_t need = qattn_decode_workspace_size(batch, num_q_heads, ws_hkv, cache ? cache->head_dim : 0,
+                                                  max_seq_len, num_splits);
   if (need > QATTN_NOALLOC_SCRATCH_BYTES) {
     snprintf(msg, sizeof(msg),
              "qattn_decode_noalloc: these sizes need %zu bytes of split scratch, more than the "
