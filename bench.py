@@ -795,6 +795,56 @@ def run_reference(args):
             "gpu_launches": 0}
 
 
+def run_quantize(name, args, device, gpu_index, rank):
+    """qattn_quantize_kv alone (a1, quantize-on-append) on a prefill workload's
+    K and V rows (fp32 in): GB/s of its algorithmic bytes, the fp32 rows read
+    plus the INT4 codes and fp16 scales written, per (token, kv-head) row
+    D*4 + D/2 + 2 bytes for each of K and V.  Rotating input copies larger
+    than 2x L2; CUDA graphs of the API call, CUDA events on the stream."""
+    import torch
+    import quantized_kv_attention_gb300 as qa
+    from quantized_kv_attention_gb300 import workloads as wl
+    cfg = dict(wl.WORKLOADS[name])
+    B, Hkv, D, N = cfg["B"], cfg["Hkv"], cfg["D"], cfg["Nk"]
+    rows = 2 * B * Hkv * N
+    step_bytes = rows * (D * 4 + D // 2 + 2)
+    in_bytes = rows * D * 4
+    copies = max(2, math.ceil(2 * _l2_bytes(torch, device) / in_bytes))
+    g = torch.Generator(device=device)
+    g.manual_seed(cfg["seed"] + 1000 * rank)
+    ks = [torch.randn(B, Hkv, N, D, device=device, generator=g) for _ in range(copies)]
+    vs = [torch.randn(B, Hkv, N, D, device=device, generator=g) for _ in range(copies)]
+    cache = qa.KvCache.contiguous(B, Hkv, N, D, device=device)
+
+    def enqueue(n):
+        for i in range(n):
+            qa.quantize_kv(ks[i % copies], vs[i % copies], cache)
+
+    enqueue(max(args.warmup, 1))
+    torch.cuda.synchronize()
+    steps = min(args.steps, 100)
+    total_ms, one_ms, clocks = _timed_graphs(torch, steps, enqueue, enqueue, copies * max(1, 32 // copies),
+                                             gpu_index, period=copies, soak_s=min(args.soak, 0.5))
+    value, tmax, world = aggregate(step_bytes * steps / 1e9, total_ms / 1e3, device)
+    peaks, pk_src = measured_peaks()
+    achieved = step_bytes / (one_ms / 1e3) / 1e9
+    res = {
+        "value": round(value, 1), "unit": "GB/s", "ms_per_step": round(tmax * 1e3 / steps, 5), "steps": steps,
+        "config": {"workload": f"{name}_quantize", "B": B, "Hkv": Hkv, "D": D, "rows_per_tensor": N,
+                   "x_dtype": "fp32", "bytes_per_step": step_bytes,
+                   "l2": "rotating input copies totalling more than 2x L2",
+                   "step": "quantize all K and V rows of the prompt into the INT4 cache (one qattn_quantize_kv)"},
+        "setup": {"input_copies": copies, "parallelism": f"replicas x{world}", "timing": "CUDA graphs of the API call"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None, "kernel": "quantize_kv",
+                     "peak_source": pk_src, "us_per_launch": round(one_ms * 1e3, 3)},
+        "clocks": clocks,
+    }
+    del ks, vs, cache
+    torch.cuda.empty_cache()
+    return res
+
+
 def compact(res):
     keep = ("value", "unit", "ms_per_step", "steps", "config", "setup", "roofline", "e2e", "clocks")
     return {k: res[k] for k in keep if k in res}
@@ -830,6 +880,11 @@ def main(argv=None):
             "causal_prefill": compact(run_prefill("causal_prefill", args, device, gpu_index, rank,
                                                   steps=min(args.steps, 50))),
         }
+        try:  # a secondary number: its failure must not take the others with it
+            res["secondary"]["causal_prefill_quantize"] = compact(
+                run_quantize("causal_prefill", args, device, gpu_index, rank))
+        except Exception as e:  # reported, not hidden
+            res["secondary"]["causal_prefill_quantize"] = {"error": f"{type(e).__name__}: {e}"}
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
         res["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
     if rank == 0:
