@@ -1,4 +1,4 @@
-// decode.cu -- split-KV decode attention over the INT4 cache.
+// decode.cu -- split-KV decode attention over the INT4 (INT3, INT2) cache.
 //
 // TurboAttention (arXiv 2412.08585) §2.1: a decode step attends the new query
 // q_t against the whole cache; §2.2: FlashAttention's tiling with the online
@@ -19,8 +19,9 @@
 // HBM speed.
 //
 // Work split.  Stages of all (sequence, head-group) segments form one list;
-// a persistent grid of one CTA per SM cuts it into equal contiguous ranges,
-// so every SM streams the same number of bytes whatever the lengths.  A
+// a persistent grid of one CTA per SM cuts it into contiguous ranges of equal
+// cost (a stage, plus a fixed share for each segment a range starts), so every
+// SM does the same work whatever the lengths.  A
 // segment inside one range is finished by its CTA (fp16 O and lse); a segment
 // cut by range boundaries leaves one fp32 partial per CTA it touches, merged
 // by decode_merge_kernel (launched as a programmatic dependent, small enough
@@ -42,6 +43,10 @@
 //     P' = P * s_V[token] in fp16, moved to the B-operand layout by movmatrix.
 //     O^T (D x 8 q-heads) += V codes^T . P'^T, V transposed by ldmatrix.trans
 //       and decoded the same way; O = 2^24 / f acc - 8 sum(P').
+//   INT3 and INT2 rows take the same path with their own field extraction
+//   (ext3, decode_sub2), code offsets 4 and 2, and Q columns scaled to match.
+//   A cache listing some of a model's kv-heads (head_map) reads the Q rows and
+//   writes the output rows of the model head each of its heads stands for.
 #include <math.h>
 
 #include "../../include/qattn.h"
