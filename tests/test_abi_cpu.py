@@ -229,3 +229,21 @@ def test_headwise_plan_rejects_bad_arguments():
     assert _plan(k=None) == qa.QATTN_ERR_INVALID_ARG
     assert _plan(dt=7) == qa.QATTN_ERR_INVALID_ARG
     assert _plan(batch=-1) == qa.QATTN_ERR_INVALID_ARG
+
+
+def test_mixed_caches_split_the_heads_by_width():
+    import torch
+    bits = torch.tensor([4, 2, 4, 4, 2, 4], dtype=torch.int32)
+    c4, c2 = qa.mixed_caches(bits, 3, 100, 128, device="cpu")
+    assert c4.kv_head_index.tolist() == [0, 2, 3, 5] and c2.kv_head_index.tolist() == [1, 4]
+    assert (c4.code_bits, c2.code_bits) == (4, 2)
+    assert c4.model_kv_heads == c2.model_kv_heads == 6
+    assert tuple(c4.k_codes.shape) == (3, 4, 128, 64)    # capacity rounded up to whole 64-token stages
+    assert tuple(c2.v_codes.shape) == (3, 2, 128, 32)    # INT2: 32 bytes per row at D = 128
+    assert c2.workspace_kv_heads == 6
+    s = c2.struct()
+    assert s.kv_head_index == c2.kv_head_index.data_ptr() and s.model_kv_heads == 6 and s.code_bits == 2
+    only4, none2 = qa.mixed_caches([4, 4], 1, 64, 64, device="cpu")
+    assert none2 is None and only4.kv_head_index.tolist() == [0, 1]
+    plain = qa.KvCache.contiguous(1, 2, 64, 128, device="cpu")
+    assert plain.struct().kv_head_index is None and plain.workspace_kv_heads == 2
