@@ -236,7 +236,9 @@ def decode(q: torch.Tensor, cache: KvCache, seq_lens: torch.Tensor, max_seq_len:
            softmax_scale: float, num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
            out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
            return_lse: bool = False):
-    """q [B, Hq, D] fp16 -> out [B, Hq, D] fp16 (and lse [B, Hq] fp32)."""
+    """q [B, Hq, D] fp16 -> out [B, Hq, D] fp16 (and lse [B, Hq] fp32).  A cache
+    with a kv_head_index writes only the rows of the q-heads its kv-heads serve
+    (pass `out` / `lse` to collect several such caches; see decode_mixed)."""
     q = q.contiguous()
     B, Hq, D = q.shape
     if out is None:
