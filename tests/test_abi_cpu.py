@@ -247,3 +247,17 @@ def test_mixed_caches_split_the_heads_by_width():
     assert none2 is None and only4.kv_head_index.tolist() == [0, 1]
     plain = qa.KvCache.contiguous(1, 2, 64, 128, device="cpu")
     assert plain.struct().kv_head_index is None and plain.workspace_kv_heads == 2
+
+
+def test_binding_argument_counts_match_the_header():
+    import os
+    import re
+    from common import ROOT
+    with open(os.path.join(ROOT, "include", "qattn.h")) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    decls = re.findall(r"\b(qattn_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S)
+    assert len(decls) == len(qa.EXPORTS)
+    for name, params in decls:
+        params = params.strip()
+        n = 0 if params in ("", "void") else params.count(",") + 1
+        assert len(getattr(lib, name).argtypes) == n, name
