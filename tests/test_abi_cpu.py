@@ -261,3 +261,31 @@ def test_binding_argument_counts_match_the_header():
         params = params.strip()
         n = 0 if params in ("", "void") else params.count(",") + 1
         assert len(getattr(lib, name).argtypes) == n, name
+
+
+def test_ctypes_structs_match_the_c_layout(tmp_path):
+    """sizeof and every field offset of the two ABI structs, as the C compiler
+    lays them out, against the binding's ctypes mirrors."""
+    import os
+    import shutil
+    from common import ROOT
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    structs = {"qattn_kv_cache": qa.KvCacheStruct, "qattn_flashq_buffer": qa.FlashqBufferStruct}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "qattn.h"', "int main(void) {"]
+    for cname, py in structs.items():
+        lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
+        for fname, _ in py._fields_:
+            lines.append(f'  printf("{cname} {fname} %zu\\n", offsetof({cname}, {fname}));')
+    lines.append("  return 0;\n}")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    want = []
+    for cname, py in structs.items():
+        want.append(f"{cname} size {ctypes.sizeof(py)}")
+        want += [f"{cname} {f} {getattr(py, f).offset}" for f, _ in py._fields_]
+    assert [l for l in got if l] == want
