@@ -3,11 +3,12 @@
  * KV cache on NVIDIA GB300 (sm_103a).
  *
  * Sources of the operations (page title and section):
- *   [FAQ3]  "Quantized Cross-Attention: Extending FlashAttention-3 with
+ *   [QCA]   "Quantized Cross-Attention: Extending FlashAttention-3 with
  *           In-SRAM Dequantization": §3.1 in-SRAM dequantization fused into
  *           the attention loop; §3.2 tile of 4-bit codes plus one FP16 scale
- *           per token; §4.1 kernel signature ([batch, heads, seq, dim]
- *           ordering, compressed KV, per-token scales, output).
+ *           per token; §3.3 split-K dequantization and the 3-bit packing;
+ *           §4.1 kernel signature ([batch, heads, seq, dim] ordering,
+ *           compressed KV, per-token scales, output).
  *   [TA]    TurboAttention (arXiv 2412.08585): §2.1 prefill and decoding with
  *           a KV cache (K_t = K_{t-1} | k_t); §2.2 Equation 2 (S = QK^T,
  *           P = softmax(S), H = PV) and FlashAttention's tiled online
@@ -18,9 +19,15 @@
  * Conventions shared by every call
  * --------------------------------
  * Memory.   Every pointer is a DEVICE pointer unless marked "host".  The
- *           caller owns every buffer; the library allocates nothing and
- *           keeps no state between calls besides immutable kernel handles
- *           and one device status word (qattn_read_device_flags).
+ *           caller owns every buffer and the library allocates nothing.
+ *           Between calls it keeps, per device that loads it, immutable
+ *           kernel handles and three static device arrays: the status word
+ *           of qattn_read_device_flags (4 bytes), the split scratch of
+ *           qattn_decode_noalloc (QATTN_NOALLOC_SCRATCH_BYTES, 8 MiB) and
+ *           the per-head statistics of qattn_headwise_plan (512 KiB).
+ *           The last two are shared by every call that uses them, so such
+ *           calls that overlap on the GPU race; each call rewrites every
+ *           value of them it later reads.
  * Streams.  Work is enqueued on `stream` (a cudaStream_t; NULL = legacy
  *           default stream).  No call synchronises, except
  *           qattn_read_device_flags; results are ready when the stream has run.
@@ -32,7 +39,7 @@
  * Layout.   All tensors are dense row-major in the shapes given, 16-byte
  *           aligned.  fp16 values travel as uint16_t bit patterns.
  *
- * The KV-cache format (bit-exact; [FAQ3] §3.2, [TA] §2.3)
+ * The KV-cache format (bit-exact; [QCA] §3.2, [TA] §2.3)
  * -------------------------------------------------------
  *   row      one (token, kv-head) vector of D values
  *   scale    s = fp16(fp32(absmax / 7)), round-to-nearest-even twice; a
@@ -186,7 +193,7 @@ size_t qattn_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t n
 
 /*
  * qattn_decode -- one query token per sequence against its whole cache
- * ([TA] §2.1 decoding; fused in-SRAM dequantization as in [FAQ3] §3.1).
+ * ([TA] §2.1 decoding; fused in-SRAM dequantization as in [QCA] §3.1).
  *
  *   q            [batch, Hq, D] fp16
  *   cache        contiguous or paged INT4 cache
@@ -240,7 +247,7 @@ qattn_status qattn_decode_append(const uint16_t *q, const void *k_new, const voi
  * qattn_prefill -- Nq query rows per sequence against Nk cached keys
  * ([TA] §2.1 prefill, §2.2 FlashAttention tiling; dense contractions on
  * the tensor cores with the dequantization fused ahead of the operand
- * stage, [FAQ3] §3.1).  Contiguous or paged cache (chunked prefill of a
+ * stage, [QCA] §3.1).  Contiguous or paged cache (chunked prefill of a
  * paged cache: the new rows' Q against every cached key).
  *
  *   q        [batch, Hq, Nq, D] fp16
@@ -257,7 +264,11 @@ qattn_status qattn_prefill(const uint16_t *q, const qattn_kv_cache *cache, int32
                            int32_t causal, uint16_t *out, float *lse, qattn_stream_t stream);
 
 /*
- * qattn_combine -- log-sum-exp merge of split-KV partial results.
+ * qattn_combine -- log-sum-exp merge of split-KV partial results ([TA]
+ * §2.2: FlashAttention's online softmax keeps a running max and sum per
+ * row, so two partial results over disjoint key sets merge exactly by
+ * rescaling each with exp(lse_c - L); [QCA] §3.3 splits the key dimension
+ * across thread blocks and needs this merge).
  *
  *   partial_o    [num_splits, rows, D] fp32, each normalised within its split
  *   partial_lse  [num_splits, rows] fp32 (natural log); a split with

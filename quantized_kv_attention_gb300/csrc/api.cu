@@ -285,13 +285,18 @@ size_t qattn_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t n
       num_kv_heads <= 0 ||
       num_splits < 0 || num_splits > QATTN_MAX_SPLITS || (head_dim != 64 && head_dim != 128))
     return 0;
+  // The automatic split count follows the current device's SM count, cached
+  // by the per-device set-up; without a usable device the answer assumes
+  // 152 SMs.  Only an error raised by this query is cleared from the
+  // runtime, never one pending from the caller's own work.
   int sms = 152;
-  int dev = 0;
-  if (num_splits == 0 && cudaGetDevice(&dev) == cudaSuccess) {
-    int v = 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) sms = v;
+  if (num_splits == 0) {
+    DeviceState *ds = nullptr;
+    if (device_state(&ds) == QATTN_OK && ds->sms > 0)
+      sms = ds->sms;
+    else
+      cudaGetLastError();
   }
-  cudaGetLastError();
   // the larger of the two cache layouts' needs (the call does not say which one)
   size_t need = 0;
   // (and of both CTA layouts, so that the answer never depends on the choice)
