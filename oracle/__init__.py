@@ -13,6 +13,11 @@ codec      -- symmetric INT4 per-(token, kv-head) quantizer, nibble packing,
 attention  -- unfused attention over the dequantized cache: GQA, causal
               (bottom-right aligned), variable lengths, paged gather, and the
               log-sum-exp merge of split partials.
+codec3, codec2 -- the INT3 and INT2 per-row codecs.
+headwise   -- headwise mixed 2/4-bit precision: priorities and the bit plan.
+flashq     -- the int8 decode buffer with a universal scale, and its flush.
+baselines  -- the comparison paths: attention over an FP16 cache, and the
+              cache dequantized to FP16 first, then attended.
 
 Every function cites the passage of the source pages it follows.  Where the
 pages are silent or garbled the reading taken is stated in the docstring.
