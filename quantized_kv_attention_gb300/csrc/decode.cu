@@ -112,7 +112,7 @@ struct Cfg {
 template <int D, int W, int BITS = 4>
 __host__ __device__ constexpr int smem_bytes(int batch) {
   return Cfg<D, W, BITS>::kRing + Cfg<D, W, BITS>::kQSlot + 2 * W * 8 * 4 + (3 * batch + 2) * 4 +
-         (2 * Cfg<D, W, BITS>::kStages + 3) * 8 + Cfg<D, W, BITS>::kStages * 4 + 16 + 1024;
+         (2 * Cfg<D, W, BITS>::kStages + 3) * 8 + Cfg<D, W, BITS>::kStages * 4 + 32 + 1024;
 }
 
 template <int W>
@@ -181,12 +181,18 @@ constexpr int64_t kUnit = 16;
 template <int W>
 constexpr int64_t kSegCost = W == 12 ? 14 : 12;
 
+// Quotient of non-negative integers: 32-bit division when both fit (the
+// common case, a few instructions), else 64-bit (a long software routine).
+__host__ __device__ __forceinline__ int64_t udiv(int64_t a, int64_t b) {
+  if (((a | b) >> 32) == 0) return static_cast<uint32_t>(a) / static_cast<uint32_t>(b);
+  return a / b;
+}
 __host__ __device__ __forceinline__ int64_t cost_target(int64_t i, int64_t Wc, int64_t n) {
-  return i * Wc / n;
+  return udiv(i * Wc, n);
 }
 // CTA owning the stage whose cost offset is x: the largest i with t_i <= x.
 __host__ __device__ __forceinline__ int64_t cost_owner(int64_t x, int64_t Wc, int64_t n) {
-  const int64_t i = ((x + 1) * n + Wc - 1) / Wc - 1;
+  const int64_t i = udiv((x + 1) * n + Wc - 1, Wc) - 1;
   return i < n - 1 ? i : n - 1;
 }
 // Inside a segment the cost offset of stage g is 0 (g = 0), else sc + kUnit*g:
@@ -194,7 +200,7 @@ __host__ __device__ __forceinline__ int64_t cost_owner(int64_t x, int64_t Wc, in
 __host__ __device__ __forceinline__ int64_t stage_at(int64_t rr, int64_t sc) {
   if (rr <= 0) return 0;
   if (rr <= sc + kUnit) return 1;
-  return (rr - sc + kUnit - 1) / kUnit;
+  return (rr - sc + kUnit - 1) / kUnit;  // kUnit = 16: a shift
 }
 // First stage of CTA i: prefix[b] = groups * (stages of sequences before b),
 // nzp[b] = non-empty sequences before b, so the cost before sequence b is
@@ -211,7 +217,7 @@ __device__ __forceinline__ int64_t cost_start(int64_t i, int64_t n, int64_t Wc, 
   }
   const int64_t nb = (prefix[lo + 1] - prefix[lo]) / groups;
   const int64_t L = sc + kUnit * nb;  // cost of one segment of sequence lo
-  const int64_t r = t - P(lo), h = r / L;
+  const int64_t r = t - P(lo), h = udiv(r, L);
   return prefix[lo] + h * nb + stage_at(r - h * L, sc);
 }
 
@@ -345,6 +351,7 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
   uint64_t *appended = qempty + 1;                                   // fused append done (consumer warps)
   int *valid = reinterpret_cast<int *>(appended + 1);                // [kStages]: 0 = missing page
   volatile int *abort_flag = valid + C::kStages;                     // set after a timed-out wait
+  int64_t *range = reinterpret_cast<int64_t *>(valid + C::kStages + 2);  // [2]: this CTA's first, end stage
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool paged = cache.page_table != nullptr;
@@ -433,8 +440,12 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
   const int64_t T = prefix[B];
   const int64_t sc = kSegCost<W>;
   const int64_t Wc = kUnit * T + sc * geo.groups * nzp[B];
-  const int64_t gs0 = cost_start(blockIdx.x, gridDim.x, Wc, prefix, nzp, B, geo.groups, sc);
-  const int64_t gs1 = cost_start(blockIdx.x + 1, gridDim.x, Wc, prefix, nzp, B, geo.groups, sc);
+  // The range is computed once per CTA, by two lanes of warp 0, and shared:
+  // every thread computing it would keep the SM's issue slots busy with the
+  // same divisions for longer than the extra barrier takes.
+  if (warp == 0 && lane < 2) range[lane] = cost_start(blockIdx.x + lane, gridDim.x, Wc, prefix, nzp, B, geo.groups, sc);
+  __syncthreads();
+  const int64_t gs0 = range[0], gs1 = range[1];
   if (gs1 <= gs0) return;
 
   if (warp >= kConsumerWarps) {

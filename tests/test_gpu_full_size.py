@@ -108,3 +108,72 @@ def test_causal_prefill_full_size():
             assert_close_attention(out[b, hq].index_select(0, idx), O)
             assert_close_lse(lse[b, hq].index_select(0, idx), L)
     assert qa.read_device_flags() == 0
+
+
+def _paged_rows(cache, table, b, h, n):
+    """Rows 0..n-1 of (sequence b, kv-head h) gathered from the page pool."""
+    pages = torch.as_tensor(table[b, : (n + 63) // 64].astype(np.int64), device=cache.k_codes.device)
+    kc = cache.k_codes.index_select(0, pages)[:, h].reshape(-1, cache.k_codes.shape[-1])[:n]
+    vc = cache.v_codes.index_select(0, pages)[:, h].reshape(-1, cache.v_codes.shape[-1])[:n]
+    ks = cache.k_scales.index_select(0, pages)[:, h].reshape(-1)[:n]
+    vs = cache.v_scales.index_select(0, pages)[:, h].reshape(-1)[:n]
+    return kc.cpu().numpy(), ks.cpu().numpy(), vc.cpu().numpy(), vs.cpu().numpy()
+
+
+@pytest.mark.parametrize("scale", [1 / math.sqrt(128), 1.0])
+def test_paged_varlen_decode_full_size(scale):
+    """64 sequences with lengths uniform in [512, 32768], 64-token pages in a
+    randomly permuted pool, Hq=32, Hkv=8, D=128, automatic splits, one
+    qattn_decode_append step (the bench's launch), at softmax scale 1/sqrt(128)
+    and 1.0.  Three sequences (the shortest, the longest and one more) hold the
+    oracle's seeded rows and are checked whole: codes and scales bit for bit,
+    every q-head's O and lse.  The others hold device-drawn rows of the same
+    distribution (seeded), which keeps the workload's size and raggedness; for
+    them the check is that every output is finite."""
+    qa = require_gpu()
+    cfg = wl.WORKLOADS["paged_decode"]
+    B, Hq, Hkv, D, seed = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["seed"]
+    G = Hq // Hkv
+    lens, table, P = wl.paged_layout(seed, B, cfg["len_lo"], cfg["len_hi"], cfg["page"])
+    assert (lens >= cfg["len_lo"]).all() and (lens <= cfg["len_hi"]).all()
+    cache = qa.KvCache.paged(P, Hkv, D, torch.from_numpy(table))
+    picked = sorted({int(np.argmin(lens)), int(np.argmax(lens)), 17})
+    g = torch.Generator(device="cuda")
+    k_new = torch.empty(B, Hkv, D, device="cuda")
+    v_new = torch.empty(B, Hkv, D, device="cuda")
+    for b, n in enumerate(lens):
+        n = int(n)
+        if b in picked:
+            k = torch.stack([wl.kv_slice(seed, "k", b, h, n, D) for h in range(Hkv)])[None].cuda()
+            v = torch.stack([wl.kv_slice(seed, "v", b, h, n, D) for h in range(Hkv)])[None].cuda()
+        else:
+            g.manual_seed(seed * 7919 + b)
+            k = torch.randn(1, Hkv, n, D, device="cuda", generator=g)
+            v = torch.randn(1, Hkv, n, D, device="cuda", generator=g)
+        sub = qa.KvCache(cache.k_codes, cache.k_scales, cache.v_codes, cache.v_scales, D, Hkv,
+                         page_table=cache.page_table[b:b + 1], num_pages=P)
+        qa.quantize_kv(k[:, :, : n - 1], v[:, :, : n - 1], sub)   # the cached rows
+        k_new[b], v_new[b] = k[0, :, n - 1], v[0, :, n - 1]        # the step appends the last one
+        del k, v
+    q = wl.queries(seed, B, Hq, D)
+    sl = torch.from_numpy(lens.astype(np.int32)).cuda()
+    out, lse = qa.decode_append(q.cuda(), k_new, v_new, cache, sl, int(cfg["len_hi"]), scale, 0, return_lse=True)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    for b in picked:
+        n = int(lens[b])
+        for h in range(Hkv):
+            k = wl.kv_slice(seed, "k", b, h, n, D).numpy()
+            v = wl.kv_slice(seed, "v", b, h, n, D).numpy()
+            pk, sk = codec.quantize_pack(k)
+            pv, sv = codec.quantize_pack(v)
+            kc, ks, vc, vs = _paged_rows(cache, table, b, h, n)
+            assert np.array_equal(kc, pk) and np.array_equal(vc, pv)
+            assert np.array_equal(ks.view(np.uint16), sk.view(np.uint16))
+            assert np.array_equal(vs.view(np.uint16), sv.view(np.uint16))
+            qs = q.numpy()[b:b + 1, h * G:(h + 1) * G, None, :]
+            O, L = att.attention_quantized(qs, pk[None, None], sk[None, None], pv[None, None], sv[None, None],
+                                           scale, False)
+            assert_close_attention(out[b:b + 1, h * G:(h + 1) * G], O[:, :, 0])
+            assert_close_lse(lse[b:b + 1, h * G:(h + 1) * G], L[:, :, 0])
+    assert qa.read_device_flags() == 0
