@@ -856,6 +856,101 @@ def run_quantize(name, args, device, gpu_index, rank):
     return res
 
 
+def run_compare(name, args, device, gpu_index, rank):
+    """The comparison arms of "Quantized Cross-Attention ... In-SRAM
+    Dequantization" §5.2-§5.3 on a workload's shape: attention over an FP16
+    KV cache (qattn_decode_fp16 / qattn_prefill_fp16), and post-
+    dequantization (qattn_dequantize_kv of the whole INT4 cache into FP16 in
+    HBM, then the same FP16 call).  Returns two lines: the FP16 arm (GB/s of
+    its FP16 K/V bytes for decode, TFLOP/s for prefill, with a roofline), and
+    the post-dequantization arm (the workload's own metric, INT4 bytes or
+    FLOP per step, so it compares with the fused line directly).  CUDA graphs
+    of the API calls; FP16 caches rotate through copies larger than 4x L2
+    when they fit in 16 GB."""
+    import torch
+    import quantized_kv_attention_gb300 as qa
+    from quantized_kv_attention_gb300 import workloads as wl
+    cfg = dict(wl.WORKLOADS[name])
+    B, Hq, Hkv, D = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"]
+    prefill = cfg["kind"] == "prefill"
+    N = cfg["Nk"]
+    scale = 1.0 / math.sqrt(D)
+    peaks, pk_src = measured_peaks()
+    g = torch.Generator(device=device)
+    g.manual_seed(cfg["seed"] + 1000 * rank + 77)
+    f16_bytes = 2 * B * Hkv * N * D * 2
+    copies = max(1, min(math.ceil(4 * _l2_bytes(torch, device) / f16_bytes), int(16e9 // f16_bytes)))
+    ks = [torch.randn(B, Hkv, N, D, device=device, generator=g).half() for _ in range(copies)]
+    vs = [torch.randn(B, Hkv, N, D, device=device, generator=g).half() for _ in range(copies)]
+    # the INT4 cache of the post-dequantization arm, and its FP16 copy
+    cache = qa.KvCache.contiguous(B, Hkv, N, D, device=device)
+    qa.quantize_kv(torch.randn(B, Hkv, N, D, device=device, generator=g),
+                   torch.randn(B, Hkv, N, D, device=device, generator=g), cache)
+    k16, v16 = torch.empty_like(ks[0]), torch.empty_like(vs[0])
+    if prefill:
+        Nq = cfg["Nq"]
+        q = torch.randn(B, Hq, Nq, D, device=device, generator=g).half()
+        out = torch.empty_like(q)
+        work = prefill_flops(B, Hq, Nq, N, D, True)
+
+        def arm16(i):
+            qa.prefill_fp16(q, ks[i % copies], vs[i % copies], N, scale, True, out=out)
+
+        def post(i):
+            qa.dequantize_kv(cache, B, N, k16, v16)
+            qa.prefill_fp16(q, k16, v16, N, scale, True, out=out)
+    else:
+        q = torch.randn(B, Hq, D, device=device, generator=g).half()
+        out = torch.empty(B, Hq, D, dtype=torch.float16, device=device)
+        sl = torch.full((B,), N, dtype=torch.int32, device=device)
+        ws = torch.empty(max(qa.decode_fp16_workspace_size(B, Hq, Hkv, D, N, 0), 16), dtype=torch.uint8,
+                         device=device)
+        work = B * Hkv * N * (D + 4)
+
+        def arm16(i):
+            qa.decode_fp16(q, ks[i % copies], vs[i % copies], sl, N, scale, 0, workspace=ws, out=out)
+
+        def post(i):
+            qa.dequantize_kv(cache, B, N, k16, v16)
+            qa.decode_fp16(q, k16, v16, sl, N, scale, 0, workspace=ws, out=out)
+
+    steps = min(args.steps, 20 if prefill else 200)
+    res = {}
+    for arm, fn, per in (("fp16", arm16, copies), ("postdequant", post, 1)):
+        def enqueue(n, fn=fn):
+            for i in range(n):
+                fn(i)
+        enqueue(max(args.warmup, 1))
+        torch.cuda.synchronize()
+        total_ms, one_ms, clocks = _timed_graphs(torch, steps, enqueue, enqueue, per * max(1, 8 // per), gpu_index,
+                                                 period=per, soak_s=min(args.soak, 0.5),
+                                                 chunk=8 if prefill else 256)
+        value, tmax, world = aggregate((work / 1e12 if prefill else work / 1e9) * steps, total_ms / 1e3, device)
+        line = {"value": round(value, 2), "unit": "TFLOP/s" if prefill else "GB/s",
+                "ms_per_step": round(tmax * 1e3 / steps, 5), "steps": steps,
+                "config": {"workload": f"{name}_{arm}", "kv": "fp16" if arm == "fp16" else
+                           "int4 dequantized to fp16 in HBM, then attended",
+                           "l2": f"{per} rotating FP16 cache copies" if arm == "fp16" else "FP16 copy rewritten every step"},
+                "clocks": clocks}
+        if arm == "fp16":
+            if prefill:
+                ach = work / (one_ms / 1e3) / 1e12
+                line["roofline"] = {"bound": "tensor", "achieved": round(ach, 1), "peak": peaks["bf16_tflops"],
+                                    "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4),
+                                    "ms_per_launch": round(one_ms, 4), "peak_source": pk_src}
+            else:
+                ach = f16_bytes / (one_ms / 1e3) / 1e9
+                line["value"] = round(f16_bytes * steps / 1e9 / tmax, 2)
+                line["roofline"] = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
+                                    "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
+                                    "us_per_launch": round(one_ms * 1e3, 3), "peak_source": pk_src}
+                line["config"]["kv_bytes_per_step"] = f16_bytes
+        res[arm] = line
+    del ks, vs, cache, k16, v16
+    torch.cuda.empty_cache()
+    return res
+
+
 def compact(res):
     """A secondary line's essentials: throughput, step time, roofline, clocks."""
     out = {k: res[k] for k in ("value", "unit", "ms_per_step") if k in res}
@@ -901,7 +996,43 @@ def secondary_lines(args, device, gpu_index, rank):
     add("causal_prefill", lambda: run_prefill("causal_prefill", args, device, gpu_index, rank,
                                               steps=min(args.steps, 50)))
     add("causal_prefill_quantize", lambda: run_quantize("causal_prefill", args, device, gpu_index, rank))
+    for wname in ("long_decode", "gqa_decode", "causal_prefill"):
+        try:
+            for arm, line in run_compare(wname, args, device, gpu_index, rank).items():
+                sec[f"{wname}_{arm}"] = compact(line)
+        except Exception as e:  # reported, not hidden
+            sec[f"{wname}_fp16"] = {"error": f"{type(e).__name__}: {e}"}
     return sec
+
+
+VARIANTS = ("_int3", "_int2", "_flashq", "_quantize", "_fp16", "_postdequant")
+
+
+def run_workload(name, args, device, gpu_index, rank):
+    """A workload by name: a base workload (the hot path's step), or a base
+    name with a suffix for one secondary line on its shape (_int3, _int2:
+    the low-bit caches; _flashq: the decode buffer; _quantize: the append
+    kernel alone; _fp16, _postdequant: the comparison arms)."""
+    from quantized_kv_attention_gb300 import workloads as wl
+    suffix = next((v for v in VARIANTS if name.endswith(v)), "")
+    base = name[: len(name) - len(suffix)]
+    if base not in wl.WORKLOADS:
+        raise SystemExit(f"unknown workload {name}")
+    if suffix in ("_int3", "_int2"):
+        res = run_decode_lowbit(base, args, device, gpu_index, rank, int(suffix[-1]))
+    elif suffix == "_flashq":
+        res = run_decode_flashq(base, args, device, gpu_index, rank)
+    elif suffix == "_quantize":
+        res = run_quantize(base, args, device, gpu_index, rank)
+    elif suffix:
+        res = run_compare(base, args, device, gpu_index, rank)[suffix[1:]]
+    else:
+        kind = wl.WORKLOADS[base]["kind"]
+        res = (run_prefill if kind == "prefill" else run_decode)(base, args, device, gpu_index, rank)
+    for key, val in (("metric", METRIC), ("n_gpus", 1), ("warmup", args.warmup), ("higher_is_better", True),
+                     ("scaling", "weak"), ("vs_baseline", None), ("dtype", "f16"), ("data", "synthetic")):
+        res.setdefault(key, val)
+    return res
 
 
 def main(argv=None):
@@ -922,9 +1053,7 @@ def main(argv=None):
     barrier()
     gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[local]) \
         if os.environ.get("CUDA_VISIBLE_DEVICES") else local
-    kind = wl.WORKLOADS[args.workload]["kind"]
-    runner = run_prefill if kind == "prefill" else run_decode
-    res = runner(args.workload, args, device, gpu_index, rank)
+    res = run_workload(args.workload, args, device, gpu_index, rank)
     if args.secondary and world == 1 and args.workload == "long_decode":
         res["secondary"] = secondary_lines(args, device, gpu_index, rank)
     if rank == 0 and world == 1 and args.cpu_seconds > 0:

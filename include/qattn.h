@@ -417,6 +417,64 @@ qattn_status qattn_headwise_plan(const void *k, const void *v, qattn_dtype x_dty
                                  int32_t num_kv_heads, int32_t n, int32_t head_dim, const int32_t *lens,
                                  int32_t num_low, int32_t *bits, double *priority, qattn_stream_t stream);
 
+/*
+ * Comparison paths ([QCA] §5.2 Baselines, §5.3 Results): the page measures
+ * the fused 4-bit kernel against an FP16 FlashAttention kernel over an FP16
+ * KV cache, and against "post-dequantization", where the 4-bit cache is
+ * first written back to HBM in FP16 and then attended.  These calls build
+ * both arms on this GPU, so that what fusion saves can be measured here.
+ * They follow the conventions above (GQA, bottom-right causal, lse, empty
+ * rows); an FP16 cache is K, V [batch, Hkv, capacity, D] fp16, contiguous.
+ */
+
+/*
+ * qattn_dequantize_kv -- the first n tokens of every (sequence, kv-head) of
+ * an INT4 cache (contiguous or paged) written out as fp16:
+ *   k_out, v_out  [batch, Hkv, n, D] fp16, x16 = fl16(c * s) (the exact
+ *                 product rounded once to binary16, ties to even; products
+ *                 beyond the fp16 range become +-inf)
+ * n must not exceed the cache (capacity, or max_pages_per_seq * 64); a token
+ * in a missing page is written as zeros and raises QATTN_FLAG_BAD_PAGE.
+ * INT4 caches without kv_head_index only (QATTN_ERR_UNSUPPORTED otherwise).
+ */
+qattn_status qattn_dequantize_kv(const qattn_kv_cache *cache, int32_t batch, int32_t n, uint16_t *k_out,
+                                 uint16_t *v_out, qattn_stream_t stream);
+
+/* Workspace bytes of qattn_decode_fp16 for these sizes (0 when one key range
+ * suffices, and for invalid sizes).  Host-only. */
+size_t qattn_decode_fp16_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                        int32_t max_seq_len, int32_t num_splits);
+
+/*
+ * qattn_decode_fp16 -- qattn_decode over an FP16 cache.
+ *   q          [batch, Hq, D] fp16
+ *   k, v       [batch, Hkv, capacity, D] fp16 (capacity >= max_seq_len)
+ *   seq_lens   [batch] int32 (device), clamped to [0, capacity]
+ *   num_splits key ranges per (sequence, kv-head), 0 = one CTA per SM in all;
+ *              each range is a multiple of 64 tokens; with more than one the
+ *              partials are merged as qattn_combine does
+ *   workspace  qattn_decode_fp16_workspace_size() bytes (may be 0 / NULL)
+ *   out, lse   [batch, Hq, D] fp16, [batch, Hq] fp32 or NULL
+ * batch * Hkv <= 65535.
+ */
+qattn_status qattn_decode_fp16(const uint16_t *q, const uint16_t *k, const uint16_t *v, int32_t batch,
+                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int64_t capacity,
+                               const int32_t *seq_lens, int32_t max_seq_len, float softmax_scale, int32_t num_splits,
+                               void *workspace, size_t workspace_bytes, uint16_t *out, float *lse,
+                               qattn_stream_t stream);
+
+/*
+ * qattn_prefill_fp16 -- qattn_prefill over an FP16 cache: q [batch, Hq, Nq, D]
+ * against the first nk keys of k, v [batch, Hkv, capacity, D] fp16,
+ * 1 <= nq <= nk <= capacity; out [batch, Hq, Nq, D] fp16, lse [batch, Hq,
+ * Nq] fp32 or NULL.  The same tensor-core kernel as qattn_prefill, with K
+ * and V tiles loaded by TMA instead of dequantized.
+ */
+qattn_status qattn_prefill_fp16(const uint16_t *q, const uint16_t *k, const uint16_t *v, int32_t batch,
+                                int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int64_t capacity,
+                                int32_t nq, int32_t nk, float softmax_scale, int32_t causal, uint16_t *out,
+                                float *lse, qattn_stream_t stream);
+
 /* Static description of a status code (never NULL). */
 const char *qattn_status_string(qattn_status status);
 

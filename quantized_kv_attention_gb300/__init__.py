@@ -8,6 +8,8 @@ stream.  The calls mirror the C ABI in include/qattn.h:
     decode(q, cache, seq_lens, max_seq_len, scale)    one query per sequence
     prefill(q, cache, nq, nk, scale, causal)          Nq queries per sequence
     combine(partial_o, partial_lse)                   log-sum-exp merge
+    dequantize_kv, decode_fp16, prefill_fp16          the comparison paths (FP16 cache;
+                                                      dequantize to FP16, then attend)
 
 There is no fallback: if libqattn.so is missing or fails to load, every call
 raises.
@@ -39,7 +41,8 @@ EXPORTS = (
     "qattn_combine", "qattn_read_device_flags", "qattn_status_string", "qattn_last_error",
     "qattn_version", "qattn_decode_noalloc", "qattn_check_wait_timeout", "qattn_decode_append",
     "qattn_flashq_init", "qattn_flashq_append", "qattn_flashq_attend", "qattn_flashq_flush",
-    "qattn_headwise_plan",
+    "qattn_headwise_plan", "qattn_dequantize_kv", "qattn_decode_fp16_workspace_size", "qattn_decode_fp16",
+    "qattn_prefill_fp16",
 )
 
 
@@ -117,6 +120,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qattn_flashq_attend": (i32, [vp, ctypes.POINTER(FlashqBufferStruct), i32, i32, f32, vp, vp, vp]),
         "qattn_flashq_flush": (i32, [ctypes.POINTER(FlashqBufferStruct), cache_p, vp, i32, vp]),
         "qattn_headwise_plan": (i32, [vp, vp, i32, i32, i32, i32, i32, vp, i32, vp, vp, vp]),
+        "qattn_dequantize_kv": (i32, [cache_p, i32, i32, vp, vp, vp]),
+        "qattn_decode_fp16_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
+        "qattn_decode_fp16": (i32, [vp, vp, vp, i32, i32, i32, i32, i64, vp, i32, f32, i32, vp, sz, vp, vp, vp]),
+        "qattn_prefill_fp16": (i32, [vp, vp, vp, i32, i32, i32, i32, i64, i32, i32, f32, i32, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -373,6 +380,69 @@ def prefill(q: torch.Tensor, cache: KvCache, nk: int, softmax_scale: float, caus
     _check(load_library().qattn_prefill(_ptr(q), ctypes.byref(st), B, Hq, Nq, nk, float(softmax_scale),
                                         int(bool(causal)), _ptr(out), _ptr(lse), _stream(q.device)),
            "qattn_prefill")
+    return (out, lse) if return_lse else out
+
+
+# ------------------------------------------------------------ comparison paths
+# An FP16 KV cache attended directly, and the INT4 cache dequantized to FP16
+# in HBM first ("Quantized Cross-Attention ... In-SRAM Dequantization" §5.2):
+# the arms the fused kernels are measured against.
+
+def dequantize_kv(cache: KvCache, batch: int, n: int, k_out: Optional[torch.Tensor] = None,
+                  v_out: Optional[torch.Tensor] = None):
+    """The first n tokens of an INT4 cache as fp16 K, V [batch, Hkv, n, D] (fl16(c * s))."""
+    shape = (batch, cache.num_kv_heads, n, cache.head_dim)
+    dev = cache.k_codes.device
+    k_out = torch.empty(shape, dtype=torch.float16, device=dev) if k_out is None else k_out
+    v_out = torch.empty(shape, dtype=torch.float16, device=dev) if v_out is None else v_out
+    st = cache.struct()
+    _check(load_library().qattn_dequantize_kv(ctypes.byref(st), batch, n, _ptr(k_out), _ptr(v_out), _stream(dev)),
+           "qattn_dequantize_kv")
+    return k_out, v_out
+
+
+def decode_fp16_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len, num_splits=0) -> int:
+    return int(load_library().qattn_decode_fp16_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
+                                                               max_seq_len, num_splits))
+
+
+def decode_fp16(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, seq_lens: torch.Tensor, max_seq_len: int,
+                softmax_scale: float, num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
+                out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None, return_lse: bool = False):
+    """q [B, Hq, D] fp16 against an fp16 cache k, v [B, Hkv, capacity, D] -> out [B, Hq, D] fp16."""
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    B, Hq, D = q.shape
+    Hkv, cap = k.shape[1], k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        need = decode_fp16_workspace_size(B, Hq, Hkv, D, max_seq_len, num_splits)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    sl = seq_lens.to(device=q.device, dtype=torch.int32).contiguous()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load_library().qattn_decode_fp16(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, D, cap, _ptr(sl), max_seq_len,
+                                            float(softmax_scale), num_splits, _ptr(workspace), ws_bytes, _ptr(out),
+                                            _ptr(lse), _stream(q.device)), "qattn_decode_fp16")
+    return (out, lse) if return_lse else out
+
+
+def prefill_fp16(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, nk: int, softmax_scale: float,
+                 causal: bool = True, out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                 return_lse: bool = False):
+    """q [B, Hq, Nq, D] fp16 against the first nk keys of k, v [B, Hkv, capacity, D] fp16."""
+    q, k, v = q.contiguous(), k.contiguous(), v.contiguous()
+    B, Hq, Nq, D = q.shape
+    Hkv, cap = k.shape[1], k.shape[2]
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(B, Hq, Nq, dtype=torch.float32, device=q.device)
+    _check(load_library().qattn_prefill_fp16(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, D, cap, Nq, nk,
+                                             float(softmax_scale), int(bool(causal)), _ptr(out), _ptr(lse),
+                                             _stream(q.device)), "qattn_prefill_fp16")
     return (out, lse) if return_lse else out
 
 

@@ -247,7 +247,7 @@ qattn_status qattn_quantize_kv(const void *k, const void *v, qattn_dtype x_dtype
   if (!aligned16(k) || !aligned16(v)) return fail(QATTN_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
   DeviceState *ds;
   if ((st = device_state(&ds)) != QATTN_OK) return st;
-  cudaError_t e = launch_quantize(k, v, x_dtype == QATTN_F16, batch, n, start_pos, view, ds->status,
+  cudaError_t e = launch_quantize(k, v, x_dtype == QATTN_F16, batch, n, start_pos, view, ds->status, ds->sms,
                                   reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "quantize launch");
 }
@@ -575,6 +575,172 @@ const char *qattn_status_string(qattn_status status) {
 }
 
 const char *qattn_last_error(void) { return t_last_error; }
+
+// ------------------------------------------------------ comparison paths
+
+qattn_status qattn_dequantize_kv(const qattn_kv_cache *cache, int32_t batch, int32_t n, uint16_t *k_out,
+                                 uint16_t *v_out, qattn_stream_t stream) {
+  if (batch < 0 || n < 0) return fail(QATTN_ERR_INVALID_ARG, "batch %d, n %d", batch, n);
+  KvView view;
+  uint64_t code_bytes = 0;
+  qattn_status st = check_cache(cache, batch, &view, &code_bytes);
+  if (st != QATTN_OK) return st;
+  if (view.bits != 4) return fail(QATTN_ERR_UNSUPPORTED, "qattn_dequantize_kv on an INT%d cache", view.bits);
+  if (view.head_map) return fail(QATTN_ERR_UNSUPPORTED, "qattn_dequantize_kv with kv_head_index");
+  const int64_t limit = view.page_table ? static_cast<int64_t>(view.max_pages) * kPage : view.capacity;
+  if (n > limit) return fail(QATTN_ERR_INVALID_ARG, "n %d exceeds the cache's %lld tokens", n, (long long)limit);
+  if (batch == 0 || n == 0) return QATTN_OK;
+  if (!k_out || !v_out) return fail(QATTN_ERR_INVALID_ARG, "k_out or v_out is NULL");
+  if (!aligned16(k_out) || !aligned16(v_out)) return fail(QATTN_ERR_INVALID_ARG, "k_out and v_out must be 16-byte aligned");
+  DeviceState *ds;
+  if ((st = device_state(&ds)) != QATTN_OK) return st;
+  cudaError_t e = launch_dequantize(view, batch, n, k_out, v_out, ds->status, ds->sms,
+                                    reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "dequantize launch");
+}
+
+}  // extern "C"
+
+namespace qattn {
+namespace {
+
+// Key ranges of an fp16 decode: the requested count, or one CTA per SM over
+// all (sequence, kv-head) pairs; ranges of a multiple of 64 tokens.
+void decode16_plan(int batch, int hkv, int max_len, int requested, int sms, int *splits, int *chunk) {
+  const int64_t tiles = (static_cast<int64_t>(max_len) + 63) / 64;
+  int64_t n = requested > 0 ? requested : max(1, sms / max(1, batch * hkv));
+  n = min(n, max(tiles, static_cast<int64_t>(1)));
+  n = min(n, static_cast<int64_t>(QATTN_MAX_SPLITS));
+  const int64_t per = (tiles + n - 1) / n;  // tiles per range
+  *chunk = static_cast<int>(max(per, static_cast<int64_t>(1)) * 64);
+  *splits = static_cast<int>(max(static_cast<int64_t>(1), (static_cast<int64_t>(max_len) + *chunk - 1) / *chunk));
+}
+
+size_t decode16_workspace(int batch, int hq, int head_dim, int splits) {
+  if (splits <= 1) return 0;
+  const size_t rows = static_cast<size_t>(splits) * batch * hq;
+  return (rows * head_dim * 4 + 255) / 256 * 256 + rows * 4;
+}
+
+// An fp16 cache [heads][capacity][D] read as 3-D [heads][extent][D] (tokens
+// at or past `extent` read as zero), boxes of 64 columns x box_tokens.
+qattn_status fp16_cache_map(CUtensorMap *m, const void *base, int64_t heads, int64_t capacity, int64_t extent,
+                            int head_dim, int box_tokens) {
+  EncodeFn enc = encode_fn();
+  if (!enc) return fail(QATTN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(extent),
+                        static_cast<cuuint64_t>(heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2, static_cast<cuuint64_t>(capacity) * head_dim * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_tokens), 1}, es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(QATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for an fp16 cache", (int)r);
+  return QATTN_OK;
+}
+
+}  // namespace
+}  // namespace qattn
+
+extern "C" {
+
+size_t qattn_decode_fp16_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                        int32_t max_seq_len, int32_t num_splits) {
+  if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads ||
+      num_q_heads / num_kv_heads > QATTN_MAX_GROUP || max_seq_len < 0 || num_splits < 0 ||
+      num_splits > QATTN_MAX_SPLITS || (head_dim != 64 && head_dim != 128))
+    return 0;
+  int sms = 152;
+  if (num_splits == 0) {
+    DeviceState *ds = nullptr;
+    if (device_state(&ds) == QATTN_OK && ds->sms > 0)
+      sms = ds->sms;
+    else
+      cudaGetLastError();
+  }
+  int splits = 1, chunk = 64;
+  decode16_plan(batch, num_kv_heads, max_seq_len, num_splits, sms, &splits, &chunk);
+  return decode16_workspace(batch, num_q_heads, head_dim, splits);
+}
+
+qattn_status qattn_decode_fp16(const uint16_t *q, const uint16_t *k, const uint16_t *v, int32_t batch,
+                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int64_t capacity,
+                               const int32_t *seq_lens, int32_t max_seq_len, float softmax_scale, int32_t num_splits,
+                               void *workspace, size_t workspace_bytes, uint16_t *out, float *lse,
+                               qattn_stream_t stream) {
+  if (batch < 0 || batch > QATTN_MAX_BATCH || num_q_heads <= 0 || num_kv_heads <= 0 || max_seq_len < 0)
+    return fail(QATTN_ERR_INVALID_ARG, "batch %d, Hq %d, Hkv %d, max_seq_len %d", batch, num_q_heads, num_kv_heads,
+                max_seq_len);
+  if (num_q_heads % num_kv_heads) return fail(QATTN_ERR_INVALID_ARG, "Hq %d is not a multiple of Hkv %d", num_q_heads, num_kv_heads);
+  if (num_q_heads / num_kv_heads > QATTN_MAX_GROUP)
+    return fail(QATTN_ERR_UNSUPPORTED, "group size %d > %d", num_q_heads / num_kv_heads, QATTN_MAX_GROUP);
+  if (head_dim != 64 && head_dim != 128) return fail(QATTN_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", head_dim);
+  if (capacity <= 0 || capacity > 0x7fffffffLL) return fail(QATTN_ERR_INVALID_ARG, "capacity %lld", (long long)capacity);
+  if (num_splits < 0 || num_splits > QATTN_MAX_SPLITS)
+    return fail(QATTN_ERR_INVALID_ARG, "num_splits %d (0..%d)", num_splits, QATTN_MAX_SPLITS);
+  if (batch == 0) return QATTN_OK;
+  if (!q || !k || !v || !seq_lens || !out) return fail(QATTN_ERR_INVALID_ARG, "q, k, v, seq_lens or out is NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(QATTN_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
+  if (static_cast<int64_t>(batch) * num_kv_heads > 65535)
+    return fail(QATTN_ERR_UNSUPPORTED, "batch * Hkv %d > 65535", batch * num_kv_heads);
+  DeviceState *ds;
+  qattn_status st = device_state(&ds);
+  if (st != QATTN_OK) return st;
+  Decode16Args a;
+  decode16_plan(batch, num_kv_heads, max_seq_len, num_splits, ds->sms, &a.splits, &a.chunk);
+  const size_t need = decode16_workspace(batch, num_q_heads, head_dim, a.splits);
+  if (need && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+    return fail(QATTN_ERR_WORKSPACE, "workspace of %zu bytes (16-byte aligned) needed, %zu given", need,
+                workspace ? workspace_bytes : (size_t)0);
+  CUtensorMap kmap, vmap;
+  const int64_t heads = static_cast<int64_t>(batch) * num_kv_heads;
+  if ((st = fp16_cache_map(&kmap, k, heads, capacity, capacity, head_dim, 64)) != QATTN_OK) return st;
+  if ((st = fp16_cache_map(&vmap, v, heads, capacity, capacity, head_dim, 64)) != QATTN_OK) return st;
+  a.q = q, a.seq_lens = seq_lens, a.out = out, a.lse = lse;
+  a.partial_o = static_cast<float *>(workspace);
+  const size_t rows = static_cast<size_t>(a.splits) * batch * num_q_heads;
+  a.partial_lse = need ? reinterpret_cast<float *>(static_cast<char *>(workspace) + (rows * head_dim * 4 + 255) / 256 * 256)
+                       : nullptr;
+  a.batch = batch, a.hq = num_q_heads, a.hkv = num_kv_heads, a.head_dim = head_dim;
+  a.capacity = capacity;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  cudaError_t e = launch_decode16(a, kmap, vmap, ds->status, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "fp16 decode launch");
+}
+
+qattn_status qattn_prefill_fp16(const uint16_t *q, const uint16_t *k, const uint16_t *v, int32_t batch,
+                                int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int64_t capacity,
+                                int32_t nq, int32_t nk, float softmax_scale, int32_t causal, uint16_t *out,
+                                float *lse, qattn_stream_t stream) {
+  if (batch < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || nq < 0 || nk < 0 || (causal != 0 && causal != 1))
+    return fail(QATTN_ERR_INVALID_ARG, "batch %d, Hq %d, Hkv %d, nq %d, nk %d, causal %d", batch, num_q_heads,
+                num_kv_heads, nq, nk, causal);
+  if (num_q_heads % num_kv_heads) return fail(QATTN_ERR_INVALID_ARG, "Hq %d is not a multiple of Hkv %d", num_q_heads, num_kv_heads);
+  if (head_dim != 64 && head_dim != 128) return fail(QATTN_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", head_dim);
+  if (nq > nk) return fail(QATTN_ERR_INVALID_ARG, "nq %d > nk %d", nq, nk);
+  if (nk > capacity || capacity > 0x7fffffffLL)
+    return fail(QATTN_ERR_INVALID_ARG, "nk %d, capacity %lld", nk, (long long)capacity);
+  if (batch == 0 || nq == 0) return QATTN_OK;
+  if (!q || !k || !v || !out) return fail(QATTN_ERR_INVALID_ARG, "q, k, v or out is NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return fail(QATTN_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
+  DeviceState *ds;
+  qattn_status st = device_state(&ds);
+  if (st != QATTN_OK) return st;
+  CUtensorMap qmap, omap, kmap, vmap;
+  if ((st = prefill_maps(&qmap, &omap, q, out, batch, num_q_heads, nq, head_dim)) != QATTN_OK) return st;
+  const int64_t heads = static_cast<int64_t>(batch) * num_kv_heads;
+  if ((st = fp16_cache_map(&kmap, k, heads, capacity, nk, head_dim, 128)) != QATTN_OK) return st;
+  if ((st = fp16_cache_map(&vmap, v, heads, capacity, nk, head_dim, 128)) != QATTN_OK) return st;
+  PrefillArgs a;
+  a.q = q, a.out = out, a.lse = lse;
+  a.batch = batch, a.hq = num_q_heads, a.nq = nq, a.nk = nk, a.causal = causal;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  cudaError_t e = launch_prefill16(a, num_kv_heads, head_dim, qmap, omap, kmap, vmap, ds->status,
+                                   reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "fp16 prefill launch");
+}
 
 int32_t qattn_version(void) { return 0x000100; }
 

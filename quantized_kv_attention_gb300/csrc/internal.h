@@ -41,8 +41,9 @@ __device__ __forceinline__ int model_head(const int32_t *head_map, int model_hkv
 }
 
 // quantize.cu
+// (a persistent grid of four CTAs per SM: `sms` = the device's SM count)
 cudaError_t launch_quantize(const void *k, const void *v, bool fp16_in, int batch, int n,
-                            const int32_t *start_pos, const KvView &cache, uint32_t *err,
+                            const int32_t *start_pos, const KvView &cache, uint32_t *err, int sms,
                             cudaStream_t stream);
 
 // decode.cu: persistent split-KV decode over `ctas` balanced key ranges plus
@@ -124,6 +125,32 @@ struct PrefillArgs {
 // x 128 rows (Q) and x 32 rows (O).
 cudaError_t launch_prefill(const PrefillArgs &a, const KvView &cache, const CUtensorMap &qmap,
                            const CUtensorMap &omap, uint32_t *err, cudaStream_t stream);
+// prefill over an fp16 cache (comparison path): kmap / vmap 3-D
+// [batch*Hkv][nk][D] fp16, 128B swizzle, boxes of 64 columns x 128 keys.
+cudaError_t launch_prefill16(const PrefillArgs &a, int hkv, int head_dim, const CUtensorMap &qmap,
+                             const CUtensorMap &omap, const CUtensorMap &kmap, const CUtensorMap &vmap, uint32_t *err,
+                             cudaStream_t stream);
+
+// fp16kv.cu: the comparison paths.  dequantize: the first n tokens of every
+// (sequence, kv-head) of an INT4 cache -> fp16 [batch, Hkv, n, D] (K and V).
+cudaError_t launch_dequantize(const KvView &cache, int batch, int n, uint16_t *k_out, uint16_t *v_out, uint32_t *err,
+                              int sms, cudaStream_t stream);
+// decode over an fp16 cache [batch, Hkv, capacity, D] (kmap, vmap: 3-D
+// [batch*Hkv][capacity][D], 128B swizzle, boxes of 64 columns x 64 tokens);
+// `splits` key ranges of `chunk` tokens; partials [splits, batch*Hq, D] and
+// [splits, batch*Hq] fp32 when splits > 1, merged by the combine kernel.
+struct Decode16Args {
+  const uint16_t *q;
+  const int32_t *seq_lens;
+  uint16_t *out;
+  float *lse;
+  float *partial_o, *partial_lse;
+  int batch, hq, hkv, head_dim, splits, chunk;
+  int64_t capacity;
+  float scale_log2;
+};
+cudaError_t launch_decode16(const Decode16Args &a, const CUtensorMap &kmap, const CUtensorMap &vmap, uint32_t *err,
+                            cudaStream_t stream);
 
 // api.cu: sets the message returned by qattn_last_error() on this thread.
 void record_error(const char *msg);

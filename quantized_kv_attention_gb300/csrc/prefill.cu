@@ -245,10 +245,17 @@ __device__ __forceinline__ float chunk_exp(const uint32_t (&s)[32], uint32_t kf,
   return t2.x + t2.y;
 }
 
-template <int D>
+// KV16: K and V come from an fp16 cache (the comparison path of "Quantized
+// Cross-Attention ... In-SRAM Dequantization" §5.2) through kmap / vmap (3-D
+// [batch*Hkv][nk][D], 128B swizzle, boxes of 64 columns x 128 keys): one
+// thread of warpgroup 2 loads each tile by TMA into the same swizzled operand
+// layout the dequantization writes, the per-key factor is the softmax scale,
+// and Q and O keep the natural column order.
+template <int D, bool KV16>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(PrefillArgs a, KvView cache, const __grid_constant__ CUtensorMap qmap,
-                      const __grid_constant__ CUtensorMap omap, uint32_t *err) {
+                      const __grid_constant__ CUtensorMap omap, const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap vmap, uint32_t *err) {
   using C = TcCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -264,8 +271,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(&bars->q_full), 1);
     for (int i = 0; i < kKvBufs; ++i) {
-      mbar_init(smem_u32(&bars->k_full[i]), kDequantThreads);
-      mbar_init(smem_u32(&bars->v_full[i]), kDequantThreads);
+      mbar_init(smem_u32(&bars->k_full[i]), KV16 ? 1 : kDequantThreads);
+      mbar_init(smem_u32(&bars->v_full[i]), KV16 ? 1 : kDequantThreads);
       mbar_init(smem_u32(&bars->k_empty[i]), 1);
       mbar_init(smem_u32(&bars->v_empty[i]), 1);
     }
@@ -306,7 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Q columns into the K operand's order (d0 d4 d1 d5 d2 d6 d3 d7 per group of 8)
     const bool qok = wait_bounded(qf, 0, err);
-    if (qok) {
+    if (qok && !KV16) {
       for (int ch = threadIdx.x - 3 * 128; ch < 2 * C::kTileBytes / 16; ch += 128) {
         const uint32_t addr = sbase + C::kQOff + ch * 16;
         uint4 v = lds128(addr);
@@ -389,6 +396,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsDequant));
     // ---------------------------------------------------- dequantization
     const int tok_l = threadIdx.x - kSoftmaxThreads;  // token within the tile
+    if constexpr (KV16) {
+      const int64_t head = static_cast<int64_t>(w.b) * cache.hkv + w.kvh;
+      if (tok_l == 0) {
+        prefetch_tmap(&kmap);
+        prefetch_tmap(&vmap);
+      }
+      for (int j = 0; j < n; ++j) {
+        const int buf = j % kKvBufs;
+        const uint32_t par = ((j / kKvBufs) & 1) ^ 1;
+        if (tok_l == 0) {
+          if (j >= kKvBufs && !wait_bounded(smem_u32(&bars->k_empty[buf]), par, err)) break;
+          const uint32_t kf = smem_u32(&bars->k_full[buf]);
+          mbar_arrive_expect_tx(kf, C::kTileBytes);
+          for (int sub = 0; sub < C::kSub; ++sub)
+            tma_load_3d(sbase + C::kKOff + buf * C::kTileBytes + sub * C::kSubBytes, &kmap, 64 * sub, j * kBN,
+                        static_cast<int32_t>(head), kf);
+        }
+        const int slot = j % kScaleSlots;
+        if (j >= kScaleSlots &&
+            !wait_bounded(smem_u32(&bars->sc_empty[slot]), ((j / kScaleSlots) & 1) ^ 1, err))
+          break;
+        scales[slot * kBN + tok_l] = j * kBN + tok_l < a.nk ? a.scale_log2 : 0.f;
+        mbar_arrive(smem_u32(&bars->sc_full[slot]));
+        if (tok_l == 0) {
+          if (j >= kKvBufs && !wait_bounded(smem_u32(&bars->v_empty[buf]), par, err)) break;
+          const uint32_t vf = smem_u32(&bars->v_full[buf]);
+          mbar_arrive_expect_tx(vf, C::kTileBytes);
+          for (int sub = 0; sub < C::kSub; ++sub)
+            tma_load_3d(sbase + C::kVOff + buf * C::kTileBytes + sub * C::kSubBytes, &vmap, 64 * sub, j * kBN,
+                        static_cast<int32_t>(head), vf);
+        }
+      }
+    } else {
     // Cache row of token `tok` of this (sequence, kv-head): contiguous
     // [B, Hkv, capacity] or, through the page table, [pages, Hkv, 64];
     // -1 for a token in a missing page (flagged; its codes read as zero).
@@ -441,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       store_row<D, true>(sbase + C::kVOff + buf * C::kTileBytes, tok_l, cv, sv);
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&bars->v_full[buf]));
+    }
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
@@ -525,11 +566,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 4; ++q) {
           const int chunk = c * 4 + q;
           const uint32_t sub = chunk / 8, col = chunk % 8;
-          // column 8q+p of O holds d = 8q + (0 4 1 5 2 6 3 7)[p]
-          const uint32_t h0 = pack_half2(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + 2]) * inv);
-          const uint32_t h1 = pack_half2(__uint_as_float(o[8 * q + 4]) * inv, __uint_as_float(o[8 * q + 6]) * inv);
-          const uint32_t h2 = pack_half2(__uint_as_float(o[8 * q + 1]) * inv, __uint_as_float(o[8 * q + 3]) * inv);
-          const uint32_t h3 = pack_half2(__uint_as_float(o[8 * q + 5]) * inv, __uint_as_float(o[8 * q + 7]) * inv);
+          // INT4: column 8q+p of O holds d = 8q + (0 4 1 5 2 6 3 7)[p]; KV16: d = 8q + p
+          constexpr int e1 = KV16 ? 1 : 2, e2 = KV16 ? 2 : 4, e3 = KV16 ? 3 : 6, e4 = KV16 ? 4 : 1;
+          constexpr int e5 = KV16 ? 5 : 3, e6 = KV16 ? 6 : 5, e7 = 7;
+          const uint32_t h0 = pack_half2(__uint_as_float(o[8 * q + 0]) * inv, __uint_as_float(o[8 * q + e1]) * inv);
+          const uint32_t h1 = pack_half2(__uint_as_float(o[8 * q + e2]) * inv, __uint_as_float(o[8 * q + e3]) * inv);
+          const uint32_t h2 = pack_half2(__uint_as_float(o[8 * q + e4]) * inv, __uint_as_float(o[8 * q + e5]) * inv);
+          const uint32_t h3 = pack_half2(__uint_as_float(o[8 * q + e6]) * inv, __uint_as_float(o[8 * q + e7]) * inv);
           const uint32_t dst = stage + sub * C::kSubBytes + row_l * 128 + ((col ^ (row_l & 7)) << 4);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(h0), "r"(h1), "r"(h2), "r"(h3)
                        : "memory");
@@ -560,13 +603,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
-cudaError_t launch_tc(const PrefillArgs &a, const KvView &cache, const CUtensorMap &qmap,
-                      const CUtensorMap &omap, uint32_t *err, cudaStream_t stream) {
+template <int D, bool KV16>
+cudaError_t launch_tc(const PrefillArgs &a, const KvView &cache, const CUtensorMap &qmap, const CUtensorMap &omap,
+                      const CUtensorMap &kmap, const CUtensorMap &vmap, uint32_t *err, cudaStream_t stream) {
   using C = TcCfg<D>;
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<D, KV16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          C::kSmem);
     if (e != cudaSuccess) return e;
     configured = true;
@@ -576,7 +619,8 @@ cudaError_t launch_tc(const PrefillArgs &a, const KvView &cache, const CUtensorM
   const int64_t items = (G % 2 == 0) ? static_cast<int64_t>(a.batch) * cache.hkv * (G / 2) * nqb
                                      : static_cast<int64_t>(a.batch) * a.hq * ((nqb + 1) / 2);
   if (items > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  prefill_tc_kernel<D><<<static_cast<unsigned>(items), kThreads, C::kSmem, stream>>>(a, cache, qmap, omap, err);
+  prefill_tc_kernel<D, KV16><<<static_cast<unsigned>(items), kThreads, C::kSmem, stream>>>(a, cache, qmap, omap, kmap,
+                                                                                           vmap, err);
   return cudaGetLastError();
 }
 
@@ -585,8 +629,18 @@ cudaError_t launch_tc(const PrefillArgs &a, const KvView &cache, const CUtensorM
 cudaError_t launch_prefill(const PrefillArgs &a, const KvView &cache, const CUtensorMap &qmap,
                            const CUtensorMap &omap, uint32_t *err, cudaStream_t stream) {
   if (a.batch == 0 || a.nq == 0) return cudaSuccess;
-  return cache.head_dim == 128 ? launch_tc<128>(a, cache, qmap, omap, err, stream)
-                               : launch_tc<64>(a, cache, qmap, omap, err, stream);
+  return cache.head_dim == 128 ? launch_tc<128, false>(a, cache, qmap, omap, qmap, qmap, err, stream)
+                               : launch_tc<64, false>(a, cache, qmap, omap, qmap, qmap, err, stream);
+}
+
+cudaError_t launch_prefill16(const PrefillArgs &a, int hkv, int head_dim, const CUtensorMap &qmap,
+                             const CUtensorMap &omap, const CUtensorMap &kmap, const CUtensorMap &vmap, uint32_t *err,
+                             cudaStream_t stream) {
+  if (a.batch == 0 || a.nq == 0) return cudaSuccess;
+  KvView cache = {};
+  cache.hkv = hkv, cache.model_hkv = hkv, cache.head_dim = head_dim, cache.bits = 16;
+  return head_dim == 128 ? launch_tc<128, true>(a, cache, qmap, omap, kmap, vmap, err, stream)
+                         : launch_tc<64, true>(a, cache, qmap, omap, kmap, vmap, err, stream);
 }
 
 }  // namespace qattn

@@ -94,6 +94,49 @@ __device__ __forceinline__ __half quantize_vals_warp(const float (&x)[D / 32], u
   return hs;
 }
 
+// quantize_vals_warp for N rows at once (the same arithmetic, so the same
+// bits), phase by phase across the rows so that their shuffle reductions and
+// divisions overlap; a row whose dst_codes is null is computed but not stored.
+template <int D, int N>
+__device__ __forceinline__ void quantize_vals_warp_n(const float (&x)[N][D / 32], uint8_t *const (&dst_codes)[N],
+                                                     uint16_t *const (&dst_scale)[N], int lane) {
+  constexpr int VPL = D / 32;
+  float am[N];
+#pragma unroll
+  for (int r = 0; r < N; ++r) {
+    am[r] = 0.f;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) am[r] = fmaxf(am[r], fabsf(x[r][j]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int r = 0; r < N; ++r) am[r] = fmaxf(am[r], __shfl_xor_sync(0xffffffffu, am[r], o));
+  __half hs[N];
+#pragma unroll
+  for (int r = 0; r < N; ++r) {
+    hs[r] = __float2half_rn(__fdiv_rn(am[r], 7.0f));
+    if (__hisinf(hs[r])) hs[r] = __ushort_as_half(0x7BFF);
+  }
+#pragma unroll
+  for (int r = 0; r < N; ++r) {
+    const float s = __half2float(hs[r]);
+    uint32_t packed = 0;
+    if (s > 0.f) {
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) packed |= static_cast<uint32_t>(code_of(x[r][j], s) & 0xF) << (4 * j);
+    }
+    if (dst_codes[r] != nullptr) {
+      uint8_t *dst = dst_codes[r] + lane * (VPL / 2);
+      if constexpr (VPL == 4)
+        *reinterpret_cast<uint16_t *>(dst) = static_cast<uint16_t>(packed);
+      else
+        *dst = static_cast<uint8_t>(packed);
+      if (lane == 0) *dst_scale[r] = __half_as_ushort(hs[r]);
+    }
+  }
+}
+
 // quantize_vals_warp of row `src` (D values of type T, lane i reading its
 // elements as above).
 template <typename T, int D>
@@ -117,11 +160,8 @@ __device__ __forceinline__ int code_of3(float x, float s) {
   return x < 0.f ? -m : m;
 }
 
-template <typename T>
-__device__ __forceinline__ void quantize_row3_warp(const T *src, uint32_t *dst_words, uint16_t *dst_scale,
-                                                   int lane) {
-  float x[4];
-  RowLoad<T, 4>::load(src + lane * 4, x);
+__device__ __forceinline__ void quantize_vals3_warp(const float (&x)[4], uint32_t *dst_words, uint16_t *dst_scale,
+                                                    int lane) {
   float am = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
@@ -151,11 +191,8 @@ __device__ __forceinline__ void quantize_row3_warp(const T *src, uint32_t *dst_w
 // element j goes to word j / 16 at bits 2 (j % 16) as a 2-bit two's-
 // complement field.  Lane i holds elements 4i..4i+3, one byte of word i / 4;
 // lanes 4k gather the four bytes of word k by shuffles and store it.
-template <typename T>
-__device__ __forceinline__ void quantize_row2_warp(const T *src, uint32_t *dst_words, uint16_t *dst_scale,
-                                                   int lane) {
-  float x[4];
-  RowLoad<T, 4>::load(src + lane * 4, x);
+__device__ __forceinline__ void quantize_vals2_warp(const float (&x)[4], uint32_t *dst_words, uint16_t *dst_scale,
+                                                    int lane) {
   float am = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
