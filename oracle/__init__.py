@@ -18,6 +18,9 @@ headwise   -- headwise mixed 2/4-bit precision: priorities and the bit plan.
 flashq     -- the int8 decode buffer with a universal scale, and its flush.
 baselines  -- the comparison paths: attention over an FP16 cache, and the
               cache dequantized to FP16 first, then attended.
+progressive -- progressive INT8 -> INT4 storage: 64-token blocks, symmetric
+              int8 with one FP16 scale, then channel-wise asymmetric 4-bit
+              codes with an integer scale and zero point per channel.
 
 Every function cites the passage of the source pages it follows.  Where the
 pages are silent or garbled the reading taken is stated in the docstring.
