@@ -856,6 +856,66 @@ def run_quantize(name, args, device, gpu_index, rank):
     return res
 
 
+def run_decode_pq(name, args, device, gpu_index, rank):
+    """A contiguous decode workload's shape over a progressive cache
+    (qattn_pq_quantize blocks of 64 tokens, qattn_decode_pq): per (token,
+    kv-head) and tensor D/2 code bytes, per 64-token block and tensor a
+    2D + 16 byte record.  A step is one qattn_decode_pq call (its blocks are
+    appended 64 tokens at a time, not per step); CUDA graphs of the API call,
+    rotating cache copies larger than 4x L2."""
+    import torch
+    import quantized_kv_attention_gb300 as qa
+    from quantized_kv_attention_gb300 import workloads as wl
+    cfg = dict(wl.WORKLOADS[name])
+    B, Hq, Hkv, D, Nk = cfg["B"], cfg["Hq"], cfg["Hkv"], cfg["D"], cfg["Nk"]
+    scale = 1.0 / math.sqrt(D)
+    kv_bytes = 2 * B * Hkv * (Nk * D // 2 + (Nk // 64) * (2 * D + 16))
+    copies = max(1, math.ceil(4 * _l2_bytes(torch, device) / kv_bytes))
+    g = torch.Generator(device=device)
+    g.manual_seed(cfg["seed"] + 1000 * rank + 5)
+    caches = []
+    for _ in range(copies):
+        c = qa.PqCache.contiguous(B, Hkv, Nk, D, device=device)
+        for b in range(B):
+            sub = qa.PqCache(c.k_codes[b:b + 1], c.v_codes[b:b + 1], c.k_params[b:b + 1], c.v_params[b:b + 1], D, Hkv,
+                             c.capacity)
+            qa.pq_quantize(torch.randn(1, Hkv, Nk, D, device=device, generator=g),
+                           torch.randn(1, Hkv, Nk, D, device=device, generator=g), sub)
+        caches.append(c)
+    torch.cuda.synchronize()
+    sl = torch.full((B,), Nk, dtype=torch.int32, device=device)
+    q = torch.randn(B, Hq, D, device=device, generator=g).half()
+    out = torch.empty(B, Hq, D, dtype=torch.float16, device=device)
+    ws = torch.empty(max(qa.decode_pq_workspace_size(B, Hq, Hkv, D, Nk, 0), 16), dtype=torch.uint8, device=device)
+
+    def enqueue(n):
+        for i in range(n):
+            qa.decode_pq(q, caches[i % copies], sl, Nk, scale, 0, workspace=ws, out=out)
+
+    enqueue(max(args.warmup, 1))
+    torch.cuda.synchronize()
+    inner = max(copies, 64 // copies * copies)
+    total_ms, one_ms, clocks = _timed_graphs(torch, args.steps, enqueue, enqueue, inner, gpu_index, period=copies,
+                                             soak_s=min(args.soak, 0.5))
+    value, tmax, world = aggregate(kv_bytes * args.steps / 1e9, total_ms / 1e3, device)
+    peaks, pk_src = measured_peaks()
+    achieved = kv_bytes / (one_ms / 1e3) / 1e9
+    res = {
+        "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(tmax * 1e3 / args.steps, 5), "steps": args.steps,
+        "config": {"workload": f"{name}_pq", "B": B, "Hq": Hq, "Hkv": Hkv, "D": D, "Nk": Nk, "softmax_scale": scale,
+                   "kv_bytes_per_step": kv_bytes, "l2": "rotating KV-cache copies totalling more than 4x L2",
+                   "step": "split-KV decode over progressive INT8 -> INT4 blocks (one qattn_decode_pq call)"},
+        "setup": {"cache_copies": copies, "parallelism": f"replicas x{world}", "timing": "CUDA graphs of the API call"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None, "kernel": "decode_pq + combine",
+                     "peak_source": pk_src, "us_per_launch": round(one_ms * 1e3, 3)},
+        "clocks": clocks,
+    }
+    del caches
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_compare(name, args, device, gpu_index, rank):
     """The comparison arms of "Quantized Cross-Attention ... In-SRAM
     Dequantization" §5.2-§5.3 on a workload's shape: attention over an FP16
@@ -993,6 +1053,7 @@ def secondary_lines(args, device, gpu_index, rank):
     add("long_decode_flashq", lambda: run_decode_flashq("long_decode", args, device, gpu_index, rank))
     add("long_decode_int3", lambda: run_decode_lowbit("long_decode", args, device, gpu_index, rank, 3))
     add("long_decode_int2", lambda: run_decode_lowbit("long_decode", args, device, gpu_index, rank, 2))
+    add("long_decode_pq", lambda: run_decode_pq("long_decode", args, device, gpu_index, rank))
     add("causal_prefill", lambda: run_prefill("causal_prefill", args, device, gpu_index, rank,
                                               steps=min(args.steps, 50)))
     add("causal_prefill_quantize", lambda: run_quantize("causal_prefill", args, device, gpu_index, rank))
@@ -1005,7 +1066,7 @@ def secondary_lines(args, device, gpu_index, rank):
     return sec
 
 
-VARIANTS = ("_int3", "_int2", "_flashq", "_quantize", "_fp16", "_postdequant")
+VARIANTS = ("_int3", "_int2", "_flashq", "_quantize", "_fp16", "_postdequant", "_pq")
 
 
 def run_workload(name, args, device, gpu_index, rank):
@@ -1024,6 +1085,8 @@ def run_workload(name, args, device, gpu_index, rank):
         res = run_decode_flashq(base, args, device, gpu_index, rank)
     elif suffix == "_quantize":
         res = run_quantize(base, args, device, gpu_index, rank)
+    elif suffix == "_pq":
+        res = run_decode_pq(base, args, device, gpu_index, rank)
     elif suffix:
         res = run_compare(base, args, device, gpu_index, rank)[suffix[1:]]
     else:

@@ -475,6 +475,77 @@ qattn_status qattn_prefill_fp16(const uint16_t *q, const uint16_t *k, const uint
                                 int32_t nq, int32_t nk, float softmax_scale, int32_t causal, uint16_t *out,
                                 float *lse, qattn_stream_t stream);
 
+/*
+ * Progressive INT8 -> INT4 storage ([TA] §3.1 Blockwise Progressive
+ * Quantization; §3.3 compresses a full decode buffer this way).  The cache is
+ * kept in blocks of 64 tokens of one (sequence, kv-head) and tensor; the page
+ * gives no equations, and this library's reading is (every step exact):
+ *   s1  = fp16(fp32(absmax(block) / 127)), round-to-nearest-even twice,
+ *         saturating; q1 = clamp(RNE(x / s1), -127, 127), 0 when s1 == 0
+ *   per channel d of the block: lo = min q1, hi = max q1,
+ *   s2  = max(1, ceil((hi - lo) / 15)), z2 = lo,
+ *   q2  = RNE((q1 - lo) / s2) on the exact rational, 0..15
+ *   value x^ = (q2 * s2 + z2) * s1
+ *
+ *   k_codes, v_codes    [batch, Hkv, capacity, D/2] uint8: q2 as unsigned
+ *                       nibbles, element 2k in the low nibble of byte k
+ *   k_params, v_params  [batch, Hkv, capacity/64, 2*D + 16] uint8, one record
+ *                       per block: s2[D] (uint8), z2[D] (int8), s1 (fp16), 14
+ *                       zero bytes
+ *   capacity            tokens per (sequence, kv-head), a multiple of 64
+ * All four pointers 16-byte aligned.  D = 64 or 128.
+ */
+typedef struct qattn_pq_cache {
+  uint8_t *k_codes;
+  uint8_t *v_codes;
+  uint8_t *k_params;
+  uint8_t *v_params;
+  int32_t head_dim;
+  int32_t num_kv_heads;
+  int64_t capacity;
+} qattn_pq_cache;
+
+/*
+ * qattn_pq_quantize -- n new rows per (sequence, kv-head), n a multiple of
+ * 64, k and v [batch, Hkv, n, D] of x_dtype (fp32 or fp16), stored as n / 64
+ * blocks at block positions start_block[b] + i (device int32 [batch]; NULL
+ * means 0).  A block past the cache is not written and raises
+ * QATTN_FLAG_BAD_PAGE.  batch * Hkv <= 65535.
+ */
+qattn_status qattn_pq_quantize(const void *k, const void *v, qattn_dtype x_dtype, int32_t batch, int32_t n,
+                               const int32_t *start_block, const qattn_pq_cache *cache, qattn_stream_t stream);
+
+/* Workspace bytes of qattn_decode_pq (the same key ranges as qattn_decode_fp16). */
+size_t qattn_decode_pq_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t max_seq_len, int32_t num_splits);
+
+/*
+ * qattn_decode_pq -- qattn_decode over a progressive cache: q [batch, Hq,
+ * D] fp16, seq_lens [batch] int32 (device; whole blocks: a length that is
+ * not a multiple of 64 attends the block's leading tokens only), key ranges
+ * and workspace as qattn_decode_fp16, out [batch, Hq, D] fp16, lse [batch,
+ * Hq] fp32 or NULL.  Each block is dequantized on chip (INT4 -> the exact
+ * integer q1' in fp16 -> the MMA, s1 applied to the scores and to P); no
+ * fp16 copy of K or V is written to HBM.
+ */
+qattn_status qattn_decode_pq(const uint16_t *q, const qattn_pq_cache *cache, const int32_t *seq_lens, int32_t batch,
+                             int32_t num_q_heads, int32_t max_seq_len, float softmax_scale, int32_t num_splits,
+                             void *workspace, size_t workspace_bytes, uint16_t *out, float *lse, qattn_stream_t stream);
+
+/*
+ * qattn_flashq_flush_pq -- a full decode buffer ([TA] §3.3: once it holds 64
+ * rows it is compressed by progressive quantization) into one block of a
+ * progressive cache: its int8 codes are stage 1 already (s1 = the buffer's
+ * universal scale u), stage 2 runs on them, and the block goes to token
+ * position cache_lens[b] (device int32 [batch], a multiple of 64; otherwise,
+ * or past the cache, nothing is written and QATTN_FLAG_BAD_PAGE is raised).
+ * The buffer empties; its range R and scale u are kept (the universal range
+ * already bounds the block).  Buffers that are not full are untouched.  The
+ * buffer and the cache must have the same D and Hkv.
+ */
+qattn_status qattn_flashq_flush_pq(const qattn_flashq_buffer *buf, const qattn_pq_cache *cache,
+                                   const int32_t *cache_lens, int32_t batch, qattn_stream_t stream);
+
 /* Static description of a status code (never NULL). */
 const char *qattn_status_string(qattn_status status);
 

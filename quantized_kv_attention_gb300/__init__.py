@@ -10,6 +10,7 @@ stream.  The calls mirror the C ABI in include/qattn.h:
     combine(partial_o, partial_lse)                   log-sum-exp merge
     dequantize_kv, decode_fp16, prefill_fp16          the comparison paths (FP16 cache;
                                                       dequantize to FP16, then attend)
+    pq_quantize, decode_pq                            progressive INT8 -> INT4 blocks
 
 There is no fallback: if libqattn.so is missing or fails to load, every call
 raises.
@@ -42,7 +43,8 @@ EXPORTS = (
     "qattn_version", "qattn_decode_noalloc", "qattn_check_wait_timeout", "qattn_decode_append",
     "qattn_flashq_init", "qattn_flashq_append", "qattn_flashq_attend", "qattn_flashq_flush",
     "qattn_headwise_plan", "qattn_dequantize_kv", "qattn_decode_fp16_workspace_size", "qattn_decode_fp16",
-    "qattn_prefill_fp16",
+    "qattn_prefill_fp16", "qattn_pq_quantize", "qattn_decode_pq_workspace_size", "qattn_decode_pq",
+    "qattn_flashq_flush_pq",
 )
 
 
@@ -71,6 +73,19 @@ class KvCacheStruct(ctypes.Structure):
         ("code_bits", ctypes.c_int32),
         ("kv_head_index", ctypes.c_void_p),
         ("model_kv_heads", ctypes.c_int32),
+    ]
+
+
+class PqCacheStruct(ctypes.Structure):
+    """Layout of ``qattn_pq_cache``."""
+    _fields_ = [
+        ("k_codes", ctypes.c_void_p),
+        ("v_codes", ctypes.c_void_p),
+        ("k_params", ctypes.c_void_p),
+        ("v_params", ctypes.c_void_p),
+        ("head_dim", ctypes.c_int32),
+        ("num_kv_heads", ctypes.c_int32),
+        ("capacity", ctypes.c_int64),
     ]
 
 
@@ -124,6 +139,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "qattn_decode_fp16_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
         "qattn_decode_fp16": (i32, [vp, vp, vp, i32, i32, i32, i32, i64, vp, i32, f32, i32, vp, sz, vp, vp, vp]),
         "qattn_prefill_fp16": (i32, [vp, vp, vp, i32, i32, i32, i32, i64, i32, i32, f32, i32, vp, vp, vp]),
+        "qattn_pq_quantize": (i32, [vp, vp, i32, i32, i32, vp, ctypes.POINTER(PqCacheStruct), vp]),
+        "qattn_decode_pq_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
+        "qattn_decode_pq": (i32, [vp, ctypes.POINTER(PqCacheStruct), vp, i32, i32, i32, f32, i32, vp, sz, vp, vp, vp]),
+        "qattn_flashq_flush_pq": (i32, [ctypes.POINTER(FlashqBufferStruct), ctypes.POINTER(PqCacheStruct), vp, i32, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -443,6 +462,83 @@ def prefill_fp16(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, nk: int, sof
     _check(load_library().qattn_prefill_fp16(_ptr(q), _ptr(k), _ptr(v), B, Hq, Hkv, D, cap, Nq, nk,
                                              float(softmax_scale), int(bool(causal)), _ptr(out), _ptr(lse),
                                              _stream(q.device)), "qattn_prefill_fp16")
+    return (out, lse) if return_lse else out
+
+
+# ------------------------------------------------------- progressive storage
+
+@dataclass
+class PqCache:
+    """Progressive INT8 -> INT4 cache in 64-token blocks (see qattn_pq_cache):
+    codes [B, Hkv, capacity, D/2] uint8, params [B, Hkv, capacity/64, 2D+16] uint8."""
+    k_codes: torch.Tensor
+    v_codes: torch.Tensor
+    k_params: torch.Tensor
+    v_params: torch.Tensor
+    head_dim: int
+    num_kv_heads: int
+    capacity: int
+
+    @staticmethod
+    def contiguous(batch, num_kv_heads, capacity, head_dim, device="cuda"):
+        cap = -(-capacity // PAGE_SIZE) * PAGE_SIZE
+        codes = lambda: torch.zeros(batch, num_kv_heads, cap, head_dim // 2, dtype=torch.uint8, device=device)
+        params = lambda: torch.zeros(batch, num_kv_heads, cap // PAGE_SIZE, 2 * head_dim + 16, dtype=torch.uint8,
+                                     device=device)
+        return PqCache(codes(), codes(), params(), params(), head_dim, num_kv_heads, cap)
+
+    def struct(self) -> PqCacheStruct:
+        return PqCacheStruct(self.k_codes.data_ptr(), self.v_codes.data_ptr(), self.k_params.data_ptr(),
+                             self.v_params.data_ptr(), self.head_dim, self.num_kv_heads, self.capacity)
+
+
+def pq_quantize(k: torch.Tensor, v: torch.Tensor, cache: PqCache, start_block: Optional[torch.Tensor] = None) -> None:
+    """k, v [B, Hkv, n, D] (fp32 or fp16, n a multiple of 64) -> n/64 blocks at start_block[b] + i."""
+    if k.dtype not in (torch.float32, torch.float16) or v.dtype != k.dtype:
+        raise TypeError("k and v must both be float32 or float16")
+    k, v = k.contiguous(), v.contiguous()
+    B, _, n, _ = k.shape
+    sb = None if start_block is None else start_block.to(device=k.device, dtype=torch.int32).contiguous()
+    st = cache.struct()
+    dt = QATTN_F16 if k.dtype == torch.float16 else QATTN_F32
+    _check(load_library().qattn_pq_quantize(_ptr(k), _ptr(v), dt, B, n, _ptr(sb), ctypes.byref(st),
+                                            _stream(k.device)), "qattn_pq_quantize")
+
+
+def flashq_flush_pq(buf, cache: PqCache, cache_lens: torch.Tensor) -> None:
+    """Full decode buffers -> one progressive block each at cache_lens[b] (a multiple of 64)."""
+    st = cache.struct()
+    bs = buf.struct()
+    cl = cache_lens.to(device=cache.k_codes.device, dtype=torch.int32).contiguous()
+    _check(load_library().qattn_flashq_flush_pq(ctypes.byref(bs), ctypes.byref(st), _ptr(cl), cl.numel(),
+                                                _stream(cache.k_codes.device)), "qattn_flashq_flush_pq")
+
+
+def decode_pq_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len, num_splits=0) -> int:
+    return int(load_library().qattn_decode_pq_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
+                                                             max_seq_len, num_splits))
+
+
+def decode_pq(q: torch.Tensor, cache: PqCache, seq_lens: torch.Tensor, max_seq_len: int, softmax_scale: float,
+              num_splits: int = 0, workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+              lse: Optional[torch.Tensor] = None, return_lse: bool = False):
+    """q [B, Hq, D] fp16 against a progressive cache -> out [B, Hq, D] fp16 (and lse)."""
+    q = q.contiguous()
+    B, Hq, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty(B, Hq, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        need = decode_pq_workspace_size(B, Hq, cache.num_kv_heads, D, max_seq_len, num_splits)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    sl = seq_lens.to(device=q.device, dtype=torch.int32).contiguous()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = cache.struct()
+    _check(load_library().qattn_decode_pq(_ptr(q), ctypes.byref(st), _ptr(sl), B, Hq, max_seq_len,
+                                          float(softmax_scale), num_splits, _ptr(workspace), ws_bytes, _ptr(out),
+                                          _ptr(lse), _stream(q.device)), "qattn_decode_pq")
     return (out, lse) if return_lse else out
 
 

@@ -709,6 +709,108 @@ qattn_status qattn_decode_fp16(const uint16_t *q, const uint16_t *k, const uint1
   return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "fp16 decode launch");
 }
 
+}  // extern "C"
+
+namespace qattn {
+namespace {
+
+// Validates a progressive cache (batch sequences).
+qattn_status check_pq(const qattn_pq_cache *c, PqView *v) {
+  if (!c) return fail(QATTN_ERR_INVALID_ARG, "progressive cache is NULL");
+  if (!c->k_codes || !c->v_codes || !c->k_params || !c->v_params)
+    return fail(QATTN_ERR_INVALID_ARG, "progressive cache has a NULL pointer");
+  if (!aligned16(c->k_codes) || !aligned16(c->v_codes) || !aligned16(c->k_params) || !aligned16(c->v_params))
+    return fail(QATTN_ERR_INVALID_ARG, "progressive cache pointers must be 16-byte aligned");
+  if (c->head_dim != 64 && c->head_dim != 128) return fail(QATTN_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", c->head_dim);
+  if (c->num_kv_heads <= 0) return fail(QATTN_ERR_INVALID_ARG, "num_kv_heads %d", c->num_kv_heads);
+  if (c->capacity <= 0 || c->capacity % kPage || c->capacity > 0x7fffffffLL)
+    return fail(QATTN_ERR_INVALID_ARG, "capacity %lld must be a positive multiple of 64", (long long)c->capacity);
+  v->k_codes = c->k_codes, v->v_codes = c->v_codes, v->k_params = c->k_params, v->v_params = c->v_params;
+  v->capacity = c->capacity, v->hkv = c->num_kv_heads, v->head_dim = c->head_dim;
+  return QATTN_OK;
+}
+
+}  // namespace
+}  // namespace qattn
+
+extern "C" {
+
+qattn_status qattn_pq_quantize(const void *k, const void *v, qattn_dtype x_dtype, int32_t batch, int32_t n,
+                               const int32_t *start_block, const qattn_pq_cache *cache, qattn_stream_t stream) {
+  if (batch < 0 || n < 0 || n % kPage) return fail(QATTN_ERR_INVALID_ARG, "batch %d, n %d (a multiple of 64)", batch, n);
+  if (x_dtype != QATTN_F32 && x_dtype != QATTN_F16) return fail(QATTN_ERR_INVALID_ARG, "x_dtype %d", (int)x_dtype);
+  PqView view;
+  qattn_status st = check_pq(cache, &view);
+  if (st != QATTN_OK) return st;
+  if (static_cast<int64_t>(batch) * view.hkv > 65535) return fail(QATTN_ERR_UNSUPPORTED, "batch * Hkv > 65535");
+  if (batch == 0 || n == 0) return QATTN_OK;
+  if (!k || !v) return fail(QATTN_ERR_INVALID_ARG, "k or v is NULL");
+  DeviceState *ds;
+  if ((st = device_state(&ds)) != QATTN_OK) return st;
+  cudaError_t e = launch_pq_quantize(k, v, x_dtype == QATTN_F16, batch, n, start_block, view, ds->status,
+                                     reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "progressive quantize launch");
+}
+
+size_t qattn_decode_pq_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t max_seq_len, int32_t num_splits) {
+  return qattn_decode_fp16_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len, num_splits);
+}
+
+qattn_status qattn_decode_pq(const uint16_t *q, const qattn_pq_cache *cache, const int32_t *seq_lens, int32_t batch,
+                             int32_t num_q_heads, int32_t max_seq_len, float softmax_scale, int32_t num_splits,
+                             void *workspace, size_t workspace_bytes, uint16_t *out, float *lse, qattn_stream_t stream) {
+  PqView view;
+  qattn_status st = check_pq(cache, &view);
+  if (st != QATTN_OK) return st;
+  if (batch < 0 || batch > QATTN_MAX_BATCH || num_q_heads <= 0 || max_seq_len < 0)
+    return fail(QATTN_ERR_INVALID_ARG, "batch %d, Hq %d, max_seq_len %d", batch, num_q_heads, max_seq_len);
+  if (num_q_heads % view.hkv) return fail(QATTN_ERR_INVALID_ARG, "Hq %d is not a multiple of Hkv %d", num_q_heads, view.hkv);
+  if (num_q_heads / view.hkv > QATTN_MAX_GROUP)
+    return fail(QATTN_ERR_UNSUPPORTED, "group size %d > %d", num_q_heads / view.hkv, QATTN_MAX_GROUP);
+  if (num_splits < 0 || num_splits > QATTN_MAX_SPLITS)
+    return fail(QATTN_ERR_INVALID_ARG, "num_splits %d (0..%d)", num_splits, QATTN_MAX_SPLITS);
+  if (static_cast<int64_t>(batch) * view.hkv > 65535) return fail(QATTN_ERR_UNSUPPORTED, "batch * Hkv > 65535");
+  if (batch == 0) return QATTN_OK;
+  if (!q || !seq_lens || !out) return fail(QATTN_ERR_INVALID_ARG, "q, seq_lens or out is NULL");
+  if (!aligned16(q) || !aligned16(out)) return fail(QATTN_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+  DeviceState *ds;
+  if ((st = device_state(&ds)) != QATTN_OK) return st;
+  DecodePqArgs a;
+  decode16_plan(batch, view.hkv, max_seq_len, num_splits, ds->sms, &a.splits, &a.chunk);
+  const size_t need = decode16_workspace(batch, num_q_heads, view.head_dim, a.splits);
+  if (need && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+    return fail(QATTN_ERR_WORKSPACE, "workspace of %zu bytes (16-byte aligned) needed, %zu given", need,
+                workspace ? workspace_bytes : (size_t)0);
+  a.q = q, a.seq_lens = seq_lens, a.out = out, a.lse = lse;
+  a.partial_o = static_cast<float *>(workspace);
+  const size_t rows = static_cast<size_t>(a.splits) * batch * num_q_heads;
+  a.partial_lse = need ? reinterpret_cast<float *>(static_cast<char *>(workspace) + (rows * view.head_dim * 4 + 255) / 256 * 256)
+                       : nullptr;
+  a.batch = batch, a.hq = num_q_heads;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  cudaError_t e = launch_decode_pq(a, view, ds->status, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "progressive decode launch");
+}
+
+qattn_status qattn_flashq_flush_pq(const qattn_flashq_buffer *buf, const qattn_pq_cache *cache,
+                                   const int32_t *cache_lens, int32_t batch, qattn_stream_t stream) {
+  FlashqView fv;
+  PqView pv;
+  qattn_status st = check_flashq(buf, batch, &fv);
+  if (st != QATTN_OK) return st;
+  if ((st = check_pq(cache, &pv)) != QATTN_OK) return st;
+  if (pv.head_dim != fv.head_dim || pv.hkv != fv.hkv)
+    return fail(QATTN_ERR_INVALID_ARG, "buffer (D %d, Hkv %d) and cache (D %d, Hkv %d) differ", fv.head_dim, fv.hkv,
+                pv.head_dim, pv.hkv);
+  if (batch == 0) return QATTN_OK;
+  if (!cache_lens) return fail(QATTN_ERR_INVALID_ARG, "cache_lens is NULL");
+  DeviceState *ds;
+  if ((st = device_state(&ds)) != QATTN_OK) return st;
+  cudaError_t e = launch_flashq_flush_pq(fv, pv, cache_lens, batch, ds->status, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "flashq progressive flush launch");
+}
+
 qattn_status qattn_prefill_fp16(const uint16_t *q, const uint16_t *k, const uint16_t *v, int32_t batch,
                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int64_t capacity,
                                 int32_t nq, int32_t nk, float softmax_scale, int32_t causal, uint16_t *out,

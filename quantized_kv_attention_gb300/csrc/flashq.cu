@@ -34,29 +34,6 @@ namespace {
 constexpr uint32_t kFlagBufferFull = 8u;  // an append found a full buffer (row dropped)
 constexpr int kNb = 64;                   // buffer rows
 
-// u = fp16(fp32(R / 127)), saturating at 65504.
-__device__ __forceinline__ __half universal_scale(float r) {
-  __half u = __float2half_rn(__fdiv_rn(r, 127.0f));
-  if (__hisinf(u)) u = __ushort_as_half(0x7BFF);
-  return u;
-}
-
-// clamp(RNE(x / u), -127, 127) on the exact quotient: the fp32 quotient gives
-// a candidate m for |x| / u, corrected against the half-way points
-// (m +- 1/2) u, which are exact in fp32 (at most 9 + 11 significant bits).
-__device__ __forceinline__ int code8(float x, float u) {
-  if (!(u > 0.f)) return 0;
-  const float ax = fabsf(x);
-  float m = rintf(__fdiv_rn(ax, u));
-  if (m >= 128.f) return x < 0.f ? -127 : 127;
-  const float hi = (m + 0.5f) * u, lo = (m - 0.5f) * u;
-  const bool odd = (static_cast<int>(m) & 1) != 0;
-  if (ax > hi || (ax == hi && odd)) m += 1.f;
-  else if (m >= 1.f && (ax < lo || (ax == lo && odd))) m -= 1.f;
-  const int c = min(static_cast<int>(m), 127);
-  return x < 0.f ? -c : c;
-}
-
 // Cache row of token `pos` of (b, h): contiguous or through the page table;
 // -1 past the cache or in a missing page.
 __device__ __forceinline__ int64_t cache_row(const KvView &c, int b, int h, int64_t pos) {

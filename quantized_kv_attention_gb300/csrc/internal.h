@@ -152,6 +152,36 @@ struct Decode16Args {
 cudaError_t launch_decode16(const Decode16Args &a, const CUtensorMap &kmap, const CUtensorMap &vmap, uint32_t *err,
                             cudaStream_t stream);
 
+// pq.cu: progressive INT8 -> INT4 storage in 64-token blocks.  Codes [batch,
+// Hkv, capacity, D/2] unsigned nibbles; one record per (sequence, kv-head,
+// block) and tensor [batch, Hkv, capacity/64, 2*D + 16] bytes: s2[D] uint8,
+// z2[D] int8, s1 fp16, 14 zero bytes.
+struct PqView {
+  uint8_t *k_codes, *v_codes;
+  uint8_t *k_params, *v_params;
+  int64_t capacity;
+  int hkv, head_dim;
+};
+// n new tokens per (sequence, kv-head), a multiple of 64, into blocks
+// start_block[b] + i (start_block NULL: 0); blocks past the cache are skipped.
+cudaError_t launch_pq_quantize(const void *k, const void *v, bool fp16_in, int batch, int n, const int32_t *start_block,
+                               const PqView &c, uint32_t *err, cudaStream_t stream);
+// decode over a progressive cache: `splits` key ranges of `chunk` tokens (a
+// multiple of 64); partials as Decode16Args.
+struct DecodePqArgs {
+  const uint16_t *q;
+  const int32_t *seq_lens;
+  uint16_t *out;
+  float *lse;
+  float *partial_o, *partial_lse;
+  int batch, hq, splits, chunk;
+  float scale_log2;
+};
+cudaError_t launch_decode_pq(const DecodePqArgs &a, const PqView &c, uint32_t *err, cudaStream_t stream);
+// full decode buffers -> one progressive block each at cache_lens[b]
+cudaError_t launch_flashq_flush_pq(const FlashqView &f, const PqView &c, const int32_t *cache_lens, int batch,
+                                   uint32_t *err, cudaStream_t stream);
+
 // api.cu: sets the message returned by qattn_last_error() on this thread.
 void record_error(const char *msg);
 

@@ -147,6 +147,31 @@ __device__ __forceinline__ void quantize_row_warp(const T *src, uint8_t *dst_cod
   quantize_vals_warp<D>(x, dst_codes, dst_scale, lane);
 }
 
+// The int8 code of TurboAttention's 8-bit symmetric stage (§3.2, §3.3), shared
+// by the decode buffer and the progressive blocks: a range R gives the scale
+// u = fp16(fp32(R / 127)), saturating at 65504, and a value x the code
+// clamp(RNE(x / u), -127, 127) on the exact quotient: the fp32 quotient gives
+// a candidate m for |x| / u, corrected against the half-way points
+// (m +- 1/2) u, which are exact in fp32 (at most 9 + 11 significant bits).
+__device__ __forceinline__ __half universal_scale(float r) {
+  __half u = __float2half_rn(__fdiv_rn(r, 127.0f));
+  if (__hisinf(u)) u = __ushort_as_half(0x7BFF);
+  return u;
+}
+
+__device__ __forceinline__ int code8(float x, float u) {
+  if (!(u > 0.f)) return 0;
+  const float ax = fabsf(x);
+  float m = rintf(__fdiv_rn(ax, u));
+  if (m >= 128.f) return x < 0.f ? -127 : 127;
+  const float hi = (m + 0.5f) * u, lo = (m - 0.5f) * u;
+  const bool odd = (static_cast<int>(m) & 1) != 0;
+  if (ax > hi || (ax == hi && odd)) m += 1.f;
+  else if (m >= 1.f && (ax < lo || (ax == lo && odd))) m -= 1.f;
+  const int c = min(static_cast<int>(m), 127);
+  return x < 0.f ? -c : c;
+}
+
 // INT3 ("Quantized Cross-Attention ... In-SRAM Dequantization" §3.3: ten
 // 3-bit values per 32-bit word) of one D = 128 row: s = fp16(fp32(absmax /
 // 3)), code = clamp(RNE(x / s), -3, 3) decided against the exact half-way

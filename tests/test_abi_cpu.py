@@ -272,7 +272,8 @@ def test_ctypes_structs_match_the_c_layout(tmp_path):
     cc = shutil.which("gcc") or shutil.which("cc")
     if cc is None:
         pytest.skip("no C compiler")
-    structs = {"qattn_kv_cache": qa.KvCacheStruct, "qattn_flashq_buffer": qa.FlashqBufferStruct}
+    structs = {"qattn_kv_cache": qa.KvCacheStruct, "qattn_flashq_buffer": qa.FlashqBufferStruct,
+               "qattn_pq_cache": qa.PqCacheStruct}
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "qattn.h"', "int main(void) {"]
     for cname, py in structs.items():
         lines.append(f'  printf("{cname} size %zu\\n", sizeof({cname}));')
@@ -289,3 +290,39 @@ def test_ctypes_structs_match_the_c_layout(tmp_path):
         want.append(f"{cname} size {ctypes.sizeof(py)}")
         want += [f"{cname} {f} {getattr(py, f).offset}" for f, _ in py._fields_]
     assert [l for l in got if l] == want
+
+
+def test_comparison_and_progressive_calls_reject_bad_arguments():
+    """Host checks of the FP16, dequantize and progressive entry points (no GPU work)."""
+    qa = ensure_library()
+    lib = qa.load_library()
+    fake = 0x10000
+    st = qa.KvCacheStruct()
+    st.k_codes = st.k_scales = st.v_codes = st.v_scales = fake
+    st.head_dim, st.num_kv_heads, st.capacity = 128, 8, 4096
+    assert lib.qattn_dequantize_kv(ctypes.byref(st), 1, 4097, fake, fake, None) == qa.QATTN_ERR_INVALID_ARG  # n > capacity
+    st.code_bits = 3
+    assert lib.qattn_dequantize_kv(ctypes.byref(st), 1, 64, fake, fake, None) == qa.QATTN_ERR_UNSUPPORTED
+    # fp16 decode: D 96, group 16, capacity 0
+    assert lib.qattn_decode_fp16(fake, fake, fake, 1, 8, 8, 96, 64, fake, 64, 1.0, 0, None, 0, fake, None,
+                                 None) == qa.QATTN_ERR_UNSUPPORTED
+    assert lib.qattn_decode_fp16(fake, fake, fake, 1, 32, 2, 128, 64, fake, 64, 1.0, 0, None, 0, fake, None,
+                                 None) == qa.QATTN_ERR_UNSUPPORTED
+    assert lib.qattn_decode_fp16(fake, fake, fake, 1, 8, 8, 128, 0, fake, 64, 1.0, 0, None, 0, fake, None,
+                                 None) == qa.QATTN_ERR_INVALID_ARG
+    assert lib.qattn_decode_fp16_workspace_size(1, 8, 3, 128, 64, 0) == 0                    # Hq % Hkv
+    # fp16 prefill: nq > nk, nk > capacity
+    assert lib.qattn_prefill_fp16(fake, fake, fake, 1, 8, 8, 128, 256, 100, 50, 1.0, 1, fake, None,
+                                  None) == qa.QATTN_ERR_INVALID_ARG
+    assert lib.qattn_prefill_fp16(fake, fake, fake, 1, 8, 8, 128, 64, 10, 100, 1.0, 1, fake, None,
+                                  None) == qa.QATTN_ERR_INVALID_ARG
+    # progressive: n not a multiple of 64, capacity not a multiple of 64, NULL pointer
+    pq = qa.PqCacheStruct(fake, fake, fake, fake, 128, 8, 4096)
+    assert lib.qattn_pq_quantize(fake, fake, 0, 1, 100, None, ctypes.byref(pq), None) == qa.QATTN_ERR_INVALID_ARG
+    bad = qa.PqCacheStruct(fake, fake, fake, fake, 128, 8, 100)
+    assert lib.qattn_pq_quantize(fake, fake, 0, 1, 64, None, ctypes.byref(bad), None) == qa.QATTN_ERR_INVALID_ARG
+    null = qa.PqCacheStruct(0, fake, fake, fake, 128, 8, 4096)
+    assert lib.qattn_decode_pq(fake, ctypes.byref(null), fake, 1, 8, 64, 1.0, 0, None, 0, fake, None,
+                               None) == qa.QATTN_ERR_INVALID_ARG
+    assert lib.qattn_decode_pq(fake, ctypes.byref(pq), fake, 1, 12, 64, 1.0, 0, None, 0, fake, None,
+                               None) == qa.QATTN_ERR_INVALID_ARG                              # Hq % Hkv
