@@ -520,7 +520,9 @@ def run_decode_lowbit(name, args, device, gpu_index, rank, bits=3):
         "setup": {"cache_copies": copies, "parallelism": f"replicas x{world}",
                   "timing": "CUDA graphs of the API calls"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": profiled_traffic(f"decode_{name}_int{bits}_ncu.txt",
+                                                 source_digest("decode.cu", "ptx.cuh", "quant_row.cuh"), kv_bytes),
                      "kernel": f"decode + merge (one qattn_decode call, INT{bits} cache)", "peak_source": pk_src,
                      "us_per_launch": round(dec_ms * 1e3, 3)},
         "clocks": clocks,
@@ -847,7 +849,10 @@ def run_quantize(name, args, device, gpu_index, rank):
                    "step": "quantize all K and V rows of the prompt into the INT4 cache (one qattn_quantize_kv)"},
         "setup": {"input_copies": copies, "parallelism": f"replicas x{world}", "timing": "CUDA graphs of the API call"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None, "kernel": "quantize_kv",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": profiled_traffic(f"quantize_{name}_quantize_ncu.txt",
+                                                 source_digest("quantize.cu", "quant_row.cuh", "ptx.cuh"), step_bytes),
+                     "kernel": "quantize_kv",
                      "peak_source": pk_src, "us_per_launch": round(one_ms * 1e3, 3)},
         "clocks": clocks,
     }
@@ -907,7 +912,10 @@ def run_decode_pq(name, args, device, gpu_index, rank):
                    "step": "split-KV decode over progressive INT8 -> INT4 blocks (one qattn_decode_pq call)"},
         "setup": {"cache_copies": copies, "parallelism": f"replicas x{world}", "timing": "CUDA graphs of the API call"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None, "kernel": "decode_pq + combine",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "traffic": profiled_traffic(f"decode_pq_{name}_pq_ncu.txt",
+                                                 source_digest("pq.cu", "quant_row.cuh", "ptx.cuh"), kv_bytes),
+                     "kernel": "decode_pq + combine",
                      "peak_source": pk_src, "us_per_launch": round(one_ms * 1e3, 3)},
         "clocks": clocks,
     }
@@ -1003,6 +1011,8 @@ def run_compare(name, args, device, gpu_index, rank):
                 line["value"] = round(f16_bytes * steps / 1e9 / tmax, 2)
                 line["roofline"] = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
                                     "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4),
+                                    "traffic": profiled_traffic(f"decode16_{name}_fp16_ncu.txt",
+                                                                source_digest("fp16kv.cu", "ptx.cuh"), f16_bytes),
                                     "us_per_launch": round(one_ms * 1e3, 3), "peak_source": pk_src}
                 line["config"]["kv_bytes_per_step"] = f16_bytes
         res[arm] = line
