@@ -353,7 +353,7 @@ qattn_status decode_impl(const uint16_t *q, const void *k_new, const void *v_new
   if (static_cast<int64_t>(batch) * view.hkv * stage_limit >= (int64_t(1) << 31))
     return fail(QATTN_ERR_UNSUPPORTED, "batch * Hkv * cached stages exceeds 2^31");
   const bool paged = view.page_table != nullptr;
-  const int warps = view.bits != 4 ? 8 : decode_layout(batch, view.hkv, max_seq_len, paged,
+  const int warps = decode_layout(batch, view.hkv, max_seq_len, paged,
                                                         num_splits > 0 ? num_splits : ds->sms);
   const int ctas = plan_ctas(batch, view.hkv, view.head_dim, max_seq_len, num_splits, ds->sms, paged, warps);
   const DecodeGeometry geo = decode_geometry(view.head_dim, view.hkv, paged, warps);

@@ -1265,8 +1265,10 @@ DecodeGeometry decode_geometry(int head_dim, int hkv, bool paged, int warps) {
 cudaError_t launch_decode(const DecodeArgs &a, const KvView &cache, const DecodeMaps &maps, uint32_t *err,
                           cudaStream_t stream) {
   if (a.batch == 0 || a.ctas <= 0) return cudaSuccess;
-  if (cache.bits == 3) return launch_d<128, 8, 3>(a, cache, maps, err, stream);  // contiguous, D = 128
-  if (cache.bits == 2) return launch_d<128, 8, 2>(a, cache, maps, err, stream);  // contiguous, D = 128
+  if (cache.bits == 3)  // contiguous, D = 128
+    return a.warps == 8 ? launch_d<128, 8, 3>(a, cache, maps, err, stream) : launch_d<128, 12, 3>(a, cache, maps, err, stream);
+  if (cache.bits == 2)
+    return a.warps == 8 ? launch_d<128, 8, 2>(a, cache, maps, err, stream) : launch_d<128, 12, 2>(a, cache, maps, err, stream);
   if (cache.page_table || a.warps == 8)
     return cache.head_dim == 128 ? launch_d<128, 8>(a, cache, maps, err, stream)
                                  : launch_d<64, 8>(a, cache, maps, err, stream);
