@@ -6,9 +6,10 @@
 // 0; "Quantized Cross-Attention ... In-SRAM Dequantization" §3.2: 4-bit codes
 // with one FP16 scale per token.  s = fp16(fp32(absmax / 7)), both roundings
 // to nearest even, saturating at 65504; code = round-half-even(x / s) clamped
-// to [-7, 7], decided by exact comparisons with the half-way points
-// (k + 1/2) s, which are exact in fp32 (s has 11 significant bits, 2k + 1 at
-// most 4 bits), so the result equals rounding of the exact quotient.
+// to [-7, 7] on the exact quotient: a candidate from one fused multiply-add,
+// proved by its exact remainder, and for the values it cannot prove (ties)
+// exact comparisons with the half-way points (k + 1/2) s, which are exact in
+// fp32 (s has 11 significant bits, 2k + 1 at most 4 bits).
 #pragma once
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -61,6 +62,73 @@ __device__ __forceinline__ int code_of(float x, float s) {
   return x < 0.f ? -m : m;
 }
 
+// min / max that return NaN when either operand is NaN.
+__device__ __forceinline__ float fmin_nan(float a, float b) {
+  float r;
+  asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// The lane's VPL codes clamp(RNE(x / s), -7, 7) as packed nibbles (element j
+// at bits 4j), for s > 0 -- the same codes as code_of, with fewer
+// instructions.  A fused multiply-add of x with r ~ 1/s and 1.5 * 2^23
+// rounds x * r to an integer m (the sum has ulp 1), and the sum's encoding is
+// 0x4B400000 + m, whose low nibble is m in two's complement.  Because r is an
+// approximation, m is then proved: with e = x - m s taken by a second fused
+// multiply-add, |e| < s / 2 means m is the integer nearest to x / s (a
+// computed |e| below the representable s / 2 implies the exact one is, as
+// rounding is monotonic).  A value at or past a half-way point -- an exact tie
+// or a candidate off by one -- and a NaN (it fails the test) are coded by the
+// threshold count instead.  kClamp first clamps x to [-7s, 7s], which leaves
+// the clamped code unchanged; it is needed only when s may be far below
+// absmax / 7: a subnormal or saturated fp16 scale.  For a normal scale below
+// 65504, s >= (absmax / 7)(1 - 2^-24)(1 - 2^-11), so |x| / s <= 7.004 and m
+// stays in [-7, 7] without it.
+template <int VPL, bool kClamp>
+__device__ __forceinline__ uint32_t codes4(const float (&x)[VPL], float s) {
+  constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
+  const float lim = 7.f * s, h = 0.5f * s;
+  // The nibbles are summed as integers: sum_j enc(y_j) 16^j = 0x4B400000 *
+  // ones + sum_j m_j 16^j (ones = sum_j 16^j, modulo 2^32); adding
+  // (8 - 0x4B400000) * ones leaves sum_j (m_j + 8) 16^j with every digit in
+  // [1, 15] (no carries), and m_j + 8 XOR 8 is m_j's two's-complement nibble.
+  static_assert(VPL == 2 || VPL == 4, "two or four values per lane");
+  constexpr uint32_t kOnes = VPL == 4 ? 0x1111u : 0x11u;
+  constexpr uint32_t kBias = (8u - 0x4B400000u) * kOnes;
+  uint32_t acc = kBias;
+  bool sure = true;
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) {
+    const float xc = kClamp ? fmax_nan(fmin_nan(x[j], lim), -lim) : x[j];
+    const float y = fmaf(xc, r, kShift);
+    const float e = fmaf(kShift - y, s, xc);
+    sure = sure && fabsf(e) < h;
+    acc += __float_as_uint(y) * (1u << (4 * j));
+  }
+  uint32_t packed = (acc ^ (8u * kOnes)) & (kOnes * 0xFu);
+  if (!sure) {
+    packed = 0;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) packed |= static_cast<uint32_t>(code_of(x[j], s) & 0xF) << (4 * j);
+  }
+  return packed;
+}
+
+// codes4 for any scale s >= 0 (all codes 0 when s == 0): the clamp only for
+// a subnormal or saturated s.
+template <int VPL>
+__device__ __forceinline__ uint32_t codes4_any(const float (&x)[VPL], float s) {
+  if (s >= 6.103515625e-05f && s < 65504.f) return codes4<VPL, false>(x, s);  // normal fp16 (2^-14 ..)
+  return s > 0.f ? codes4<VPL, true>(x, s) : 0u;
+}
+
 // Quantizes one row of D values held by the 32 lanes of a warp: lane i
 // holds elements 4i..4i+3 (D = 128) or 2i, 2i+1 (D = 64) in x and writes
 // their packed nibbles (low nibble = even element) to dst_codes + i * D / 64;
@@ -80,11 +148,7 @@ __device__ __forceinline__ __half quantize_vals_warp(const float (&x)[D / 32], u
   if (__hisinf(hs)) hs = __ushort_as_half(0x7BFF);
   const float s = __half2float(hs);
 
-  uint32_t packed = 0;
-  if (s > 0.f) {
-#pragma unroll
-    for (int j = 0; j < VPL; ++j) packed |= static_cast<uint32_t>(code_of(x[j], s) & 0xF) << (4 * j);
-  }
+  const uint32_t packed = codes4_any<VPL>(x, s);
   uint8_t *dst = dst_codes + lane * (VPL / 2);
   if constexpr (VPL == 4)
     *reinterpret_cast<uint16_t *>(dst) = static_cast<uint16_t>(packed);
@@ -94,46 +158,38 @@ __device__ __forceinline__ __half quantize_vals_warp(const float (&x)[D / 32], u
   return hs;
 }
 
-// quantize_vals_warp for N rows at once (the same arithmetic, so the same
-// bits), phase by phase across the rows so that their shuffle reductions and
-// divisions overlap; a row whose dst_codes is null is computed but not stored.
-template <int D, int N>
-__device__ __forceinline__ void quantize_vals_warp_n(const float (&x)[N][D / 32], uint8_t *const (&dst_codes)[N],
-                                                     uint16_t *const (&dst_scale)[N], int lane) {
-  constexpr int VPL = D / 32;
-  float am[N];
+// Four rows at once, one per group of 8 lanes (g = lane / 8, l = lane % 8),
+// with the arithmetic of quantize_vals_warp (so the same bits): the row's
+// D values are C = D / 32 chunks of 32, and lane l holds values 4l .. 4l + 3
+// of each chunk, x[c] being the group's chunk (c + g) % C (the rotation keeps
+// the groups' shared-memory reads of a 16-lane phase on distinct banks).  The
+// absmax takes three shuffle levels inside the group, the scale one division
+// per lane for four rows; lane l stores the nibbles of its values of chunk cc
+// at byte 16 cc + 2l of the row, lane 0 of the group the scale.  A group whose
+// dst_codes is null stores nothing.  Every lane of the warp must call it.
+template <int D>
+__device__ __forceinline__ void quantize_vals_warp4(const float (&x)[D / 32][4], uint8_t *dst_codes,
+                                                    uint16_t *dst_scale, int lane) {
+  constexpr int C = D / 32;
+  const int g = lane >> 3, l = lane & 7;
+  float am = 0.f;
 #pragma unroll
-  for (int r = 0; r < N; ++r) {
-    am[r] = 0.f;
+  for (int c = 0; c < C; ++c)
 #pragma unroll
-    for (int j = 0; j < VPL; ++j) am[r] = fmaxf(am[r], fabsf(x[r][j]));
-  }
+    for (int t = 0; t < 4; ++t) am = fmaxf(am, fabsf(x[c][t]));
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1)
+  for (int o = 4; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+  __half hs = __float2half_rn(__fdiv_rn(am, 7.0f));
+  if (__hisinf(hs)) hs = __ushort_as_half(0x7BFF);
+  const float s = __half2float(hs);
+  if (dst_codes != nullptr) {
 #pragma unroll
-    for (int r = 0; r < N; ++r) am[r] = fmaxf(am[r], __shfl_xor_sync(0xffffffffu, am[r], o));
-  __half hs[N];
-#pragma unroll
-  for (int r = 0; r < N; ++r) {
-    hs[r] = __float2half_rn(__fdiv_rn(am[r], 7.0f));
-    if (__hisinf(hs[r])) hs[r] = __ushort_as_half(0x7BFF);
-  }
-#pragma unroll
-  for (int r = 0; r < N; ++r) {
-    const float s = __half2float(hs[r]);
-    uint32_t packed = 0;
-    if (s > 0.f) {
-#pragma unroll
-      for (int j = 0; j < VPL; ++j) packed |= static_cast<uint32_t>(code_of(x[r][j], s) & 0xF) << (4 * j);
+    for (int c = 0; c < C; ++c) {
+      const uint32_t packed = codes4_any<4>(x[c], s);
+      const int cc = (c + g) & (C - 1);
+      *reinterpret_cast<uint16_t *>(dst_codes + cc * 16 + 2 * l) = static_cast<uint16_t>(packed);
     }
-    if (dst_codes[r] != nullptr) {
-      uint8_t *dst = dst_codes[r] + lane * (VPL / 2);
-      if constexpr (VPL == 4)
-        *reinterpret_cast<uint16_t *>(dst) = static_cast<uint16_t>(packed);
-      else
-        *dst = static_cast<uint8_t>(packed);
-      if (lane == 0) *dst_scale[r] = __half_as_ushort(hs[r]);
-    }
+    if (l == 0) *dst_scale = __half_as_ushort(hs);
   }
 }
 

@@ -7,15 +7,14 @@
 //
 // A single HBM pass (D*4 or D*2 bytes read, D/2 + 2 bytes written per INT4
 // row), streamed the way the decode kernel streams the cache: a persistent
-// grid of four CTAs per SM walks the list of 32-row blocks (K's, then V's);
+// grid of two CTAs per SM walks the list of 64-row blocks (K's, then V's);
 // in each CTA one producer thread copies its blocks' source rows into a
 // 3-deep shared-memory ring with bulk copies (the rows of a block are
 // contiguous in k and v unless the cache lists its heads), and 8 consumer
-// warps quantize 4 rows each from shared memory (quantize_vals_warp_n, the
-// four rows' reductions interleaved; the INT3 / INT2 forms row by row) and
-// store codes and scales to the cache.  The work is bound by instruction
-// issue (the exact round-half-even decision per value), so the grid keeps
-// 32 consumer warps per SM.
+// warps quantize 8 rows each from shared memory and store codes and scales
+// to the cache.  INT4 rows take one group of 8 lanes each, so one warp
+// instruction works on four rows (quantize_vals_warp4, two rounds); INT3 /
+// INT2 rows are quantized one at a time by the whole warp.
 #include "internal.h"
 #include "ptx.cuh"
 #include "quant_row.cuh"
@@ -25,8 +24,9 @@ namespace {
 
 constexpr int kQWarps = 8;                     // consumer warps
 constexpr int kQThreads = (kQWarps + 1) * 32;  // + one producer warp
-constexpr int kQRows = 32;                     // rows per block (4 per consumer warp)
-constexpr int kQCtasPerSm = 4;                 // quantizing is issue-bound: many warps per SM
+constexpr int kQWarpRows = 8;                  // rows per consumer warp and block (two rounds of four)
+constexpr int kQRows = kQWarps * kQWarpRows;   // rows per block
+constexpr int kQCtasPerSm = 2;
 constexpr int kQStages = 3;
 
 template <typename T, int D>
@@ -58,7 +58,40 @@ __device__ __forceinline__ void lds_row(uint32_t row, int lane, float (&x)[VPL])
   }
 }
 
-template <typename T, int D>
+// Four consecutive values of type T at shared address p, as floats.
+template <typename T>
+__device__ __forceinline__ void lds4(uint32_t p, float (&x)[4]) {
+  if constexpr (sizeof(T) == 4) {
+    const uint4 u = lds128(p);
+    x[0] = __uint_as_float(u.x), x[1] = __uint_as_float(u.y), x[2] = __uint_as_float(u.z), x[3] = __uint_as_float(u.w);
+  } else {
+    const uint2 u = lds64(p);
+    const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
+    const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
+    x[0] = a.x, x[1] = a.y, x[2] = b.x, x[3] = b.y;
+  }
+}
+
+// Cache row of source row i of (sequence b, cache head h), bh = b * Hkv + h,
+// or -1 when the row is not written: its position is past the capacity or in
+// no page, its page is missing (flagged) or the head map does not name the
+// head (flagged).  Only a lane with `flag` set raises the flags.
+__device__ __forceinline__ int64_t dest_row(const KvView &cache, const int32_t *__restrict__ start_pos, int b,
+                                            int h, int64_t bh, int i, bool flag, uint32_t *err) {
+  if (model_head(cache.head_map, cache.model_hkv, h) < 0) {
+    if (flag && err) atomicOr(err, kFlagBadHead);
+    return -1;
+  }
+  const int64_t pos = static_cast<int64_t>(start_pos ? __ldg(start_pos + b) : 0) + i;
+  if (cache.page_table == nullptr) return pos >= 0 && pos < cache.capacity ? bh * cache.capacity + pos : -1;
+  if (pos < 0 || pos / kPage >= cache.max_pages) return -1;
+  const int page = __ldg(cache.page_table + static_cast<int64_t>(b) * cache.max_pages + pos / kPage);
+  if (page >= 0 && page < cache.num_pages) return (static_cast<int64_t>(page) * cache.hkv + h) * kPage + (pos % kPage);
+  if (flag && err) atomicOr(err, kFlagBadPage);
+  return -1;
+}
+
+template <typename T, int D, bool kInt4>
 __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
     quantize_kv_kernel(const T *__restrict__ k, const T *__restrict__ v, int batch, int n,
                        const int32_t *__restrict__ start_pos, KvView cache, uint32_t *err) {
@@ -127,6 +160,15 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
   }
 
   // -------------------------------------------------------------- consumers
+  // (b, h, i) of the warp's first row: one pair of divisions when the CTA
+  // enters a tensor, then a step of gridDim.x blocks by additions
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kQRows;  // rows between a CTA's blocks
+  const int64_t step_bh = stride / n;
+  const int step_i = static_cast<int>(stride - step_bh * n);
+  const int step_h = static_cast<int>(step_bh % cache.hkv);
+  const int step_b = static_cast<int>(step_bh / cache.hkv);
+  int64_t bh = 0, sp = 0;  // sp: start_pos[sp_b]
+  int i = 0, h = 0, b = 0, tensor = -1, sp_b = -1;
   int it = 0;
   for (int64_t blk = blockIdx.x; blk < blocks; blk += gridDim.x, ++it) {
     const int s = it % kQStages;
@@ -136,86 +178,101 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
     const int64_t r0 = (is_v ? blk - per_tensor : blk) * kQRows;
     uint8_t *codes = is_v ? cache.v_codes : cache.k_codes;
     uint16_t *scales = is_v ? cache.v_scales : cache.k_scales;
-    // (b, h, i) of the warp's first row by one pair of divisions (32-bit
-    // when the row count allows), then stepped row by row
-    const int64_t rw = r0 + warp * 4;
-    int64_t bh;
-    int i;
-    if (rows < (int64_t(1) << 31)) {
-      const uint32_t q = static_cast<uint32_t>(rw) / static_cast<uint32_t>(n);
-      bh = q, i = static_cast<int>(static_cast<uint32_t>(rw) - q * static_cast<uint32_t>(n));
+    const int64_t rw = r0 + warp * kQWarpRows;
+    if (tensor != static_cast<int>(is_v)) {
+      tensor = is_v;
+      if (rows < (int64_t(1) << 31)) {
+        const uint32_t q = static_cast<uint32_t>(rw) / static_cast<uint32_t>(n);
+        bh = q, i = static_cast<int>(static_cast<uint32_t>(rw) - q * static_cast<uint32_t>(n));
+      } else {
+        bh = rw / n, i = static_cast<int>(rw - bh * n);
+      }
+      h = static_cast<int>(bh % cache.hkv), b = static_cast<int>(bh / cache.hkv);
     } else {
-      bh = rw / n, i = static_cast<int>(rw - bh * n);
+      i += step_i, bh += step_bh, h += step_h, b += step_b;
+      if (i >= n) i -= n, ++bh, ++h;
+      if (h >= cache.hkv) h -= cache.hkv, ++b;
     }
-    int h = static_cast<int>(static_cast<uint32_t>(bh) % static_cast<uint32_t>(cache.hkv));
-    int b = static_cast<int>(static_cast<uint32_t>(bh) / static_cast<uint32_t>(cache.hkv));
-    // the warp's 4 rows: destinations and values first, then (INT4) one
-    // quantization of all four with their reductions interleaved
-    uint8_t *dc[4];
-    uint16_t *ds[4];
-    float x[4][VPL];
-#pragma unroll
-    for (int r = 0; r < 4; ++r, ++i) {
-      if (i == n) {
-        i = 0, ++bh;
-        if (++h == cache.hkv) h = 0, ++b;
+    // the warp's rows of one (sequence, head) going to consecutive cache rows
+    // (contiguous, or inside one page): one destination for all of them
+    int64_t span_row = -1;
+    if (got && rw + kQWarpRows - 1 < rows && i + kQWarpRows - 1 < n && cache.head_map == nullptr) {
+      if (b != sp_b) sp_b = b, sp = start_pos ? __ldg(start_pos + b) : 0;
+      const int64_t pos = sp + i;
+      if (cache.page_table == nullptr) {
+        if (pos >= 0 && pos + kQWarpRows - 1 < cache.capacity) span_row = bh * cache.capacity + pos;
+      } else if (pos >= 0 && pos % kPage + kQWarpRows - 1 < kPage && pos / kPage < cache.max_pages) {
+        const int page = __ldg(cache.page_table + static_cast<int64_t>(b) * cache.max_pages + pos / kPage);
+        if (page >= 0 && page < cache.num_pages)
+          span_row = (static_cast<int64_t>(page) * cache.hkv + h) * kPage + (pos % kPage);
       }
-      dc[r] = nullptr, ds[r] = nullptr;
-      const int64_t row = rw + r;
-      if (got && row < rows) {
-        if (model_head(cache.head_map, cache.model_hkv, h) < 0) {
-          if (lane == 0 && err) atomicOr(err, kFlagBadHead);
-        } else {
-          const int64_t pos = static_cast<int64_t>(start_pos ? __ldg(start_pos + b) : 0) + i;
-          int64_t dst_row = -1;  // row index in the destination cache
-          if (cache.page_table == nullptr) {
-            if (pos >= 0 && pos < cache.capacity) dst_row = bh * cache.capacity + pos;
-          } else if (pos >= 0 && pos / kPage < cache.max_pages) {
-            const int page = __ldg(cache.page_table + static_cast<int64_t>(b) * cache.max_pages + pos / kPage);
-            if (page >= 0 && page < cache.num_pages)
-              dst_row = (static_cast<int64_t>(page) * cache.hkv + h) * kPage + (pos % kPage);
-            else if (lane == 0 && err)
-              atomicOr(err, kFlagBadPage);
-          }
-          if (dst_row >= 0) {
-            const int tb = cache.bits == 3 ? 52 : cache.bits == 2 ? 32 : D / 2;  // code bytes per row
-            dc[r] = codes + dst_row * tb, ds[r] = scales + dst_row;
-          }
+      // otherwise row by row below (which flags a missing page)
+    }
+    const uint32_t stage = smem_u32(smem + s * C::kStageBytes + warp * kQWarpRows * C::kRowBytes);
+    if constexpr (kInt4) {
+      // round u: lane group g = lane / 8 takes the warp's row 4u + g
+      const int g = lane >> 3, l = lane & 7;
+#pragma unroll 1
+      for (int u = 0; u < kQWarpRows / 4; ++u) {
+        const int wr = 4 * u + g;  // the group's row within the warp's rows
+        int64_t dst = span_row >= 0 ? span_row + wr : -1;
+        if (span_row < 0 && got && rw + wr < rows) {
+          int64_t bhg = bh;
+          int ig = i, hg = h, bg = b;
+          for (int r = 0; r < wr; ++r)
+            if (++ig == n) {
+              ig = 0, ++bhg;
+              if (++hg == cache.hkv) hg = 0, ++bg;
+            }
+          dst = dest_row(cache, start_pos, bg, hg, bhg, ig, l == 0, err);
         }
-      }
-      if (dc[r] != nullptr)
-        lds_row<T, VPL>(smem_u32(smem + s * C::kStageBytes + (warp * 4 + r) * C::kRowBytes), lane, x[r]);
-      else
+        constexpr int NC = D / 32;  // chunks of 32 values
+        float x[NC][4];
 #pragma unroll
-        for (int j = 0; j < VPL; ++j) x[r][j] = 0.f;
-    }
-    if (D == 128 && cache.bits != 4) {
-      if constexpr (D == 128) {
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          if (dc[r] == nullptr) continue;  // warp-uniform
-          if (cache.bits == 3)
-            quantize_vals3_warp(x[r], reinterpret_cast<uint32_t *>(dc[r]), ds[r], lane);
+        for (int c = 0; c < NC; ++c) {
+          const int cc = (c + g) & (NC - 1);
+          if (dst >= 0)
+            lds4<T>(stage + wr * C::kRowBytes + (cc * 32 + 4 * l) * static_cast<int>(sizeof(T)), x[c]);
           else
-            quantize_vals2_warp(x[r], reinterpret_cast<uint32_t *>(dc[r]), ds[r], lane);
+            x[c][0] = x[c][1] = x[c][2] = x[c][3] = 0.f;
         }
+        quantize_vals_warp4<D>(x, dst >= 0 ? codes + dst * (D / 2) : nullptr, scales + (dst >= 0 ? dst : 0), lane);
       }
     } else {
-      quantize_vals_warp_n<D, 4>(x, dc, ds, lane);
+      // INT3 / INT2 (D = 128): the warp quantizes its rows one by one
+      const int tb = cache.bits == 3 ? 52 : 32;  // code bytes per row
+      int64_t bh_r = bh;
+      int i_r = i, h_r = h, b_r = b;
+#pragma unroll 1
+      for (int r = 0; r < kQWarpRows; ++r, ++i_r) {
+        if (i_r == n) {
+          i_r = 0, ++bh_r;
+          if (++h_r == cache.hkv) h_r = 0, ++b_r;
+        }
+        int64_t dst = span_row >= 0 ? span_row + r : -1;
+        if (span_row < 0 && got && rw + r < rows) dst = dest_row(cache, start_pos, b_r, h_r, bh_r, i_r, lane == 0, err);
+        if (dst < 0) continue;  // warp-uniform
+        float x[VPL];
+        lds_row<T, VPL>(stage + r * C::kRowBytes, lane, x);
+        if (cache.bits == 3)
+          quantize_vals3_warp(x, reinterpret_cast<uint32_t *>(codes + dst * tb), scales + dst, lane);
+        else
+          quantize_vals2_warp(x, reinterpret_cast<uint32_t *>(codes + dst * tb), scales + dst, lane);
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(empty + s));
   }
 }
 
-template <typename T, int D>
+template <typename T, int D, bool kInt4>
 cudaError_t launch_t(const void *k, const void *v, int batch, int n, const int32_t *start_pos,
                      const KvView &cache, uint32_t *err, int sms, cudaStream_t stream) {
   using C = QCfg<T, D>;
   static bool configured = false;  // per-function attribute, set once per process
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(quantize_kv_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmem);
+    cudaError_t e = cudaFuncSetAttribute(quantize_kv_kernel<T, D, kInt4>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
@@ -223,7 +280,7 @@ cudaError_t launch_t(const void *k, const void *v, int batch, int n, const int32
   if (rows == 0) return cudaSuccess;
   const int64_t blocks = 2 * ((rows + kQRows - 1) / kQRows);
   const int64_t grid = min(blocks, static_cast<int64_t>(kQCtasPerSm * (sms > 0 ? sms : 1)));
-  quantize_kv_kernel<T, D><<<static_cast<unsigned>(grid), kQThreads, C::kSmem, stream>>>(
+  quantize_kv_kernel<T, D, kInt4><<<static_cast<unsigned>(grid), kQThreads, C::kSmem, stream>>>(
       static_cast<const T *>(k), static_cast<const T *>(v), batch, n, start_pos, cache, err);
   return cudaGetLastError();
 }
@@ -233,11 +290,14 @@ cudaError_t launch_t(const void *k, const void *v, int batch, int n, const int32
 cudaError_t launch_quantize(const void *k, const void *v, bool fp16_in, int batch, int n,
                             const int32_t *start_pos, const KvView &cache, uint32_t *err, int sms,
                             cudaStream_t stream) {
+  if (cache.bits != 4)  // INT3 / INT2: D = 128 (checked by the caller)
+    return fp16_in ? launch_t<__half, 128, false>(k, v, batch, n, start_pos, cache, err, sms, stream)
+                   : launch_t<float, 128, false>(k, v, batch, n, start_pos, cache, err, sms, stream);
   if (cache.head_dim == 128)
-    return fp16_in ? launch_t<__half, 128>(k, v, batch, n, start_pos, cache, err, sms, stream)
-                   : launch_t<float, 128>(k, v, batch, n, start_pos, cache, err, sms, stream);
-  return fp16_in ? launch_t<__half, 64>(k, v, batch, n, start_pos, cache, err, sms, stream)
-                 : launch_t<float, 64>(k, v, batch, n, start_pos, cache, err, sms, stream);
+    return fp16_in ? launch_t<__half, 128, true>(k, v, batch, n, start_pos, cache, err, sms, stream)
+                   : launch_t<float, 128, true>(k, v, batch, n, start_pos, cache, err, sms, stream);
+  return fp16_in ? launch_t<__half, 64, true>(k, v, batch, n, start_pos, cache, err, sms, stream)
+                 : launch_t<float, 64, true>(k, v, batch, n, start_pos, cache, err, sms, stream);
 }
 
 }  // namespace qattn
