@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(kWarps * 32)
     combine_kernel(const float *__restrict__ po, const float *__restrict__ pl, int splits,
                    int64_t rows, uint16_t *__restrict__ out, float *__restrict__ lse) {
   pdl_wait();  // partials come from the preceding kernel on the stream
-  pdl_launch_dependents();  // a dependent writes nothing before its own wait
+  pdl_launch_dependents();  // before its own wait a dependent reads only sequence lengths (not written here)
   constexpr int VPL = D / 32;
   __shared__ float w[QATTN_MAX_SPLITS];
   __shared__ float red[kWarps];

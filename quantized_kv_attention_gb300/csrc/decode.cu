@@ -374,37 +374,15 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
     prefetch_tmap(&maps.ks);
     prefetch_tmap(&maps.vs);
   }
-  // Speculative L2 prefetch of this range's first stages, as if every
-  // sequence held max_len keys (the common case), issued before the lengths
-  // are known; the real loads follow the lengths.  Byte counts stay inside
-  // the cache (capacity), so a wrong guess only costs bandwidth.
-  if (!paged && threadIdx.x == kConsumerWarps * 32 + 1) {
-    const int64_t per = (static_cast<int64_t>(min(a.max_len, static_cast<int>(cache.capacity))) + geo.tokens - 1) / geo.tokens;
-    if (per > 0) {
-      // the cost-balanced ranges of B * groups segments of `per` stages
-      const int64_t sc = kSegCost<W>, L = sc + kUnit * per, Wg = static_cast<int64_t>(B) * geo.groups * L;
-      auto start = [&](int64_t i) {
-        const int64_t t = cost_target(i, Wg, gridDim.x), sg = t / L;
-        return t >= Wg ? static_cast<int64_t>(B) * geo.groups * per : sg * per + stage_at(t - sg * L, sc);
-      };
-      const int64_t g0 = start(blockIdx.x), g1 = start(blockIdx.x + 1);
-      for (int k = 0; k < 2 && g0 + k < g1; ++k) {
-        const int64_t gs = g0 + k, sg = gs / per;
-        const int64_t tok0 = (gs - sg * per) * geo.tokens;
-        const int64_t head = (sg / geo.groups) * hkv + (sg % geo.groups) * geo.hb;
-        const int64_t ntok = min(static_cast<int64_t>(geo.tokens), cache.capacity - tok0);
-        const int64_t row = head * cache.capacity + tok0;
-        const uint32_t cb = static_cast<uint32_t>(ntok * C::kTokBytes), sb = static_cast<uint32_t>(ntok * 2);
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cache.k_codes + row * C::kTokBytes), "r"(cb) : "memory");
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cache.v_codes + row * C::kTokBytes), "r"(cb) : "memory");
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cache.k_scales + row), "r"(sb) : "memory");
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cache.v_scales + row), "r"(sb) : "memory");
-      }
-    }
-  }
-  pdl_wait();                // inputs may come from the preceding kernel on the stream
-  pdl_launch_dependents();   // the merge kernel may be scheduled as SMs free up
 
+  // Before the programmatic wait below, the kernels that may still be running
+  // are this library's decode, merge and combine kernels of earlier calls on
+  // the stream (the only ones that release their dependents early).  They
+  // write cache rows (the fused append), partials, out and lse, never the
+  // sequence lengths or the page table: so the lengths, the stage prefix and
+  // this CTA's range are computed here, and its first stages are prefetched
+  // into L2 (the point of coherence: a later write still wins).  Q and the
+  // cache rows are read only after the wait.
   // prefix[b]: first global stage of sequence b (all its head groups)
   for (int b = threadIdx.x; b < B; b += kThreads) {
     int len = __ldg(a.seq_lens + b);
@@ -447,6 +425,23 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
   __syncthreads();
   const int64_t gs0 = range[0], gs1 = range[1];
   if (gs1 <= gs0) return;
+  // L2 prefetch of the range's first two stages while a preceding kernel may
+  // still run (L2 is the coherence point: a later write still wins)
+  if (!paged && threadIdx.x == kConsumerWarps * 32 + 1) {
+    for (int k = 0; k < 2 && gs0 + k < gs1; ++k) {
+      const Loc l = locate(gs0 + k, prefix, B, geo.groups);
+      const int64_t tok0 = static_cast<int64_t>(l.s) * geo.tokens;
+      const int64_t ntok = min(static_cast<int64_t>(geo.tokens), cache.capacity - tok0);
+      const int64_t row = (static_cast<int64_t>(l.b) * hkv + l.hg * geo.hb) * cache.capacity + tok0;
+      const uint32_t cb = static_cast<uint32_t>(ntok * C::kTokBytes), sb = static_cast<uint32_t>(ntok * 2);
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cache.k_codes + row * C::kTokBytes), "r"(cb) : "memory");
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cache.v_codes + row * C::kTokBytes), "r"(cb) : "memory");
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cache.k_scales + row), "r"(sb) : "memory");
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(cache.v_scales + row), "r"(sb) : "memory");
+    }
+  }
+  pdl_wait();                // cache rows and Q may come from the preceding kernel on the stream
+  pdl_launch_dependents();   // the merge kernel may be scheduled as SMs free up
 
   if (warp >= kConsumerWarps) {
     // ------------------------------------------------------------ producer
@@ -1086,8 +1081,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4)
   const int r = blockIdx.y;  // row within the segment: kv-head r / G, q-head r % G
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // A programmatic dependent (the next decode on the stream) may be scheduled
-  // now: it writes nothing before its own wait, which ends only once this
-  // grid has completed, so its set-up and L2 prefetch overlap this merge.
+  // now: before its own wait, which ends only once this grid has completed,
+  // it reads only the sequence lengths and computes its range (nothing this
+  // kernel writes) and prefetches into L2, so that work overlaps this merge.
   pdl_launch_dependents();
   // The decode kernel triggers this launch only after its own wait on the
   // inputs, so the lengths are final here; its partials are read after pdl_wait.
