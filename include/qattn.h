@@ -192,6 +192,33 @@ size_t qattn_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t n
                                    int32_t head_dim, int32_t max_seq_len, int32_t num_splits);
 
 /*
+ * qattn_decode_plan -- the launch shape that qattn_decode and
+ * qattn_decode_append (and qattn_decode_noalloc) take for these sizes on the
+ * current device.  Split-KV decoding ([TA] §2.1 over [QCA] §3.3's split-K
+ * partials, merged by the log-sum-exp rule of [TA] §2.2) runs one of two ways:
+ *   cluster = 0   cost-balanced key ranges over `ctas` CTAs, the partials
+ *                 merged by a second kernel (paged caches, listed caches,
+ *                 an explicit num_splits, INT3 / INT2, or shapes whose
+ *                 clusters would leave most SMs idle);
+ *   cluster = S   one thread-block cluster of S CTAs (2 <= S <= 16) per
+ *                 (sequence, kv-head group), ctas = batch * groups * S, the
+ *                 S partials merged through distributed shared memory in the
+ *                 same kernel; chosen when num_splits is 0, the cache is
+ *                 contiguous INT4 without kv_head_index, every cluster can be
+ *                 resident at once and the grid covers at least 80 % of the
+ *                 SMs.
+ *   warps  consumer warps per CTA (8: 256-row stages; 12: 384-token stages)
+ *   paged  nonzero for a paged cache; code_bits 4, 3 or 2;
+ *   has_kv_head_index  nonzero for a listed cache
+ * The three outputs are host pointers (any may be NULL).  Host-only: reads
+ * device attributes and occupancy, launches nothing.  Errors:
+ * QATTN_ERR_INVALID_ARG for sizes qattn_decode would reject.
+ */
+qattn_status qattn_decode_plan(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t max_seq_len, int32_t num_splits, int32_t paged, int32_t code_bits,
+                               int32_t has_kv_head_index, int32_t *warps, int32_t *ctas, int32_t *cluster);
+
+/*
  * qattn_decode -- one query token per sequence against its whole cache
  * ([TA] §2.1 decoding; fused in-SRAM dequantization as in [QCA] §3.1).
  *

@@ -6,6 +6,7 @@ stream.  The calls mirror the C ABI in include/qattn.h:
 
     quantize_kv(k, v, cache, start_pos=None)          quantize-on-append
     decode(q, cache, seq_lens, max_seq_len, scale)    one query per sequence
+    decode_plan(batch, Hq, Hkv, D, max_len, splits) the launch shape a decode takes
     prefill(q, cache, nq, nk, scale, causal)          Nq queries per sequence
     combine(partial_o, partial_lse)                   log-sum-exp merge
     dequantize_kv, decode_fp16, prefill_fp16          the comparison paths (FP16 cache;
@@ -44,7 +45,7 @@ EXPORTS = (
     "qattn_flashq_init", "qattn_flashq_append", "qattn_flashq_attend", "qattn_flashq_flush",
     "qattn_headwise_plan", "qattn_dequantize_kv", "qattn_decode_fp16_workspace_size", "qattn_decode_fp16",
     "qattn_prefill_fp16", "qattn_pq_quantize", "qattn_decode_pq_workspace_size", "qattn_decode_pq",
-    "qattn_flashq_flush_pq",
+    "qattn_flashq_flush_pq", "qattn_decode_plan",
 )
 
 
@@ -120,6 +121,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     sig = {
         "qattn_quantize_kv": (i32, [vp, vp, i32, i32, i32, vp, cache_p, vp]),
         "qattn_decode_workspace_size": (sz, [i32, i32, i32, i32, i32, i32]),
+        "qattn_decode_plan": (i32, [i32, i32, i32, i32, i32, i32, i32, i32, i32, vp, vp, vp]),
         "qattn_decode": (i32, [vp, cache_p, vp, i32, i32, i32, f32, i32, vp, sz, vp, vp, vp]),
         "qattn_prefill": (i32, [vp, cache_p, i32, i32, i32, i32, f32, i32, vp, vp, vp]),
         "qattn_combine": (i32, [vp, vp, i32, i64, i32, vp, vp, vp]),
@@ -256,6 +258,18 @@ def quantize_kv(k: torch.Tensor, v: torch.Tensor, cache: KvCache,
 def decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len, num_splits=0) -> int:
     return int(load_library().qattn_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
                                                           max_seq_len, num_splits))
+
+
+def decode_plan(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len, num_splits=0, paged=False, code_bits=4,
+                listed=False) -> dict:
+    """The launch shape of a decode call on the current device: consumer warps
+    per CTA, CTAs, and the segment-cluster size (0: cost-balanced ranges and a
+    merge kernel)."""
+    w, n, c = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _check(load_library().qattn_decode_plan(batch, num_q_heads, num_kv_heads, head_dim, max_seq_len, num_splits,
+                                            int(paged), code_bits, int(listed), ctypes.byref(w), ctypes.byref(n),
+                                            ctypes.byref(c)), "qattn_decode_plan")
+    return {"warps": w.value, "ctas": n.value, "cluster": c.value}
 
 
 def decode(q: torch.Tensor, cache: KvCache, seq_lens: torch.Tensor, max_seq_len: int,

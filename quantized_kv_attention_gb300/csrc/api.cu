@@ -278,6 +278,28 @@ qattn_status qattn_headwise_plan(const void *k, const void *v, qattn_dtype x_dty
   return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "headwise plan launch");
 }
 
+qattn_status qattn_decode_plan(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t max_seq_len, int32_t num_splits, int32_t paged, int32_t code_bits,
+                               int32_t has_kv_head_index, int32_t *warps, int32_t *ctas, int32_t *cluster) {
+  if (batch <= 0 || batch > QATTN_MAX_BATCH || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      num_q_heads % num_kv_heads || num_q_heads / num_kv_heads > QATTN_MAX_GROUP || max_seq_len < 0 ||
+      num_splits < 0 || num_splits > QATTN_MAX_SPLITS || (head_dim != 64 && head_dim != 128) ||
+      (code_bits != 4 && code_bits != 3 && code_bits != 2) || !hkv_supported(num_kv_heads, paged != 0))
+    return fail(QATTN_ERR_INVALID_ARG, "decode plan: invalid sizes");
+  DeviceState *ds;
+  qattn_status st = device_state(&ds);
+  if (st != QATTN_OK) return st;
+  const int w = decode_layout(batch, num_kv_heads, max_seq_len, paged != 0, num_splits > 0 ? num_splits : ds->sms);
+  int n = plan_ctas(batch, num_kv_heads, head_dim, max_seq_len, num_splits, ds->sms, paged != 0, w);
+  const int S = decode_cluster(head_dim, w, code_bits, num_splits == 0, paged != 0, has_kv_head_index != 0, batch,
+                               num_kv_heads, max_seq_len, ds->sms);
+  if (S > 0) n = batch * decode_geometry(head_dim, num_kv_heads, false, w).groups * S;
+  if (warps) *warps = w;
+  if (ctas) *ctas = n;
+  if (cluster) *cluster = S;
+  return QATTN_OK;
+}
+
 size_t qattn_decode_workspace_size(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                    int32_t head_dim, int32_t max_seq_len, int32_t num_splits) {
   if (batch <= 0 || batch > QATTN_MAX_BATCH || num_q_heads <= 0 || num_kv_heads <= 0 ||
@@ -374,6 +396,7 @@ qattn_status decode_impl(const uint16_t *q, const void *k_new, const void *v_new
   a.max_len = max_seq_len;
   a.batch = batch, a.hq = num_q_heads, a.ctas = ctas, a.warps = warps;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.auto_splits = num_splits == 0, a.sms = ds->sms, a.cluster = 0;
   cudaError_t e = launch_decode(a, view, maps, ds->status, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QATTN_OK : cuda_fail(e, "decode launch");
 }

@@ -27,6 +27,16 @@
 // by decode_merge_kernel (launched as a programmatic dependent, small enough
 // to be resident beside the decode CTAs).
 //
+// Segment clusters.  When the split count is left to the library and the
+// cache is contiguous INT4 without a head map, every segment may instead get
+// a thread-block cluster of S CTAs (S = min(16, SMs / segments, stages); kept
+// only if all clusters fit at once and cover at least 80 % of the SMs): CTA
+// rank r takes the segment's stages [r n / S, (r + 1) n / S), leaves its
+// normalised partial in its own Q slot, and after a cluster barrier the CTAs
+// merge the S partials through distributed shared memory, each a share of the
+// output columns -- no merge kernel, no partials in global memory, and the
+// next call's CTAs can start as soon as SMs free up (decode_kernel<..., true>).
+//
 // CTA roles (W = 8 or 12 consumer warps).
 //   producer    one elected thread of warp W issues the stage's TMA loads
 //               into a 6-deep (W = 8) or 4-deep (W = 12) mbarrier ring; with
@@ -66,6 +76,10 @@ constexpr float kTwo24 = 16777216.0f;
 //   W = 12  stages of 384 tokens of one kv-head (contiguous caches), three
 //           consumer warps per SM sub-partition; a producer warpgroup whose
 //           registers go to the consumers (setmaxnreg: 3 x 160 + 32 = 4 x 128)
+// Largest segment cluster (CTAs that share one segment and merge through
+// distributed shared memory): 16, a non-portable cluster size.
+constexpr int kMaxCluster = 16;
+
 template <int W>
 struct Layout {
   static constexpr int kConsumerWarps = W;
@@ -324,7 +338,55 @@ struct Maps {
   CUtensorMap k, v, ks, vs;
 };
 
-template <int D, int W, int BITS = 4>
+// ---------------------------------------------- segment cluster: merge CTAs
+// Every thread of every CTA of the cluster reaches both cluster barriers once
+// (the producer warps after their loads; `threads` consumer threads here).
+// Between them, the segment's rows x D/4 float4 columns are shared out over
+// the cluster; each reads the S partials (O rows, then the lse in log2 units,
+// in the CTAs' Q slots) and writes out, lse.
+template <int D>
+__device__ __forceinline__ void cluster_merge(const DecodeArgs &a, const StageGeo &geo, int G, __half *qslot, bool empty,
+                                           int threads) {
+  const int S = a.cluster, rows = geo.hb * G;
+  float *xo = reinterpret_cast<float *>(qslot);
+  float *xl = xo + QATTN_MAX_GROUP * D;
+  if (empty)  // no stage in this CTA: an empty partial
+    for (int r = threadIdx.x; r < rows; r += threads) xl[r] = -INFINITY;
+  cluster_sync();
+  const uint32_t rank = cluster_rank();
+  const int sg = blockIdx.x / S, b = sg / geo.groups, hg = sg - b * geo.groups;
+  const uint32_t xo_a = smem_u32(xo), xl_a = smem_u32(xl);
+  for (int it = static_cast<int>(rank) + S * threadIdx.x; it < rows * (D / 4); it += S * threads) {
+    const int r = it / (D / 4), d = (it - r * (D / 4)) * 4;
+    float lv[kMaxCluster];
+    float M = -INFINITY;
+#pragma unroll
+    for (int p = 0; p < kMaxCluster; ++p) {
+      lv[p] = p < S ? ld_dsmem_f32(dsmem_addr(xl_a + 4 * r, p)) : -INFINITY;
+      M = fmaxf(M, lv[p]);
+    }
+    float Z = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int p = 0; p < kMaxCluster; ++p) {
+      if (p < S && lv[p] != -INFINITY) {
+        const float w = ex2(lv[p] - M);
+        const float4 v = ld_dsmem_f32x4(dsmem_addr(xo_a + 4 * (r * D + d), p));
+        Z += w;
+        acc.x += w * v.x, acc.y += w * v.y, acc.z += w * v.z, acc.w += w * v.w;
+      }
+    }
+    const bool live = Z > 0.f;
+    const float inv = live ? 1.f / Z : 0.f;
+    const int64_t row = static_cast<int64_t>(b) * a.hq + (hg * geo.hb + r / G) * G + r % G;
+    const uint32_t h01 = pack_half2(acc.x * inv, acc.y * inv), h23 = pack_half2(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2 *>(a.out + row * D + d) = make_uint2(h01, h23);
+    if (d == 0 && a.lse) a.lse[row] = live ? (M + log2f(Z)) * 0.69314718055994531f : -INFINITY;
+  }
+  cluster_sync();  // the other CTAs have read this CTA's partial
+}
+
+template <int D, int W, int BITS = 4, bool kCluster = false>
 __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
     decode_kernel(DecodeArgs a, KvView cache, const __grid_constant__ Maps maps, uint32_t *err) {
   using C = Cfg<D, W, BITS>;
@@ -421,10 +483,22 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
   // The range is computed once per CTA, by two lanes of warp 0, and shared:
   // every thread computing it would keep the SM's issue slots busy with the
   // same divisions for longer than the extra barrier takes.
-  if (warp == 0 && lane < 2) range[lane] = cost_start(blockIdx.x + lane, gridDim.x, Wc, prefix, nzp, B, geo.groups, sc);
+  // With segment clusters (a.cluster = S CTAs per (sequence, head group)
+  // segment, CTAs k S .. k S + S - 1 forming cluster k), CTA rank r takes the
+  // segment's stages [r n / S, (r + 1) n / S).
+  if (warp == 0 && lane < 2) {
+    if constexpr (kCluster) {
+      const int S = a.cluster, sg = blockIdx.x / S, rk = blockIdx.x - sg * S + lane;
+      const int b = sg / geo.groups, hg = sg - b * geo.groups;
+      const int n = (prefix[b + 1] - prefix[b]) / geo.groups;
+      range[lane] = prefix[b] + static_cast<int64_t>(hg) * n + static_cast<int64_t>(rk) * n / S;
+    } else {
+      range[lane] = cost_start(blockIdx.x + lane, gridDim.x, Wc, prefix, nzp, B, geo.groups, sc);
+    }
+  }
   __syncthreads();
   const int64_t gs0 = range[0], gs1 = range[1];
-  if (gs1 <= gs0) return;
+  if (!kCluster && gs1 <= gs0) return;  // (a cluster's CTAs all meet at its merge)
   // L2 prefetch of the range's first two stages while a preceding kernel may
   // still run (L2 is the coherence point: a later write still wins)
   if (!paged && threadIdx.x == kConsumerWarps * 32 + 1) {
@@ -448,6 +522,8 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
     // (layout W = 12: a warpgroup whose registers go to the consumers; one
     // thread of its first warp issues the loads)
     if constexpr (Layout<W>::kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Layout<W>::kRegsProducer));
+    // the loads; every way out of them (an abort included) reaches the
+    // cluster barriers below
     if (warp == kConsumerWarps && lane == 0) {
       const int rows_per_tok = C::kTokBytes;  // code bytes per token
       const uint32_t qbytes = geo.hb * G * D * 2;
@@ -462,7 +538,7 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
           if (seg >= 1 && !mbar_wait(smem_u32(qempty), (seg & 1) ^ 1, err,
                                      *abort_flag ? kDrainCycles : kWaitCycles)) {
             *abort_flag = 1;
-            return;
+            goto producer_done;
           }
           const uint32_t qf = smem_u32(qfull);
           int mh = model_head(cache.head_map, cache.model_hkv, l.hg * geo.hb);
@@ -479,13 +555,13 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
           if (it >= C::kStages &&
               !mbar_wait(smem_u32(empty + s), ph ^ 1, err, *abort_flag ? kDrainCycles : kWaitCycles)) {
             *abort_flag = 1;  // stop issuing; the consumers drain with short waits
-            return;
+            goto producer_done;
           }
           if (!rows_in && l.s + j == l.n - 1) {  // a segment's last stage holds its new rows
             rows_in = true;
             if (!mbar_wait(smem_u32(appended), 0, err, *abort_flag ? kDrainCycles : kWaitCycles)) {
               *abort_flag = 1;
-              return;
+              goto producer_done;
             }
           }
           const int tok0 = (l.s + j) * geo.tokens;  // first token of the stage in the sequence
@@ -554,6 +630,12 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
         }
         gs += cnt;
       }
+    }
+  producer_done:
+    if constexpr (kCluster) {  // the consumers' two cluster barriers, met by this warp too
+      __syncwarp();
+      cluster_sync();
+      cluster_sync();
     }
     return;
   } else {  // each role sets its register budget inside its own branch
@@ -997,7 +1079,7 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
       sml[warp * 8 + 2 * c] = l0, sml[warp * 8 + 2 * c + 1] = l1;
     }
     consumer_sync<W>();
-    const bool complete = l.s == 0 && cnt == l.n;
+    const bool complete = !kCluster && l.s == 0 && cnt == l.n;
     const int64_t pslot = l.s > 0 ? 2 * static_cast<int64_t>(blockIdx.x) : 2 * static_cast<int64_t>(blockIdx.x) + 1;
     // One thread per (row, 4 consecutive d): the row's warp weights
     // 2^(m_w - M) are computed once per thread, then 4 columns are folded
@@ -1038,6 +1120,13 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
         const uint32_t h01 = pack_half2(acc.x * inv, acc.y * inv), h23 = pack_half2(acc.z * inv, acc.w * inv);
         *reinterpret_cast<uint2 *>(a.out + row * D + d) = make_uint2(h01, h23);
         if (d == 0 && a.lse) a.lse[row] = lse_v;
+      } else if (kCluster) {
+        // the cluster merge's input, in this CTA's Q slot (free once Q is in
+        // registers; a cluster CTA has one segment): O rows, then the lse in
+        // log2 units
+        float *xo = reinterpret_cast<float *>(qslot);
+        *reinterpret_cast<float4 *>(xo + r * D + d) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        if (d == 0) xo[QATTN_MAX_GROUP * D + r] = live ? M + log2f(L) : -INFINITY;
       } else {
         const int64_t prow = pslot * geo.hb * G + r;
         *reinterpret_cast<float4 *>(a.partial_o + prow * D + d) =
@@ -1049,6 +1138,7 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
     if (lane == 0) mbar_arrive(smem_u32(empty + last));
     gs += cnt;
   }
+  if constexpr (kCluster) cluster_merge<D>(a, geo, G, qslot, gs1 <= gs0, kConsumerWarps * 32);
   }
 }
 
@@ -1196,31 +1286,98 @@ cudaLaunchAttribute pdl_attr() {
   return attr;
 }
 
+// Segment clusters: with the split count left to the library, a contiguous
+// cache without a head map, and at least two stages for each CTA, every
+// (sequence, head group) segment gets a cluster of S = min(16, SMs /
+// segments, stages) CTAs that merge through distributed shared memory: no
+// merge kernel, no partials in global memory.  Taken only when every cluster
+// of the grid can be resident at once (cudaOccupancyMaxActiveClusters, at the
+// largest shared-memory size) and the grid covers at least 80 % of the SMs,
+// else the cost-balanced ranges.
+template <int D, int W, int BITS>
+int cluster_size(bool auto_splits, bool paged, bool head_map, int batch, int hkv, int64_t max_len, int sms) {
+  if (BITS != 4 || !auto_splits || paged || head_map) return 0;
+  const StageGeo geo = stage_geo<W>(hkv, false);
+  const int64_t segments = static_cast<int64_t>(batch) * geo.groups;
+  const int64_t stages = (max_len + geo.tokens - 1) / geo.tokens;
+  int64_t S = min(static_cast<int64_t>(kMaxCluster), min(sms / max(segments, int64_t(1)), stages));
+  static int fits[kMaxCluster + 1] = {};  // per S: 0 unknown, else 1 + the resident clusters
+  for (; S >= 2; --S) {
+    if (fits[S] == 0) {
+      cudaLaunchAttribute at;
+      at.id = cudaLaunchAttributeClusterDimension;
+      at.val.clusterDim.x = static_cast<unsigned>(S), at.val.clusterDim.y = 1, at.val.clusterDim.z = 1;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(static_cast<unsigned>(S));
+      cfg.blockDim = dim3(Layout<W>::kThreads);
+      cfg.dynamicSmemBytes = smem_bytes<D, W, BITS>(QATTN_MAX_BATCH);
+      cfg.attrs = &at;
+      cfg.numAttrs = 1;
+      int n = 0;
+      cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, W, BITS, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           smem_bytes<D, W, BITS>(QATTN_MAX_BATCH));
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(decode_kernel<D, W, BITS, true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, decode_kernel<D, W, BITS, true>, &cfg);
+      if (e != cudaSuccess) {
+        cudaGetLastError();  // not an error of the call: the cost-balanced ranges are taken
+        n = 0;
+      }
+      fits[S] = n + 1;
+    }
+    if (fits[S] - 1 >= segments)  // taken only if the clusters cover most of the SMs
+      return 5 * segments * S >= 4 * static_cast<int64_t>(sms) ? static_cast<int>(S) : 0;
+  }
+  return 0;
+}
+
 template <int D, int W, int BITS = 4>
-cudaError_t launch_d(const DecodeArgs &a, const KvView &cache, const DecodeMaps &dm, uint32_t *err,
+cudaError_t launch_d(const DecodeArgs &a0, const KvView &cache, const DecodeMaps &dm, uint32_t *err,
                      cudaStream_t stream) {
-  static bool configured = false;  // per-function attribute, set once per process
+  static bool configured = false;  // per-function attributes, set once per process
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<D, W, BITS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          smem_bytes<D, W, BITS>(QATTN_MAX_BATCH));
+    if constexpr (BITS == 4) {  // the segment-cluster form (INT4 only)
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(decode_kernel<D, W, BITS, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 smem_bytes<D, W, BITS>(QATTN_MAX_BATCH));
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(decode_kernel<D, W, BITS, true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    }
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  const int G = a.hq / cache.model_hkv;
+  const int G = a0.hq / cache.model_hkv;
   const bool paged = cache.page_table != nullptr;
   const StageGeo geo = stage_geo<W>(cache.hkv, paged);
+  DecodeArgs a = a0;
+  a.cluster = 0;
+  if constexpr (BITS == 4)
+    a.cluster = cluster_size<D, W, BITS>(a0.auto_splits != 0, paged, cache.head_map != nullptr, a0.batch, cache.hkv,
+                                         min(static_cast<int64_t>(a0.max_len), cache.capacity), a0.sms);
+  if (a.cluster > 0) a.ctas = a.batch * geo.groups * a.cluster;
   Maps maps;
   maps.k = dm.k, maps.v = dm.v, maps.ks = dm.ks, maps.vs = dm.vs;
-  cudaLaunchAttribute attr[1] = {pdl_attr()};
+  cudaLaunchAttribute attr[2] = {pdl_attr(), pdl_attr()};
+  if (a.cluster > 0) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(a.cluster), attr[1].val.clusterDim.y = 1, attr[1].val.clusterDim.z = 1;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.ctas);
   cfg.blockDim = dim3(Layout<W>::kThreads);
   cfg.dynamicSmemBytes = smem_bytes<D, W, BITS>(a.batch);
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<D, W, BITS>, a, cache, maps, err);
-  if (e != cudaSuccess) return e;
+  cfg.numAttrs = a.cluster > 0 ? 2 : 1;
+  cudaError_t e;
+  if constexpr (BITS == 4)
+    e = a.cluster > 0 ? cudaLaunchKernelEx(&cfg, decode_kernel<D, W, BITS, true>, a, cache, maps, err)
+                      : cudaLaunchKernelEx(&cfg, decode_kernel<D, W, BITS>, a, cache, maps, err);
+  else
+    e = cudaLaunchKernelEx(&cfg, decode_kernel<D, W, BITS>, a, cache, maps, err);
+  if (e != cudaSuccess || a.cluster > 0) return e;
   const int64_t limit = cache.page_table ? static_cast<int64_t>(cache.max_pages) * kPage : cache.capacity;
   cudaLaunchConfig_t mc = {};
   mc.gridDim = dim3(a.batch * geo.groups, geo.hb * G);
@@ -1256,6 +1413,16 @@ DecodeGeometry decode_geometry(int head_dim, int hkv, bool paged, int warps) {
   r.box_tokens = paged ? (g.tokens > kPage ? kPage : g.tokens) : (g.tokens > 256 ? g.tokens / 2 : g.tokens);
   r.box_rows = (paged ? r.box_tokens : g.tokens) * head_dim / 256;
   return r;
+}
+
+int decode_cluster(int head_dim, int warps, int bits, bool auto_splits, bool paged, bool head_map, int batch,
+                   int hkv, int64_t max_len, int sms) {
+  if (bits != 4) return 0;
+  if (head_dim == 128)
+    return warps == 8 ? cluster_size<128, 8, 4>(auto_splits, paged, head_map, batch, hkv, max_len, sms)
+                      : cluster_size<128, 12, 4>(auto_splits, paged, head_map, batch, hkv, max_len, sms);
+  return warps == 8 ? cluster_size<64, 8, 4>(auto_splits, paged, head_map, batch, hkv, max_len, sms)
+                    : cluster_size<64, 12, 4>(auto_splits, paged, head_map, batch, hkv, max_len, sms);
 }
 
 cudaError_t launch_decode(const DecodeArgs &a, const KvView &cache, const DecodeMaps &maps, uint32_t *err,

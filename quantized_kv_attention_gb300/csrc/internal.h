@@ -67,6 +67,9 @@ struct DecodeArgs {
   int batch, hq, ctas;
   int warps;         // CTA layout: 8 or 12 consumer warps (decode_layout)
   float scale_log2;  // softmax_scale * log2(e)
+  int auto_splits;   // the caller left the split count to the library
+  int sms;           // SM count of the device
+  int cluster;       // set by launch_decode: CTAs per segment cluster (0: cost-balanced ranges + merge kernel)
 };
 struct DecodeGeometry {
   int heads_per_stage, tokens_per_stage, groups;
@@ -78,6 +81,10 @@ struct DecodeGeometry {
 // split count, or the SM count for the automatic choice.
 int decode_layout(int batch, int hkv, int max_len, bool paged, int ranges);
 DecodeGeometry decode_geometry(int head_dim, int hkv, bool paged, int warps);
+// Segment-cluster size of a decode launch (0: cost-balanced ranges and the
+// merge kernel); see launch_decode.  Host-only.
+int decode_cluster(int head_dim, int warps, int bits, bool auto_splits, bool paged, bool head_map, int batch,
+                   int hkv, int64_t max_len, int sms);
 struct DecodeMaps {
   CUtensorMap k, v, ks, vs;  // codes 3-D [heads][rows][128 B], scales 2-D [heads][tokens]
 };
