@@ -164,8 +164,10 @@ struct Cq {
   static constexpr int kMergeBytes = kWq * 8 * kPitch * 4;
   static constexpr int kSmem = kStages * kStageBytes + kWq * 2 * kTileBytes + kMergeBytes + 2 * kWq * 8 * 4 +
                                2 * kStages * 8 + 16 + 1024;
-  // the rebuild: a lane keeps 8 channels of kTokLane tokens
-  static constexpr int kLanesRow = D / 8, kTokLane = 16 / (32 / kLanesRow);
+  // the rebuild: a lane keeps 8 channels of kTokLane tokens, the warp's
+  // kGroups lane groups taking interleaved tokens (the groups' code rows then
+  // sit D/2 bytes apart: distinct banks)
+  static constexpr int kLanesRow = D / 8, kGroups = 32 / kLanesRow, kTokLane = 16 / kGroups;
 };
 
 __device__ __forceinline__ void ldsm4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
@@ -321,8 +323,8 @@ __global__ void __launch_bounds__(kThreadsPq, 1)
   for (int mt = 0; mt < kMt; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   const uint32_t ktile = smem_u32(tiles + warp * 2 * C::kTileBytes), vtile = ktile + C::kTileBytes;
   // the rebuild: lane keeps channels 8 (lane % kLanesRow) .. + 7 of tokens
-  // (lane / kLanesRow) * kTokLane .. + kTokLane - 1 of the warp's 16
-  const int rch = 8 * (lane % C::kLanesRow), rtok = (lane / C::kLanesRow) * C::kTokLane;
+  // rgrp, rgrp + kGroups, ... of the warp's 16 (rgrp = lane / kLanesRow)
+  const int rch = 8 * (lane % C::kLanesRow), rgrp = lane / C::kLanesRow;
   const int mq = lane >> 3;
   const int ktok = (lane & 7) + (mq & 1) * 8, kch = mq >> 1;   // ldmatrix rows of K (non-transposed)
   const int vtok = (lane & 7) + (mq >> 1) * 8, vch = mq & 1;   // and of V (transposed)
@@ -345,14 +347,14 @@ __global__ void __launch_bounds__(kThreadsPq, 1)
       for (int t = 0; t < 2; ++t) {  // K, V
         const uint32_t pr = t ? vp : kp;
         const Params8 p8 = params8(lds64(pr + rch), lds64(pr + D + rch));
-        const uint32_t codes = st + (t ? C::kVOff : C::kKOff) + wb * C::kCodeBytes + (wt + rtok) * (D / 2) + rch / 2;
+        const uint32_t codes = st + (t ? C::kVOff : C::kKOff) + wb * C::kCodeBytes + (wt + rgrp) * (D / 2) + rch / 2;
         const uint32_t tile = t ? vtile : ktile;
 #pragma unroll
         for (int i = 0; i < C::kTokLane; ++i) {
           uint32_t w;
-          asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(codes + i * (D / 2)));
+          asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(codes + i * C::kGroups * (D / 2)));
           const uint4 y = rebuild8(w, p8);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(wtile_addr<D>(tile, rtok + i, rch >> 3)),
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(wtile_addr<D>(tile, rgrp + i * C::kGroups, rch >> 3)),
                        "r"(y.x), "r"(y.y), "r"(y.z), "r"(y.w)
                        : "memory");
         }
