@@ -124,6 +124,10 @@ __global__ void __launch_bounds__(1024) flashq_append_kernel(const T *__restrict
 // buffered rows, p = 2^(S - m_b), O_b = sum p x~_V / l_b, lse_b =
 // (m_b + log2 l_b) ln 2; then merged with the (O_c, lse_c) already in out /
 // lse: L = log(e^lse_c + e^lse_b), O = e^(lse_c - L) O_c + e^(lse_b - L) O_b.
+// Launched as a programmatic dependent: the buffer part is done before the
+// wait -- the kernels that may still run then are this library's decode,
+// merge and combine kernels, which never write the buffer (the append
+// releases no dependent early) -- and out / lse after it.
 template <int D>
 __global__ void __launch_bounds__(128) flashq_attend_kernel(const uint16_t *__restrict__ q, FlashqView f, int batch,
                                                             int hq, float scale_log2, uint16_t *out, float *lse) {
@@ -167,19 +171,32 @@ __global__ void __launch_bounds__(128) flashq_attend_kernel(const uint16_t *__re
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-    if (lane == 0) mls[0] = m, mls[1] = l, mls[2] = lse[row];
+    if (lane == 0) mls[0] = m, mls[1] = l;
   }
+  __syncthreads();
+  constexpr int kCols = (D + 127) / 128;  // columns of O a thread keeps
+  float ob[kCols];
+#pragma unroll
+  for (int k = 0; k < kCols; ++k) {  // O_b
+    const int d = threadIdx.x + 128 * k;
+    float acc = 0.f;
+    if (d < D)
+      for (int t = 0; t < n; ++t) acc = fmaf(ps[t], static_cast<float>(cv[t][d]), acc);
+    ob[k] = acc * uv / mls[1];
+  }
+  pdl_wait();  // out and lse of the cache part come from the preceding kernel
+  if (threadIdx.x == 0) mls[2] = lse[row];
   __syncthreads();  // lse_c is read before it is overwritten below
   const float lse_b = (mls[0] + log2f(mls[1])) * 0.69314718055994531f, lse_c = mls[2];
   const float mx = fmaxf(lse_c, lse_b);
   const float wc = expf(lse_c - mx), wb = expf(lse_b - mx);  // e^-inf = 0 for an empty cache part
   const float z = wc + wb;
-  for (int d = threadIdx.x; d < D; d += blockDim.x) {  // O_b and the merge
-    float acc = 0.f;
-    for (int t = 0; t < n; ++t) acc = fmaf(ps[t], static_cast<float>(cv[t][d]), acc);
-    const float ob = acc * uv / mls[1];
+#pragma unroll
+  for (int k = 0; k < kCols; ++k) {  // the merge
+    const int d = threadIdx.x + 128 * k;
+    if (d >= D) continue;
     const float oc = __half2float(__ushort_as_half(out[row * D + d]));
-    out[row * D + d] = __half_as_ushort(__float2half_rn((wc * oc + wb * ob) / z));
+    out[row * D + d] = __half_as_ushort(__float2half_rn((wc * oc + wb * ob[k]) / z));
   }
   if (threadIdx.x == 0) lse[row] = mx + logf(z);
 }
@@ -261,11 +278,17 @@ cudaError_t launch_flashq_attend(const uint16_t *q, const FlashqView &f, int bat
                                  uint16_t *out, float *lse, cudaStream_t stream) {
   if (batch == 0) return cudaSuccess;
   const unsigned rows = static_cast<unsigned>(batch) * static_cast<unsigned>(hq);
-  if (f.head_dim == 128)
-    flashq_attend_kernel<128><<<rows, 128, 0, stream>>>(q, f, batch, hq, scale_log2, out, lse);
-  else
-    flashq_attend_kernel<64><<<rows, 128, 0, stream>>>(q, f, batch, hq, scale_log2, out, lse);
-  return cudaGetLastError();
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(rows);
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return f.head_dim == 128 ? cudaLaunchKernelEx(&cfg, flashq_attend_kernel<128>, q, f, batch, hq, scale_log2, out, lse)
+                           : cudaLaunchKernelEx(&cfg, flashq_attend_kernel<64>, q, f, batch, hq, scale_log2, out, lse);
 }
 
 cudaError_t launch_flashq_flush(const FlashqView &f, const KvView &c, const int32_t *cache_lens, int batch,
