@@ -378,7 +378,9 @@ qattn_status qattn_flashq_append(const void *k_new, const void *v_new, qattn_dty
  * (lse = -inf where those were empty): L = log(e^lse + e^lse_buf), out =
  * e^(lse - L) out + e^(lse_buf - L) O_buf.  q [batch, Hq, D] fp16, the same
  * query; GQA as in qattn_decode.  Sequences with an empty buffer are left as
- * they are. */
+ * they are.  The buffered rows are attended while the preceding decode on the
+ * stream may still run (a programmatic launch; out and lse are read after
+ * it completes), so q must not be that decode's out. */
 qattn_status qattn_flashq_attend(const uint16_t *q, const qattn_flashq_buffer *buf, int32_t batch,
                                  int32_t num_q_heads, float softmax_scale, uint16_t *out, float *lse,
                                  qattn_stream_t stream);
