@@ -16,15 +16,17 @@
 //                      channel), nibble packing by shuffles
 // decode_pq_kernel     split-KV decode, one CTA per (key range, sequence,
 //                      kv-head): a producer thread streams whole blocks
-//                      (two per stage: codes + parameter records) by bulk
-//                      copies into a ring; each of 8 consumer warps (4 per
-//                      block) rebuilds its 16 tokens' exact
+//                      (four per stage: codes + parameter records) by bulk
+//                      copies into a 2-deep ring; each of 16 consumer warps
+//                      (4 per block) rebuilds its 16 tokens' exact
 //                      integer values q1' in fp16 in a private swizzled tile
 //                      (the block's stage is released right after), then
 //                      S^T = q1'_K . Q^T by mma.sync (tokens on M), S scaled
 //                      by the block's s1_K, an online softmax, and
 //                      O^T += q1'_V^T . (P s1_V)^T; warps merge in shared
-//                      memory, ranges by the combine kernel.
+//                      memory laid over the ring, ranges by the combine
+//                      kernel.  The work is latency-bound: 16 warps an SM
+//                      measured faster than 12 and those than 8.
 #include <math.h>
 
 #include "../../include/qattn.h"
@@ -146,23 +148,25 @@ __global__ void __launch_bounds__(D) flashq_flush_pq_kernel(FlashqView f, PqView
 }
 
 // -------------------------------------------------------------------- decode
-constexpr int kWq = 8;                  // consumer warps, 16 tokens each: 4 per block, 2 blocks a stage
-constexpr int kBlocksPerStage = 2;
+constexpr int kWq = 16;                 // consumer warps, 16 tokens each: 4 per block, 4 blocks a stage
+constexpr int kBlocksPerStage = 4;
 constexpr int kThreadsPq = (kWq + 1) * 32;
 
 template <int D>
 struct Cq {
   static constexpr int kCodeBytes = kPqBlock * D / 2;       // one tensor's codes of a block
   static constexpr int kRec = 2 * D + 16;                   // one tensor's parameter record
-  // stage: K codes, V codes (2 blocks each), K records, V records (2 each)
+  // stage: K codes, V codes (4 blocks each), K records, V records (4 each)
   static constexpr int kKOff = 0, kVOff = kBlocksPerStage * kCodeBytes;
   static constexpr int kKpOff = 2 * kBlocksPerStage * kCodeBytes, kVpOff = kKpOff + kBlocksPerStage * kRec;
   static constexpr int kStageBytes = (kVpOff + kBlocksPerStage * kRec + 127) / 128 * 128;
-  static constexpr int kStages = D == 128 ? 6 : 10;
+  static constexpr int kStages = D == 128 ? 2 : 3;
   static constexpr int kTileBytes = 16 * D * 2;             // 16 tokens x D fp16
   static constexpr int kPitch = D + 4;
+  // the warps' merge area is laid over the ring once every stage is read
   static constexpr int kMergeBytes = kWq * 8 * kPitch * 4;
-  static constexpr int kSmem = kStages * kStageBytes + kWq * 2 * kTileBytes + kMergeBytes + 2 * kWq * 8 * 4 +
+  static_assert(kMergeBytes <= kStages * kStageBytes, "the merge area fits the ring");
+  static constexpr int kSmem = kStages * kStageBytes + kWq * 2 * kTileBytes + 2 * kWq * 8 * 4 +
                                2 * kStages * 8 + 16 + 1024;
   // the rebuild: a lane keeps 8 channels of kTokLane tokens, the warp's
   // kGroups lane groups taking interleaved tokens (the groups' code rows then
@@ -233,8 +237,8 @@ __global__ void __launch_bounds__(kThreadsPq, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *tiles = smem + C::kStages * C::kStageBytes;                     // [warp][K, V] tiles
-  float *mo = reinterpret_cast<float *>(tiles + kWq * 2 * C::kTileBytes);  // [warp][head][kPitch]
-  float *mm = mo + kWq * 8 * C::kPitch;
+  float *mo = reinterpret_cast<float *>(smem);  // [warp][head][kPitch], over the ring after the last stage
+  float *mm = reinterpret_cast<float *>(tiles + kWq * 2 * C::kTileBytes);
   float *ml = mm + kWq * 8;
   uint64_t *full = reinterpret_cast<uint64_t *>(ml + kWq * 8);
   uint64_t *empty = full + C::kStages;
@@ -413,6 +417,7 @@ __global__ void __launch_bounds__(kThreadsPq, 1)
     l0 += __shfl_xor_sync(0xffffffffu, l0, off);
     l1 += __shfl_xor_sync(0xffffffffu, l1, off);
   }
+  asm volatile("bar.sync 1, %0;" ::"n"(kWq * 32) : "memory");  // every warp is done with the ring
   float *mw = mo + warp * 8 * C::kPitch;
 #pragma unroll
   for (int mt = 0; mt < kMt; ++mt) {  // O^T carried s1_V * 2^-8: the 2^8 returns here
