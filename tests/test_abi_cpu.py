@@ -119,6 +119,23 @@ def test_workspace_size_host_arithmetic():
     assert qa.decode_workspace_size(4096, 8, 2, 128, 600, 4) == 0         # batch above the limit
 
 
+def test_decode_plan_rejects_bad_sizes():
+    # invalid sizes are refused on the host, before any device query
+    w, n, c = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    bad = [
+        (0, 8, 2, 128, 100, 0, 0, 4, 0),      # no sequence
+        (2, 8, 3, 128, 100, 0, 0, 4, 0),      # Hq not a multiple of Hkv
+        (2, 8, 2, 96, 100, 0, 0, 4, 0),       # head_dim
+        (2, 8, 2, 128, -1, 0, 0, 4, 0),       # negative max length
+        (2, 8, 2, 128, 100, 2000, 0, 4, 0),   # too many splits
+        (2, 8, 2, 128, 100, 0, 0, 5, 0),      # code bits
+        (2, 24, 6, 128, 100, 0, 1, 4, 0),     # paged Hkv = 6
+        (2, 72, 2, 128, 100, 0, 0, 4, 0),     # group above QATTN_MAX_GROUP
+    ]
+    for args in bad:
+        assert lib.qattn_decode_plan(*args, ctypes.byref(w), ctypes.byref(n), ctypes.byref(c)) == qa.QATTN_ERR_INVALID_ARG, args
+
+
 def test_wait_check_rejects_bad_arguments():
     assert lib.qattn_check_wait_timeout(None, 1000, None) == qa.QATTN_ERR_INVALID_ARG
     assert lib.qattn_check_wait_timeout(FAKE, 0, None) == qa.QATTN_ERR_INVALID_ARG
