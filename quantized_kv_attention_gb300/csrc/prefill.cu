@@ -79,13 +79,19 @@ struct Bars {
 };
 
 // Bounded mbarrier wait; the clock is read once every 32 polls so that a
-// waiting warp takes few issue slots from the working ones.
+// waiting warp takes few issue slots from the working ones.  kHinted polls
+// pass a 32 ns suspend-time hint: the MMA thread and the dequantization
+// warps resume sooner after the phase completes (about 1 % of the prefill);
+// the softmax warps keep the default suspension, which measured faster for
+// them.
+template <bool kHinted = false>
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint32_t *err,
                                            long long limit = kWaitCycles) {
-  if (mbar_try_wait(bar, parity)) return true;
+  auto poll = [&] { return kHinted ? mbar_try_wait_sleep(bar, parity, 32) : mbar_try_wait(bar, parity); };
+  if (poll()) return true;
   const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (poll()) return true;
     if ((it & 31u) == 0 && clock64() - t0 > limit) {
       atomicOr(err, kFlagWaitTimeout);
       return false;
@@ -352,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) umma_ts(d, p + kk * 8, vb + kk * (2048 >> 4), C::kIdescPV, kk > 0 ? 1u : acc0);
       };
-      if (ok) ok = wait_bounded(smem_u32(&bars->k_full[0]), 0, err);
+      if (ok) ok = wait_bounded<true>(smem_u32(&bars->k_full[0]), 0, err);
       if (ok) {
         tc_fence_after();
         issue_s(0, 0);
@@ -364,19 +370,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; ok && j < n; ++j) {
         const int vbuf = j % kKvBufs;
         const uint32_t par = (j / kKvBufs) & 1;
-        if (!(ok = wait_bounded(smem_u32(&bars->v_full[vbuf]), par, err))) break;
-        if (!(ok = wait_bounded(smem_u32(&bars->p_full[0]), j & 1, err))) break;
+        if (!(ok = wait_bounded<true>(smem_u32(&bars->v_full[vbuf]), par, err))) break;
+        if (!(ok = wait_bounded<true>(smem_u32(&bars->p_full[0]), j & 1, err))) break;
         tc_fence_after();
         issue_pv(0, j);
         const bool more = j + 1 < n;
         if (more) {
           const int kb = (j + 1) % kKvBufs;
-          if (!(ok = wait_bounded(smem_u32(&bars->k_full[kb]), ((j + 1) / kKvBufs) & 1, err))) break;
+          if (!(ok = wait_bounded<true>(smem_u32(&bars->k_full[kb]), ((j + 1) / kKvBufs) & 1, err))) break;
           tc_fence_after();
           issue_s(0, j + 1);
           tc_commit(smem_u32(&bars->s_full[0]));
         }
-        if (!(ok = wait_bounded(smem_u32(&bars->p_full[1]), j & 1, err))) break;
+        if (!(ok = wait_bounded<true>(smem_u32(&bars->p_full[1]), j & 1, err))) break;
         tc_fence_after();
         issue_pv(1, j);
         tc_commit(smem_u32(&bars->v_empty[vbuf]));
@@ -406,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int buf = j % kKvBufs;
         const uint32_t par = ((j / kKvBufs) & 1) ^ 1;
         if (tok_l == 0) {
-          if (j >= kKvBufs && !wait_bounded(smem_u32(&bars->k_empty[buf]), par, err)) break;
+          if (j >= kKvBufs && !wait_bounded<true>(smem_u32(&bars->k_empty[buf]), par, err)) break;
           const uint32_t kf = smem_u32(&bars->k_full[buf]);
           mbar_arrive_expect_tx(kf, C::kTileBytes);
           for (int sub = 0; sub < C::kSub; ++sub)
@@ -415,12 +421,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int slot = j % kScaleSlots;
         if (j >= kScaleSlots &&
-            !wait_bounded(smem_u32(&bars->sc_empty[slot]), ((j / kScaleSlots) & 1) ^ 1, err))
+            !wait_bounded<true>(smem_u32(&bars->sc_empty[slot]), ((j / kScaleSlots) & 1) ^ 1, err))
           break;
         scales[slot * kBN + tok_l] = j * kBN + tok_l < a.nk ? a.scale_log2 : 0.f;
         mbar_arrive(smem_u32(&bars->sc_full[slot]));
         if (tok_l == 0) {
-          if (j >= kKvBufs && !wait_bounded(smem_u32(&bars->v_empty[buf]), par, err)) break;
+          if (j >= kKvBufs && !wait_bounded<true>(smem_u32(&bars->v_empty[buf]), par, err)) break;
           const uint32_t vf = smem_u32(&bars->v_full[buf]);
           mbar_arrive_expect_tx(vf, C::kTileBytes);
           for (int sub = 0; sub < C::kSub; ++sub)
@@ -467,17 +473,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int buf = j % kKvBufs;
       const uint32_t par = ((j / kKvBufs) & 1) ^ 1;
-      if (j >= kKvBufs && !wait_bounded(smem_u32(&bars->k_empty[buf]), par, err)) break;
+      if (j >= kKvBufs && !wait_bounded<true>(smem_u32(&bars->k_empty[buf]), par, err)) break;
       store_row<D, false>(sbase + C::kKOff + buf * C::kTileBytes, tok_l, ck, sv);
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&bars->k_full[buf]));
       const int slot = j % kScaleSlots;
       if (j >= kScaleSlots &&
-          !wait_bounded(smem_u32(&bars->sc_empty[slot]), ((j / kScaleSlots) & 1) ^ 1, err))
+          !wait_bounded<true>(smem_u32(&bars->sc_empty[slot]), ((j / kScaleSlots) & 1) ^ 1, err))
         break;
       scales[slot * kBN + tok_l] = fk;
       mbar_arrive(smem_u32(&bars->sc_full[slot]));
-      if (j >= kKvBufs && !wait_bounded(smem_u32(&bars->v_empty[buf]), par, err)) break;
+      if (j >= kKvBufs && !wait_bounded<true>(smem_u32(&bars->v_empty[buf]), par, err)) break;
       store_row<D, true>(sbase + C::kVOff + buf * C::kTileBytes, tok_l, cv, sv);
       fence_proxy_async_smem();
       mbar_arrive(smem_u32(&bars->v_full[buf]));
