@@ -15,34 +15,12 @@ import numpy as np
 import pytest
 import torch
 
-from common import assert_close_attention, assert_close_lse, require_gpu
+from common import assert_close_attention, assert_close_lse, check_guards, guarded, require_gpu
 from oracle import attention as att
 from oracle import codec
 from quantized_kv_attention_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
-
-MARGIN = 4096  # elements of guard pattern on each side (16-byte multiples for fp16 and fp32)
-PATTERN = {torch.float16: (torch.int16, 0x5A5A), torch.float32: (torch.int32, 0x5A5A5A5A)}
-
-
-def guarded(shape, dtype):
-    """A device tensor of `shape` in the middle of a buffer whose margins hold PATTERN;
-    the tensor itself starts with the pattern too, so unwritten elements show."""
-    n = int(np.prod(shape))
-    ity, bits = PATTERN[dtype]
-    buf = torch.full((n + 2 * MARGIN,), bits, dtype=ity, device="cuda")
-    return buf, buf[MARGIN:MARGIN + n].view(dtype).view(*shape)
-
-
-def check_guards(buf, what):
-    ity = buf.dtype
-    bits = {torch.int16: 0x5A5A, torch.int32: 0x5A5A5A5A}[ity]
-    n = buf.numel() - 2 * MARGIN
-    head, tail, body = buf[:MARGIN], buf[MARGIN + n:], buf[MARGIN:MARGIN + n]
-    assert bool((head == bits).all()), f"{what}: write before the output"
-    assert bool((tail == bits).all()), f"{what}: write after the output"
-    assert not bool((body == bits).any()), f"{what}: output elements left unwritten"
 
 
 def _oracle_decode(q, k, v, lens, scale):

@@ -14,7 +14,7 @@ import numpy as np
 import pytest
 import torch
 
-from common import assert_close_attention, assert_close_lse, require_gpu
+from common import assert_close_attention, assert_close_lse, check_guards, guarded, require_gpu
 from oracle import codec
 from oracle import flashq as fq
 from quantized_kv_attention_gb300 import workloads as wl
@@ -67,9 +67,14 @@ def _replay(seed, B, Hq, Hkv, D, L0, steps, paged=False, dt=torch.float32, outli
                 assert np.array_equal(buf.k_codes[b, h, slot].cpu().numpy(), ck), (s, b, h)
                 assert np.array_equal(buf.v_codes[b, h, slot].cpu().numpy(), cv), (s, b, h)
         q = wl.queries(seed + 100 + s, B, Hq, D)
-        out, lse = qa.decode(q.cuda(), cache, torch.full((B,), cache_len, dtype=torch.int32).cuda(),
-                             cache_len + 64, scale, 0, return_lse=True)
+        ob, out = guarded((B, Hq, D), torch.float16)
+        lb, lse = guarded((B, Hq), torch.float32)
+        qa.decode(q.cuda(), cache, torch.full((B,), cache_len, dtype=torch.int32).cuda(), cache_len + 64, scale, 0,
+                  out=out, lse=lse)
         qa.flashq_attend(q.cuda(), buf, scale, out, lse)
+        torch.cuda.synchronize()
+        check_guards(ob, "out")
+        check_guards(lb, "lse")
         O = np.zeros((B, Hq, D))
         LSE = np.zeros((B, Hq))
         for b in range(B):

@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 import torch
 
-from common import assert_close_attention, assert_close_lse, require_gpu
+from common import assert_close_attention, assert_close_lse, check_guards, guarded, require_gpu
 from oracle import baselines as bl
 from oracle import codec
 from quantized_kv_attention_gb300 import workloads as wl
@@ -32,8 +32,12 @@ def test_dequantize_matches_oracle_bits(D, n):
     cache, _, _ = _filled_cache(qa, 61, B, Hkv, cap, D)
     # a saturated scale: 7 * 65504 overflows binary16 (+-inf), 1 * 65504 does not
     cache.k_scales[0, 0, 0] = 65504.0
-    k16, v16 = qa.dequantize_kv(cache, B, n)
+    kb, k16 = guarded((B, Hkv, n, D), torch.float16)
+    vb, v16 = guarded((B, Hkv, n, D), torch.float16)
+    qa.dequantize_kv(cache, B, n, k16, v16)
     torch.cuda.synchronize()
+    check_guards(kb, "k_out")
+    check_guards(vb, "v_out")
     for t, (codes, scales) in ((k16, (cache.k_codes, cache.k_scales)), (v16, (cache.v_codes, cache.v_scales))):
         want = bl.dequantize_fp16(codes[:, :, :n].cpu().numpy(), scales[:, :, :n].cpu().numpy())
         assert np.array_equal(t.cpu().numpy().view(np.uint16), want.view(np.uint16))
@@ -88,8 +92,13 @@ def test_decode_fp16_matches_oracle(case):
     cap = max(64, -(-max(lens) // 64) * 64)
     k, v = _fp16_cache(63, B, Hkv, cap, D, lens)
     q = wl.queries(63, B, Hq, D)
-    out, lse = qa.decode_fp16(q.cuda(), k.cuda(), v.cuda(), torch.tensor(lens, dtype=torch.int32), max(lens),
-                              scale, splits, return_lse=True)
+    ob, out = guarded((B, Hq, D), torch.float16)
+    lb, lse = guarded((B, Hq), torch.float32)
+    qa.decode_fp16(q.cuda(), k.cuda(), v.cuda(), torch.tensor(lens, dtype=torch.int32), max(lens), scale, splits,
+                   out=out, lse=lse)
+    torch.cuda.synchronize()
+    check_guards(ob, "out")
+    check_guards(lb, "lse")
     O, L = bl.attention_fp16(q.numpy()[:, :, None], np.nan_to_num(k.numpy()), np.nan_to_num(v.numpy()), scale,
                              False, lens)
     assert_close_attention(out, O[:, :, 0])
@@ -111,7 +120,12 @@ def test_prefill_fp16_matches_oracle(case):
     k, v = _fp16_cache(64, B, Hkv, cap, D, [nk] * B)
     q = wl.queries(64, B, Hq, nq, D)
     scale = 1 / math.sqrt(D)
-    out, lse = qa.prefill_fp16(q.cuda(), k.cuda(), v.cuda(), nk, scale, causal, return_lse=True)
+    ob, out = guarded((B, Hq, nq, D), torch.float16)
+    lb, lse = guarded((B, Hq, nq), torch.float32)
+    qa.prefill_fp16(q.cuda(), k.cuda(), v.cuda(), nk, scale, causal, out=out, lse=lse)
+    torch.cuda.synchronize()
+    check_guards(ob, "out")
+    check_guards(lb, "lse")
     O, L = bl.attention_fp16(q.numpy(), k.numpy()[:, :, :nk], v.numpy()[:, :, :nk], scale, causal)
     assert_close_attention(out, O)
     assert_close_lse(lse, L)

@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 import torch
 
-from common import assert_close_attention, assert_close_lse, require_gpu
+from common import assert_close_attention, assert_close_lse, check_guards, guarded, require_gpu
 from oracle import attention as att
 from oracle import codec2 as c2
 from quantized_kv_attention_gb300 import workloads as wl
@@ -59,8 +59,12 @@ def test_int2_decode(case):
     L = max(max(lens), 1)
     cache, k, v = _fill(qa, 73, B, Hkv, L)
     q = wl.queries(73, B, Hq, 128)
-    out, lse = qa.decode(q.cuda(), cache, torch.tensor(lens, dtype=torch.int32).cuda(), L, scale, splits,
-                         return_lse=True)
+    ob, out = guarded((B, Hq, 128), torch.float16)
+    lb, lse = guarded((B, Hq), torch.float32)
+    qa.decode(q.cuda(), cache, torch.tensor(lens, dtype=torch.int32).cuda(), L, scale, splits, out=out, lse=lse)
+    torch.cuda.synchronize()
+    check_guards(ob, "out")
+    check_guards(lb, "lse")
     wk, sk = c2.quantize_pack2(k.numpy())
     wv, sv = c2.quantize_pack2(v.numpy())
     O, LSE = att.attention(q.numpy()[:, :, None], c2.dequantize2(wk, sk, 128), c2.dequantize2(wv, sv, 128),

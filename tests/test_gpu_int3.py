@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 import torch
 
-from common import assert_close_attention, assert_close_lse, require_gpu
+from common import assert_close_attention, assert_close_lse, check_guards, guarded, require_gpu
 from oracle import attention as att
 from oracle import codec3 as c3
 from quantized_kv_attention_gb300 import workloads as wl
@@ -58,8 +58,12 @@ def test_int3_decode(case):
     L = max(max(lens), 1)
     cache, k, v = _fill(qa, 67, B, Hkv, L)
     q = wl.queries(67, B, Hq, 128)
-    out, lse = qa.decode(q.cuda(), cache, torch.tensor(lens, dtype=torch.int32).cuda(), L, scale, splits,
-                         return_lse=True)
+    ob, out = guarded((B, Hq, 128), torch.float16)
+    lb, lse = guarded((B, Hq), torch.float32)
+    qa.decode(q.cuda(), cache, torch.tensor(lens, dtype=torch.int32).cuda(), L, scale, splits, out=out, lse=lse)
+    torch.cuda.synchronize()
+    check_guards(ob, "out")
+    check_guards(lb, "lse")
     wk, sk = c3.quantize_pack3(k.numpy())
     wv, sv = c3.quantize_pack3(v.numpy())
     O, LSE = att.attention(q.numpy()[:, :, None], c3.dequantize3(wk, sk, 128), c3.dequantize3(wv, sv, 128),

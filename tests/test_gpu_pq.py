@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 import torch
 
-from common import assert_close_attention, assert_close_lse, require_gpu
+from common import assert_close_attention, assert_close_lse, check_guards, guarded, require_gpu
 from oracle import progressive as pq
 from quantized_kv_attention_gb300 import workloads as wl
 
@@ -86,8 +86,12 @@ def test_decode_pq_matches_oracle(case):
     cache = qa.PqCache.contiguous(B, Hkv, cap, D)
     qa.pq_quantize(k.cuda(), v.cuda(), cache)
     q = wl.queries(72, B, Hq, D)
-    out, lse = qa.decode_pq(q.cuda(), cache, torch.tensor(lens, dtype=torch.int32), max(lens), scale, splits,
-                            return_lse=True)
+    ob, out = guarded((B, Hq, D), torch.float16)
+    lb, lse = guarded((B, Hq), torch.float32)
+    qa.decode_pq(q.cuda(), cache, torch.tensor(lens, dtype=torch.int32), max(lens), scale, splits, out=out, lse=lse)
+    torch.cuda.synchronize()
+    check_guards(ob, "out")
+    check_guards(lb, "lse")
     O, L = pq.attention_pq(q.numpy()[:, :, None], pq.quantize_blocks(k.numpy()), pq.quantize_blocks(v.numpy()),
                            scale, False, lens)
     assert_close_attention(out, O[:, :, 0])

@@ -81,6 +81,16 @@ def test_paged_append_bit_exact():
         (pk, sk), (pv, sv) = ref[b]
         assert (gk[b, :, :n] == pk).all() and (gks[b, :, :n].view(np.uint16) == sk.view(np.uint16)).all()
         assert (gv[b, :, :n] == pv).all() and (gvs[b, :, :n].view(np.uint16) == sv.view(np.uint16)).all()
+    # nothing else written: pool rows past each sequence's length (its last
+    # page's tail) and pages no table row names keep their zeros
+    used = np.zeros(ks.shape, dtype=bool)  # [P, H, 64]
+    for b, n in enumerate(lens):
+        for t in range(int(n)):
+            used[table[b, t // 64], :, t % 64] = True
+    for name, a in (("k codes", kc), ("v codes", vc)):
+        assert (a[~used] == 0).all(), name
+    for name, a in (("k scales", ks), ("v scales", vs)):
+        assert (a[~used].view(np.uint16) == 0).all(), name
     assert qa.read_device_flags() == 0
 
 
