@@ -251,6 +251,32 @@ def test_paged_equals_contiguous_and_permutation_invariance():
     assert np.array_equal(O, O2) and np.array_equal(L, L2)
 
 
+def test_gather_pages_literal_example():
+    """A hand-written pool and table with the gathered result written out by
+    hand (not by the gather formula): pages of 2 tokens, two kv-heads, one code
+    byte per token.  Byte value 100 * page + 10 * head + slot; scale value
+    page + slot / 4 + head / 8."""
+    P, H, page = 3, 2, 2
+    pool = np.zeros((P, H, page, 1), dtype=np.uint8)
+    sc = np.zeros((P, H, page), dtype=np.float16)
+    for p in range(P):
+        for h in range(H):
+            for o in range(page):
+                pool[p, h, o, 0] = 100 * p + 10 * h + o
+                sc[p, h, o] = p + o / 4 + h / 8
+    table = np.array([[2, 0], [1, -1]])
+    lens = [3, 2]
+    got_p, got_s = att.gather_pages(pool, sc, table, lens, page)
+    # sequence 0: tokens 0, 1 in page 2; token 2 in page 0, slot 0
+    # sequence 1: tokens 0, 1 in page 1; its third row is past its length: zero
+    want_p = np.array([[[200, 201, 0], [210, 211, 10]],
+                       [[100, 101, 0], [110, 111, 0]]], dtype=np.uint8)[..., None]
+    want_s = np.array([[[2.0, 2.25, 0.0], [2.125, 2.375, 0.125]],
+                       [[1.0, 1.25, 0.0], [1.125, 1.375, 0.0]]], dtype=np.float16)
+    assert np.array_equal(got_p, want_p)
+    assert np.array_equal(got_s.view(np.uint16), want_s.view(np.uint16))
+
+
 # ---------------------------------------------------------------------------
 # planted mistakes: each one, put into the oracle on the CPU, must fail a pin
 # ---------------------------------------------------------------------------
@@ -281,3 +307,23 @@ def test_planted_attention_mistakes_are_caught(monkeypatch, mutation):
             failed = True
             break
     assert failed, f"mutation {mutation} was not caught"
+
+
+GATHER_MUTATIONS = [
+    ("page_table[b][t // page_size]", "page_table[b][t % page_size]"),  # page and slot swapped
+    ("off = t % page_size", "off = t // page_size"),
+    ("out_s[b, :, t] = pool_scales[page, :, off]", "out_s[b, :, t] = pool_scales[page, :, 0]"),
+    ("for t in range(seq_lens[b])", "for t in range(L)"),                # rows past the length filled
+]
+
+
+@pytest.mark.parametrize("mutation", GATHER_MUTATIONS)
+def test_planted_gather_mistakes_are_caught(monkeypatch, mutation):
+    src = inspect.getsource(att.gather_pages)
+    old, new = mutation
+    assert old in src
+    ns = dict(vars(att))
+    exec(compile(src.replace(old, new), "<mutant>", "exec"), ns)
+    monkeypatch.setattr(att, "gather_pages", ns["gather_pages"])
+    with pytest.raises((AssertionError, IndexError)):
+        test_gather_pages_literal_example()
