@@ -158,39 +158,93 @@ __device__ __forceinline__ __half quantize_vals_warp(const float (&x)[D / 32], u
   return hs;
 }
 
+// Packed fp32 pairs: two IEEE round-to-nearest operations per instruction,
+// no flush to zero, so the same bits as the scalar forms.
+__device__ __forceinline__ uint64_t pair_of(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void pair_split(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t pair_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t pair_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // Four rows at once, one per group of 8 lanes (g = lane / 8, l = lane % 8),
-// with the arithmetic of quantize_vals_warp (so the same bits): the row's
-// D values are C = D / 32 chunks of 32, and lane l holds values 4l .. 4l + 3
-// of each chunk, x[c] being the group's chunk (c + g) % C (the rotation keeps
-// the groups' shared-memory reads of a 16-lane phase on distinct banks).  The
+// with the codes of quantize_vals_warp (the same bits): the row's D values
+// are C = D / 32 chunks of 32, and lane l holds values 4l .. 4l + 3 of each
+// chunk, x[c] being the group's chunk (c + g) % C (the rotation keeps the
+// groups' shared-memory reads of a 16-lane phase on distinct banks).  The
 // absmax takes three shuffle levels inside the group, the scale one division
-// per lane for four rows; lane l stores the nibbles of its values of chunk cc
-// at byte 16 cc + 2l of the row, lane 0 of the group the scale.  A group whose
-// dst_codes is null stores nothing.  Every lane of the warp must call it.
+// per lane for four rows.  For a normal fp16 scale the one-FMA coding of
+// codes4 runs on pairs of values (y = x * rcp(s) + 1.5 * 2^23, m = y - 1.5 *
+// 2^23, e = x - m * s, all exact but y), and the lane's values are exact when
+// the largest |e| is below s / 2 (a NaN remainder fails the test); otherwise,
+// and for other scales, codes4_any codes the chunks.  Lane l stores the
+// nibbles of its values of chunk cc at byte 16 cc + 2l of the row, lane 0 of
+// the group the scale.  A group whose dst_codes is null stores nothing.
+// Every lane of the warp must call it.
 template <int D>
 __device__ __forceinline__ void quantize_vals_warp4(const float (&x)[D / 32][4], uint8_t *dst_codes,
                                                     uint16_t *dst_scale, int lane) {
   constexpr int C = D / 32;
+  constexpr float kShift = 12582912.0f;  // 1.5 * 2^23
+  constexpr uint32_t kBias = (8u - 0x4B400000u) * 0x1111u;  // see codes4
   const int g = lane >> 3, l = lane & 7;
   float am = 0.f;
 #pragma unroll
-  for (int c = 0; c < C; ++c)
-#pragma unroll
-    for (int t = 0; t < 4; ++t) am = fmaxf(am, fabsf(x[c][t]));
+  for (int c = 0; c < C; ++c) {
+    am = fmaxf(am, fmaxf(fabsf(x[c][0]), fabsf(x[c][1])));
+    am = fmaxf(am, fmaxf(fabsf(x[c][2]), fabsf(x[c][3])));
+  }
 #pragma unroll
   for (int o = 4; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
   __half hs = __float2half_rn(__fdiv_rn(am, 7.0f));
   if (__hisinf(hs)) hs = __ushort_as_half(0x7BFF);
   const float s = __half2float(hs);
-  if (dst_codes != nullptr) {
+  if (dst_codes == nullptr) return;
+  uint32_t packed[C];
+  bool exact = false;
+  if (s >= 6.103515625e-05f && s < 65504.f) {  // normal fp16 scale: |x| / s <= 7.004, no clamp
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
+    const uint64_t r2 = pair_of(r, r), shift2 = pair_of(kShift, kShift), unshift2 = pair_of(-kShift, -kShift);
+    const uint64_t ns2 = pair_of(-s, -s);
+    float emax = 0.f;
 #pragma unroll
     for (int c = 0; c < C; ++c) {
-      const uint32_t packed = codes4_any<4>(x[c], s);
-      const int cc = (c + g) & (C - 1);
-      *reinterpret_cast<uint16_t *>(dst_codes + cc * 16 + 2 * l) = static_cast<uint16_t>(packed);
+      const uint64_t x01 = pair_of(x[c][0], x[c][1]), x23 = pair_of(x[c][2], x[c][3]);
+      const uint64_t y01 = pair_fma(x01, r2, shift2), y23 = pair_fma(x23, r2, shift2);
+      const uint64_t e01 = pair_fma(pair_add(y01, unshift2), ns2, x01);
+      const uint64_t e23 = pair_fma(pair_add(y23, unshift2), ns2, x23);
+      float e0, e1, e2, e3, y0, y1, y2, y3;
+      pair_split(e01, e0, e1), pair_split(e23, e2, e3), pair_split(y01, y0, y1), pair_split(y23, y2, y3);
+      emax = fmax_nan(fmax_nan(emax, fabsf(e0)), fmax_nan(fabsf(e1), fmax_nan(fabsf(e2), fabsf(e3))));
+      const uint32_t acc = kBias + __float_as_uint(y0) + (__float_as_uint(y1) << 4) + (__float_as_uint(y2) << 8) +
+                           (__float_as_uint(y3) << 12);
+      packed[c] = (acc ^ 0x8888u) & 0xFFFFu;
     }
-    if (l == 0) *dst_scale = __half_as_ushort(hs);
+    exact = emax < 0.5f * s;
   }
+  if (!exact) {
+#pragma unroll
+    for (int c = 0; c < C; ++c) packed[c] = codes4_any<4>(x[c], s);
+  }
+#pragma unroll
+  for (int c = 0; c < C; ++c) {
+    const int cc = (c + g) & (C - 1);
+    *reinterpret_cast<uint16_t *>(dst_codes + cc * 16 + 2 * l) = static_cast<uint16_t>(packed[c]);
+  }
+  if (l == 0) *dst_scale = __half_as_ushort(hs);
 }
 
 // quantize_vals_warp of row `src` (D values of type T, lane i reading its

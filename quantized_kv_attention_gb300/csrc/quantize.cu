@@ -13,7 +13,8 @@
 // contiguous in k and v unless the cache lists its heads), and 8 consumer
 // warps quantize 8 rows each from shared memory and store codes and scales
 // to the cache.  INT4 rows take one group of 8 lanes each, so one warp
-// instruction works on four rows (quantize_vals_warp4, two rounds); INT3 /
+// instruction works on four rows (quantize_vals_warp4, two rounds, its coding
+// arithmetic on packed fp32 pairs); INT3 /
 // INT2 rows are quantized one at a time by the whole warp.
 #include "internal.h"
 #include "ptx.cuh"
