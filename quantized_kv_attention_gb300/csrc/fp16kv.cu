@@ -27,7 +27,8 @@ namespace {
 // ---------------------------------------------------------------- dequantize
 // x16 = fl16(c * s): decode_nibbles gives the exact fp16 codes, the permutes
 // restore element order, and HMUL2 of two fp16 values is the correctly
-// rounded product.  One thread per 32 codes (16 bytes) of a row.
+// rounded product.  One thread per 8 codes (one 32-bit word) of a row: a
+// warp reads 128 contiguous bytes of codes and writes 512 contiguous bytes.
 __device__ __forceinline__ uint4 dequant_word_pairs(uint32_t w, __half2 s2) {
   uint32_t x[4];
   decode_nibbles(w, x);  // (e0, e4), (e1, e5), (e2, e6), (e3, e7)
@@ -46,42 +47,50 @@ template <int D>
 __global__ void __launch_bounds__(256)
     dequantize_kernel(KvView cache, int batch, int n, uint16_t *__restrict__ k_out, uint16_t *__restrict__ v_out,
                       uint32_t *err) {
-  constexpr int P = D / 32;  // 16-byte code chunks per row
+  constexpr int WPR = D / 8;  // 32-bit code words per row; a thread turns one into 16 bytes of fp16
   const int64_t rows = static_cast<int64_t>(batch) * cache.hkv * n;
-  const int64_t total = rows * P;
+  const int64_t total = rows * WPR;
+  const bool small = rows <= 0x7fffffffLL;  // row / n in 32 bits
   const bool is_v = blockIdx.y != 0;
-  const uint8_t *codes = is_v ? cache.v_codes : cache.k_codes;
+  const uint32_t *codes = reinterpret_cast<const uint32_t *>(is_v ? cache.v_codes : cache.k_codes);
   const uint16_t *scales = is_v ? cache.v_scales : cache.k_scales;
-  uint16_t *out = is_v ? v_out : k_out;
-  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < total;
-       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t row = t / P;
-    const int part = static_cast<int>(t % P);
-    const int i = static_cast<int>(row % n);
-    const int64_t bh = row / n;
-    int64_t src = -1;
-    if (cache.page_table == nullptr) {
-      src = bh * cache.capacity + i;
+  uint4 *out = reinterpret_cast<uint4 *>(is_v ? v_out : k_out);
+  // four words a thread per pass (the grid's stride apart), their loads issued together
+  constexpr int U = 4;
+  auto src_row = [&](int64_t row) -> int64_t {
+    int64_t bh;
+    int i;
+    if (small) {
+      const uint32_t r32 = static_cast<uint32_t>(row), q = r32 / static_cast<uint32_t>(n);
+      bh = q, i = static_cast<int>(r32 - q * static_cast<uint32_t>(n));
     } else {
-      const int h = static_cast<int>(bh % cache.hkv), b = static_cast<int>(bh / cache.hkv);
-      const int page = __ldg(cache.page_table + static_cast<int64_t>(b) * cache.max_pages + i / kPage);
-      if (page >= 0 && page < cache.num_pages)
-        src = (static_cast<int64_t>(page) * cache.hkv + h) * kPage + i % kPage;
-      else if (part == 0)
-        atomicOr(err, kFlagBadPage);
+      bh = row / n, i = static_cast<int>(row - bh * n);
     }
-    uint4 o[4] = {};
-    if (src >= 0) {
-      const uint4 c = __ldg(reinterpret_cast<const uint4 *>(codes + src * (D / 2)) + part);
-      const __half2 s2 = __half2half2(__ushort_as_half(__ldg(scales + src)));
-      o[0] = dequant_word_pairs(c.x, s2);
-      o[1] = dequant_word_pairs(c.y, s2);
-      o[2] = dequant_word_pairs(c.z, s2);
-      o[3] = dequant_word_pairs(c.w, s2);
-    }
-    uint4 *dst = reinterpret_cast<uint4 *>(out + row * D + part * 32);
+    if (cache.page_table == nullptr) return bh * cache.capacity + i;
+    const int h = static_cast<int>(bh % cache.hkv), b = static_cast<int>(bh / cache.hkv);
+    const int page = __ldg(cache.page_table + static_cast<int64_t>(b) * cache.max_pages + i / kPage);
+    if (page >= 0 && page < cache.num_pages) return (static_cast<int64_t>(page) * cache.hkv + h) * kPage + i % kPage;
+    return -1;
+  };
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t t0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t0 < total; t0 += U * stride) {
+    uint32_t c[U];
+    uint16_t sc[U];
+    int64_t src[U];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) dst[q] = o[q];
+    for (int u = 0; u < U; ++u) {
+      const int64_t t = t0 + u * stride;
+      src[u] = t < total ? src_row(t / WPR) : -2;
+      if (src[u] == -1 && t % WPR == 0) atomicOr(err, kFlagBadPage);
+      c[u] = src[u] >= 0 ? __ldg(codes + src[u] * WPR + static_cast<int>(t % WPR)) : 0u;
+      sc[u] = src[u] >= 0 ? __ldg(scales + src[u]) : static_cast<uint16_t>(0);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t t = t0 + u * stride;
+      if (src[u] == -2) break;
+      out[t] = src[u] >= 0 ? dequant_word_pairs(c[u], __half2half2(__ushort_as_half(sc[u]))) : make_uint4(0, 0, 0, 0);
+    }
   }
 }
 
@@ -356,8 +365,8 @@ cudaError_t launch_dequantize(const KvView &cache, int batch, int n, uint16_t *k
                               int sms, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(batch) * cache.hkv * n;
   if (rows == 0) return cudaSuccess;
-  const int64_t threads = rows * (cache.head_dim / 32);
-  const int64_t blocks = min((threads + 255) / 256, static_cast<int64_t>(8) * (sms > 0 ? sms : 1));
+  const int64_t threads = rows * (cache.head_dim / 8);
+  const int64_t blocks = min((threads + 255) / 256, static_cast<int64_t>(16) * (sms > 0 ? sms : 1));
   dim3 grid(static_cast<unsigned>(blocks), 2);
   if (cache.head_dim == 128)
     dequantize_kernel<128><<<grid, 256, 0, stream>>>(cache, batch, n, k_out, v_out, err);
