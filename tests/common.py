@@ -87,3 +87,25 @@ def check_guards(buf, what, body_written=True):
     assert bool((buf[GUARD_MARGIN + n:] == bits).all()), f"{what}: a write after the output"
     if body_written:
         assert not bool((buf[GUARD_MARGIN:GUARD_MARGIN + n] == bits).any()), f"{what}: elements left unwritten"
+
+
+def mutant_fails_a_pin(monkeypatch, module, func_name, old, new, pins):
+    """Plant a mistake in one oracle function (its source with `old` replaced by
+    `new`, on the CPU) and report whether one of the pin tests `pins` fails."""
+    import inspect
+    import textwrap
+    owner, attr = module, func_name
+    if "." in func_name:  # a method: "Class.method"
+        cls, attr = func_name.split(".")
+        owner = getattr(module, cls)
+    src = textwrap.dedent(inspect.getsource(getattr(owner, attr)))
+    assert old in src, (func_name, old)
+    ns = dict(vars(module))
+    exec(compile(src.replace(old, new, 1), "<mutant>", "exec"), ns)
+    monkeypatch.setattr(owner, attr, ns[attr])
+    for pin in pins:
+        try:
+            pin()
+        except (AssertionError, ValueError, IndexError, ZeroDivisionError, TypeError, OverflowError):
+            return True
+    return False

@@ -15,6 +15,7 @@ import math
 import numpy as np
 import pytest
 
+from common import mutant_fails_a_pin
 from oracle import attention as att
 from oracle import codec
 
@@ -201,6 +202,13 @@ def test_combine_closed_forms():
     assert np.allclose(O, o[0]) and np.allclose(L, l[0])
     O, L = att.combine(np.stack([o[0]]), np.full((1, 3), -np.inf))
     assert (O == 0).all() and np.isneginf(L).all()
+    # partial sums of exponentials 1 and 3 (lse 0 and ln 3): weights 1/4 and 3/4, lse ln 4
+    a, b = np.array([[1.0, -2.0]]), np.array([[5.0, 2.0]])
+    O, L = att.combine(np.stack([a, b]), np.array([[0.0], [math.log(3.0)]]))
+    assert np.allclose(O, [[4.0, 1.0]], rtol=0, atol=1e-15) and np.allclose(L, [math.log(4.0)], rtol=0, atol=1e-15)
+    # a shift of every lse moves the result's lse by the same amount and leaves O
+    O2, L2 = att.combine(np.stack([a, b]), np.array([[700.0], [700.0 + math.log(3.0)]]))
+    assert np.allclose(O2, O, rtol=0, atol=1e-13) and np.allclose(L2, L + 700.0, rtol=0, atol=1e-12)
 
 
 def test_empty_sequence():
@@ -327,3 +335,23 @@ def test_planted_gather_mistakes_are_caught(monkeypatch, mutation):
     monkeypatch.setattr(att, "gather_pages", ns["gather_pages"])
     with pytest.raises((AssertionError, IndexError)):
         test_gather_pages_literal_example()
+
+
+def _all_split_cases():
+    for bounds in ([0, 5, 9, 16], [0, 16], [0, 0, 3, 16, 20], [0, 1, 2, 3, 16]):
+        test_split_combine_equals_unsplit(bounds)
+
+
+COMBINE_MUTATIONS = [
+    ("combine", "lse = np.where(live, m_safe + np.log(Zs)", "lse = np.where(live, np.log(Zs)"),  # max dropped from lse
+    ("combine", "np.exp(pl - m_safe[None])", "np.exp(pl)"),                                        # unshifted exponentials
+    ("combine", "(w[..., None] * po).sum(axis=0) / Zs[..., None]", "(w[..., None] * po).sum(axis=0)"),  # no normalisation
+    ("combine", "(w[..., None] * po).sum(axis=0)", "po.sum(axis=0)"),                              # unweighted
+    ("split_partials", "sub_lens = [max(0, min(hi, n) - lo) for n in lens]", "sub_lens = [w0 for w0 in [max(hi - lo, 0)] * len(lens)]"),
+]
+
+
+@pytest.mark.parametrize("mutation", COMBINE_MUTATIONS, ids=[m[0] + ":" + m[2][:40] for m in COMBINE_MUTATIONS])
+def test_planted_combine_mistakes_are_caught(monkeypatch, mutation):
+    func, old, new = mutation
+    assert mutant_fails_a_pin(monkeypatch, att, func, old, new, [test_combine_closed_forms, _all_split_cases]), mutation

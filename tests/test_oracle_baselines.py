@@ -8,6 +8,7 @@ import struct
 import numpy as np
 import pytest
 
+from common import mutant_fails_a_pin
 from oracle import attention as att
 from oracle import baselines as bl
 from oracle import codec
@@ -118,3 +119,27 @@ def test_attention_fp16_is_the_plain_definition_on_fp16_values():
     O2, L2 = bl.attention_fp16(q, k, v, 0.5)
     assert np.allclose(O2[0, 0, 0], v[0, 0, 0].astype(np.float64), rtol=0, atol=1e-15)
     assert L2[0, 0, 0] == pytest.approx(0.5 * (0.25 + 1.0 - 2.0) + np.log(2.0))
+
+
+def _all_hand_vectors():
+    for args in _vectors():
+        test_dequantize_fp16_hand_vectors(*args)
+
+
+MUTATIONS = [
+    ("dequantize_fp16", "exact.astype(np.float16)", "(exact * (1 + 2.0**-30)).astype(np.float16)"),  # ties away from zero
+    ("dequantize_fp16", "codec.dequantize(packed, scales)", "codec.dequantize(packed, scales) * 1.0009765625"),  # off by an ulp
+    ("attention_fp16", "np.asarray(v16, dtype=np.float16)", "np.asarray(k16, dtype=np.float16)"),   # K used as V
+    ("attention_fp16", "softmax_scale, causal", "1.0, causal"),                                       # scale dropped
+    ("attention_post_dequant", "dequantize_fp16(v_packed, v_scales)", "dequantize_fp16(v_packed, k_scales)"),  # K scales on V
+    ("attention_post_dequant", "softmax_scale, causal, k_lens)", "softmax_scale, False, k_lens)"),     # mask dropped
+]
+PINS = [_all_hand_vectors, test_dequantize_fp16_half_ulp_bound_and_exact_codes,
+        test_post_dequant_equals_fused_when_products_are_fp16_exact, test_post_dequant_uses_the_rounded_copy,
+        test_attention_fp16_is_the_plain_definition_on_fp16_values]
+
+
+@pytest.mark.parametrize("mutation", MUTATIONS, ids=[m[0] + ":" + m[2][:40] for m in MUTATIONS])
+def test_planted_mistakes_are_caught(monkeypatch, mutation):
+    func, old, new = mutation
+    assert mutant_fails_a_pin(monkeypatch, bl, func, old, new, PINS), mutation

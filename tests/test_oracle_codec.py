@@ -11,9 +11,12 @@ import math
 import os
 from fractions import Fraction as F
 
+import functools
+
 import numpy as np
 import pytest
 
+from common import mutant_fails_a_pin
 from oracle import codec
 
 
@@ -238,3 +241,24 @@ def test_planted_codec_mistakes_are_caught(monkeypatch, golden_dir, mutation):
             test_golden_vectors(golden_dir)
     finally:
         monkeypatch.undo()
+
+
+SOURCE_MUTATIONS = [
+    ("row_scales", "np.max(np.abs(x32), axis=-1)", "np.max(x32, axis=-1)"),                # range without the sign
+    ("row_scales", "np.where(np.isinf(s16), np.float16(FP16_MAX), s16)", "np.where(np.isinf(s16), np.float16(0), s16)"),  # overflow to 0
+    ("quantize_rows", "np.clip(np.rint(q), -QMAX, QMAX)", "np.clip(np.rint(q), -QMAX - 1, QMAX)"),  # asymmetric clamp
+    ("quantize_rows", "q = np.where(s64 > 0.0, x64 / safe, 0.0)", "q = np.where(s64 > 0.0, x64 / safe * 0.999999, 0.0)"),
+    ("pack_nibbles", "(lo | (hi << np.uint8(4)))", "(hi | (lo << np.uint8(4)))"),          # nibble order
+    ("unpack_nibbles", "lo = np.where(lo >= 8, lo - 16, lo)", "lo = np.where(lo > 8, lo - 16, lo)"),  # -8 read as +8
+    ("unpack_nibbles", "hi = np.where(hi >= 8, hi - 16, hi)", "hi = np.where(hi >= 8, hi - 15, hi)"),  # sign extension
+    ("dequantize", "return c * np.asarray", "return c * 0.5 * np.asarray"),                 # scale off by two
+]
+
+
+@pytest.mark.parametrize("mutation", SOURCE_MUTATIONS, ids=[m[0] + ":" + m[2][:40] for m in SOURCE_MUTATIONS])
+def test_planted_source_mistakes_are_caught(monkeypatch, golden_dir, mutation):
+    func, old, new = mutation
+    pins = [functools.partial(test_golden_vectors, golden_dir), functools.partial(test_golden_vectors_match_exact_model, golden_dir),
+            test_exact_rational_reference, test_all_fp16_values_against_fixed_absmax, test_invariants,
+            test_zero_and_tiny_rows, test_pack_layout_and_roundtrip, test_dequantize_exact]
+    assert mutant_fails_a_pin(monkeypatch, codec, func, old, new, pins), mutation

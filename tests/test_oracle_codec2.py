@@ -5,7 +5,9 @@ invariants (TurboAttention, arXiv 2412.08585, §3.2: 2-bit heads)."""
 from fractions import Fraction
 
 import numpy as np
+import pytest
 
+from common import mutant_fails_a_pin
 from oracle import codec2 as c2
 
 
@@ -63,3 +65,27 @@ def test_rounding_equals_exact_rationals_and_invariants():
         err = np.abs(x[r].astype(np.float64) - c[r] * float(s[r]))
         assert err.max() <= float(s[r]) / 2 + 1e-12 * float(s[r])
     assert np.abs(c).max() <= 1
+
+
+def test_dequantize_hand_vector():
+    words = c2.pack16(np.array([[1, 0, -1, 1, 0, -1]], np.int8))
+    got = c2.dequantize2(words, np.array([0.5], np.float16), 6)
+    assert got.tolist() == [[0.5, 0.0, -0.5, 0.5, 0.0, -0.5]]
+
+
+MUTATIONS = [
+    ("row_scales2", "am / np.float32(QMAX2)", "am / np.float32(2)"),              # wrong divisor
+    ("quantize_rows2", "np.rint(q)", "np.floor(q + 0.5)"),                      # ties away from even
+    ("pack16", "c & 3", "c & 1"),                                                # field mask
+    ("pack16", "shifts = 2 * np.arange", "shifts = 3 * np.arange"),              # field width
+    ("unpack16", "f - 4", "f - 2"),                                              # sign extension
+    ("dequantize2", "unpack16(words, d).astype(np.float64) *", "unpack16(words, d).astype(np.float64) + 0 *"),  # scale dropped
+]
+PINS = [test_hand_vectors, test_packing_bit_positions, test_unpack_inverts_pack_for_every_field_value,
+        test_rounding_equals_exact_rationals_and_invariants, test_dequantize_hand_vector]
+
+
+@pytest.mark.parametrize("mutation", MUTATIONS, ids=[m[0] + ":" + m[2] for m in MUTATIONS])
+def test_planted_mistakes_are_caught(monkeypatch, mutation):
+    func, old, new = mutation
+    assert mutant_fails_a_pin(monkeypatch, c2, func, old, new, PINS), mutation

@@ -5,7 +5,9 @@ exact rational rounding, bit positions of the ten-per-word packing
 from fractions import Fraction
 
 import numpy as np
+import pytest
 
+from common import mutant_fails_a_pin
 from oracle import codec3 as c3
 
 
@@ -62,3 +64,27 @@ def test_rounding_equals_exact_rationals_and_invariants():
         err = np.abs(x[r].astype(np.float64) - c[r] * float(s[r]))
         assert err.max() <= float(s[r]) / 2 + 1e-12 * float(s[r])
     assert np.abs(c).max() <= 3
+
+
+def test_dequantize_hand_vector():
+    words = c3.pack10(np.array([[3, 0, -1, -3, 2, 1, 0, -2, 1, 3, -1]], np.int8))
+    got = c3.dequantize3(words, np.array([0.25], np.float16), 11)
+    assert got.tolist() == [[0.75, 0.0, -0.25, -0.75, 0.5, 0.25, 0.0, -0.5, 0.25, 0.75, -0.25]]
+
+
+MUTATIONS = [
+    ("row_scales3", "am / np.float32(QMAX3)", "am / np.float32(4)"),              # wrong divisor
+    ("quantize_rows3", "np.rint(q)", "np.floor(q + 0.5)"),                      # ties away from even
+    ("pack10", "c & 7", "c & 3"),                                                # field mask
+    ("pack10", "shifts = 3 * np.arange", "shifts = 4 * np.arange"),              # field width
+    ("unpack10", "f - 8", "f - 4"),                                              # sign extension
+    ("dequantize3", "unpack10(words, d).astype(np.float64) *", "unpack10(words, d).astype(np.float64) + 0 *"),  # scale dropped
+]
+PINS = [test_hand_vectors, test_packing_bit_positions, test_unpack_inverts_pack_for_every_field_value,
+        test_rounding_equals_exact_rationals_and_invariants, test_dequantize_hand_vector]
+
+
+@pytest.mark.parametrize("mutation", MUTATIONS, ids=[m[0] + ":" + m[2] for m in MUTATIONS])
+def test_planted_mistakes_are_caught(monkeypatch, mutation):
+    func, old, new = mutation
+    assert mutant_fails_a_pin(monkeypatch, c3, func, old, new, PINS), mutation

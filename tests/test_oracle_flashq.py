@@ -10,6 +10,7 @@ from fractions import Fraction
 import numpy as np
 import pytest
 
+from common import mutant_fails_a_pin
 from oracle import codec
 from oracle import flashq as fq
 
@@ -103,3 +104,29 @@ def test_attention_over_one_buffered_key_is_its_value():
     o, lse = fq.attention_buffered(q, k, v, 0.5)
     assert np.array_equal(o, np.tile([-127.0, 2.0, 0.0, 100.0], (2, 1)))
     assert np.allclose(lse, 0.5 * (q @ np.array([127.0, 0.0, -127.0, 64.0])), rtol=0, atol=1e-12)
+
+
+def test_dequantize_int8_hand_values():
+    got = fq.dequantize_int8(np.array([[3, -2, 127, 0]], np.int8), np.array([0.5], np.float16))
+    assert got.tolist() == [[1.5, -1.0, 63.5, 0.0]]
+
+
+MUTATIONS = [
+    ("universal_scale", "r32 / np.float32(QMAX8)", "r32 / np.float32(128)"),          # wrong divisor
+    ("quantize_int8", "np.rint(", "np.floor(0.5 + "),                                # ties away from even
+    ("quantize_int8", "np.clip(q, -QMAX8, QMAX8)", "np.clip(q, -QMAX8 - 1, QMAX8)"),  # asymmetric clamp
+    ("history_range", "np.float32(codec.QMAX) * s.max", "np.float32(8) * s.max"),    # R = 7 x max s
+    ("BufferedHead.append", "if self.r == 0:", "if False:"),                         # empty history keeps R = 0
+    ("BufferedHead.flush", "max(float(self.r), float(history_range(s)))", "float(history_range(s))"),  # R not kept
+    ("dequantize_int8", "np.asarray(c, dtype=np.float64) *", "np.asarray(c, dtype=np.float64) + 0 *"),  # u dropped
+]
+PINS = [test_universal_scale_closed_forms, test_int8_codes_equal_exact_rounding_and_clamp,
+        test_history_range_is_seven_times_the_largest_scale, test_first_row_sets_the_range_of_an_empty_history,
+        test_outlier_past_the_range_is_clamped, test_flush_reproduces_representable_rows,
+        test_attention_over_one_buffered_key_is_its_value, test_dequantize_int8_hand_values]
+
+
+@pytest.mark.parametrize("mutation", MUTATIONS, ids=[m[0] + ":" + m[2] for m in MUTATIONS])
+def test_planted_mistakes_are_caught(monkeypatch, mutation):
+    func, old, new = mutation
+    assert mutant_fails_a_pin(monkeypatch, fq, func, old, new, PINS), mutation

@@ -8,7 +8,9 @@ import math
 import statistics
 
 import numpy as np
+import pytest
 
+from common import mutant_fails_a_pin
 from oracle import attention as att
 from oracle import codec, codec2
 from oracle import headwise as hw
@@ -53,6 +55,9 @@ def test_plan_bits_and_key_value_maximum():
     assert hw.plan_bits([1.0, 1.0, 1.0], 1).tolist() == [2, 4, 4]   # ties: lower head first
     assert hw.plan_bits([5.0, 1.0], 0).tolist() == [4, 4]
     assert hw.plan_bits([5.0, 1.0], 2).tolist() == [2, 2]
+    # 64 heads in two priority classes: the 20 low ones are the first 20 of the lower class
+    want = [2 if h % 2 == 0 and h < 40 else 4 for h in range(64)]
+    assert hw.plan_bits([1.0, 2.0] * 32, 20).tolist() == want
     rng = np.random.default_rng(6)
     k = rng.standard_normal((2, 3, 10, 8)).astype(np.float32)
     v = rng.standard_normal((2, 3, 10, 8)).astype(np.float32)
@@ -93,3 +98,23 @@ def test_mixed_attention_composes_head_by_head():
     # 2-bit heads lose accuracy against the unquantized values, 4-bit ones less
     of, _ = att.attention(q, k, v, 0.25)
     assert np.abs(o2 - of).mean() > np.abs(o4 - of).mean()
+
+
+MUTATIONS = [
+    ("head_priority", "math.sqrt(sq / d)", "math.sqrt(sq / (d - 1))"),                 # sample, not population std
+    ("head_priority", "float(mx.max()) - float(mn.min())", "float(mx.max()) - float(mx.min())"),  # wrong gap
+    ("head_priority", "return gap * math.sqrt", "return gap + math.sqrt"),              # sum, not product
+    ("priorities", "max(head_priority(kr), head_priority(vr))", "head_priority(kr)"),  # values ignored
+    ("priorities", "k[b, h, :ln[b]]", "k[b, h]"),                                        # lengths ignored
+    ("plan_bits", "bits[order[:n_low]] = 2", "bits[order[len(bits) - n_low:]] = 2"),    # highest go low
+    ("plan_bits", 'kind="stable"', 'kind="quicksort"'),                                  # ties unordered
+    ("dequantize_mixed", "if b == 2:", "if b != 2:"),                                    # widths swapped
+]
+PINS = [test_priority_by_hand, test_priority_against_independent_statistics, test_priority_invariants,
+        test_plan_bits_and_key_value_maximum, test_mixed_attention_composes_head_by_head]
+
+
+@pytest.mark.parametrize("mutation", MUTATIONS, ids=[m[0] + ":" + m[2] for m in MUTATIONS])
+def test_planted_mistakes_are_caught(monkeypatch, mutation):
+    func, old, new = mutation
+    assert mutant_fails_a_pin(monkeypatch, hw, func, old, new, PINS), mutation

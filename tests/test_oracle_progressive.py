@@ -8,6 +8,7 @@ from fractions import Fraction
 import numpy as np
 import pytest
 
+from common import mutant_fails_a_pin
 from oracle import flashq
 from oracle import progressive as pq
 
@@ -115,3 +116,31 @@ def test_constant_channels_store_only_the_zero_point():
     assert not pq.unpack_unsigned(packed).any() and (s2 == 1).all()
     q1, s = pq.stage1(x)
     assert np.array_equal(z2[0], q1[0]) and s1[0] == s
+
+
+def _all_hand_vectors():
+    for args in _vectors():
+        test_stage2_hand_vectors(*args)
+
+
+MUTATIONS = [
+    ("stage1", "np.max(np.abs(x32))", "np.max(x32)"),                            # range without the sign
+    ("stage2", "-((lo - hi) // QMAX4)", "(hi - lo) // QMAX4"),                    # floor, not ceiling
+    ("stage2", "np.maximum(1, ", "np.maximum(2, "),                               # scale floor off by one
+    ("stage2", "(fl % 2 == 1)", "(fl % 2 == 0)"),                                 # ties to odd
+    ("stage2", "num = q - lo", "num = q - lo - 1"),                               # zero point off by one
+    ("pack_unsigned", "(q[..., 0::2] | (q[..., 1::2] << 4))", "(q[..., 1::2] | (q[..., 0::2] << 4))"),  # nibble order
+    ("read_int8", "+ np.asarray(z2", "- np.asarray(z2"),                          # zero point sign
+    ("dequantize_blocks", "x = q1.astype(np.float64) *", "x = qb.astype(np.float64) *"),  # nibbles read as int8
+    ("compress_int8_block", "np.float16(s1)", "np.float16(1.0)"),                  # buffer scale dropped
+]
+PINS = [_all_hand_vectors, test_stage2_rounding_is_round_half_even_on_exact_rationals,
+        test_stage2_invariants_on_random_blocks, test_pack_order_and_round_trip,
+        test_stage1_is_the_buffer_code_over_the_block_range, test_blocks_round_trip_within_the_two_stage_bound,
+        test_compressing_a_full_buffer_uses_its_codes_and_scale, test_constant_channels_store_only_the_zero_point]
+
+
+@pytest.mark.parametrize("mutation", MUTATIONS, ids=[m[0] + ":" + m[2] for m in MUTATIONS])
+def test_planted_mistakes_are_caught(monkeypatch, mutation):
+    func, old, new = mutation
+    assert mutant_fails_a_pin(monkeypatch, pq, func, old, new, PINS), mutation
