@@ -1146,29 +1146,33 @@ __global__ void __launch_bounds__(Layout<W>::kThreads, 1)
 // balanced ranges cut: a segment spanning CTAs c0 < c1 has partials in slot
 // 2*c0 + 1 (its start, in c0's last segment) and slots 2*c for c0 < c <= c1
 // whose range is not empty.  Segments of empty sequences get O = 0 and
-// lse = -inf.  Grid (segments, rows of a segment); the 8 warps of a CTA split
-// one row's partials, each folding its share with a running max so that the
-// lse and O of a partial are fetched together, then combine in shared memory.
-// Small on purpose (256 threads, <= 64 registers, 4 KB shared memory): one
-// merge CTA fits on an SM beside a decode CTA, so the programmatic launch
-// makes it resident while the decode still runs and it starts the moment the
-// decode grid completes.
-constexpr int kMergeWarps = 8;
-
-template <int D, int W>
-__global__ void __launch_bounds__(kMergeWarps * 32, 4)
+// lse = -inf.  Two shapes, kWarps = 8 or 32:
+//   8   grid (segments, rows of a segment): the 8 warps of a CTA split one
+//       row's partials.  Small on purpose (256 threads, <= 64 registers, 4 KB
+//       shared memory): beside an 8-warp decode CTA the programmatic launch
+//       makes it resident while the decode still runs.  For few segments of
+//       many partials (a long sequence cut into ~20 ranges per segment), the
+//       rows spread over many SMs.
+//   32  grid (segments): one 1024-thread CTA merges all rows of a segment,
+//       32 / rows warps on each.  For many segments of 1-3 partials (a
+//       batch of variable-length sequences), where launching and waiting for
+//       one CTA per row costs more than the fold.
+// A warp folds its partials with a running max so that the lse and O of a
+// partial are fetched together, in batches of 4 whose loads are all issued
+// before any is used; the warps of a row combine in shared memory.
+template <int D, int W, int kWarps>
+__global__ void __launch_bounds__(kWarps * 32, kWarps == 8 ? 4 : 1)
     decode_merge_kernel(const int32_t *__restrict__ seq_lens, int batch, int hkv, int G, int ctas,
                         int64_t limit, int paged, const int32_t *__restrict__ head_map, int model_hkv,
                         const float *__restrict__ po,
                         const float *__restrict__ pl, uint16_t *__restrict__ out,
                         float *__restrict__ lse) {
-  constexpr int VPL = D / 32;
-  __shared__ float accs[kMergeWarps][D];
-  __shared__ float wm[kMergeWarps], wz[kMergeWarps];
-  __shared__ int redi[4][kMergeWarps];
+  constexpr int VPL = D / 32, KB = 4;
+  __shared__ float accs[kWarps][D];
+  __shared__ float wm[kWarps], wz[kWarps];
+  __shared__ int redi[4][kWarps];
   const StageGeo geo = stage_geo<W>(hkv, paged != 0);
   const int b = blockIdx.x / geo.groups, hg = blockIdx.x % geo.groups;
-  const int r = blockIdx.y;  // row within the segment: kv-head r / G, q-head r % G
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // A programmatic dependent (the next decode on the stream) may be scheduled
   // now: before its own wait, which ends only once this grid has completed,
@@ -1183,7 +1187,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4)
   };
   // stages and non-empty sequences: in all, and before sequence b
   int tot = 0, pre = 0, nzt = 0, nzb = 0;
-  for (int bb = threadIdx.x; bb < batch; bb += kMergeWarps * 32) {
+  for (int bb = threadIdx.x; bb < batch; bb += kWarps * 32) {
     const int n = stages(bb);
     tot += n, nzt += n > 0;
     if (bb < b) pre += n, nzb += n > 0;
@@ -1198,16 +1202,25 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4)
   if (lane == 0) redi[0][warp] = tot, redi[1][warp] = pre, redi[2][warp] = nzt, redi[3][warp] = nzb;
   __syncthreads();
   tot = pre = nzt = nzb = 0;
-  for (int w = 0; w < kMergeWarps; ++w) tot += redi[0][w], pre += redi[1][w], nzt += redi[2][w], nzb += redi[3][w];
+  for (int w = 0; w < kWarps; ++w) tot += redi[0][w], pre += redi[1][w], nzt += redi[2][w], nzb += redi[3][w];
   const int rows = geo.hb * G;
-  const int mh = model_head(head_map, model_hkv, hg * geo.hb + r / G);
-  if (mh < 0) return;  // flagged by the decode kernel
-  const int64_t row = (static_cast<int64_t>(b) * model_hkv + mh) * G + r % G;
+  // this CTA's rows: one (kWarps = 8, grid.y = rows) or all of the segment's
+  const int nr = kWarps == 8 ? 1 : rows, r0 = kWarps == 8 ? static_cast<int>(blockIdx.y) : 0;
+  const int wpr = kWarps == 8 ? 8 : kWarps / rows;  // warps per row (rows <= 32)
+  const int rl = warp / wpr, sub = warp - rl * wpr;
+  auto out_row = [&](int r) {  // output row of segment row r; -1: no model head (flagged by the decode)
+    const int mh = model_head(head_map, model_hkv, hg * geo.hb + r / G);
+    return mh < 0 ? int64_t(-1) : (static_cast<int64_t>(b) * model_hkv + mh) * G + r % G;
+  };
   const int n = stages(b);
-  if (n == 0) {  // no decode CTA touches this row
+  if (n == 0) {  // no decode CTA touches these rows
     pdl_wait();
-    for (int d = threadIdx.x; d < D; d += kMergeWarps * 32) out[row * D + d] = 0;
-    if (threadIdx.x == 0 && lse) lse[row] = -INFINITY;
+    for (int i = threadIdx.x; i < nr * D; i += kWarps * 32) {
+      const int64_t row = out_row(r0 + i / D);
+      if (row < 0) continue;
+      out[row * D + i % D] = 0;
+      if (i % D == 0 && lse) lse[row] = -INFINITY;
+    }
     return;
   }
   // the decode kernel's cost-balanced ranges: cost offsets of the segment's
@@ -1224,59 +1237,63 @@ __global__ void __launch_bounds__(kMergeWarps * 32, 4)
   float m = -INFINITY, z = 0.f, acc[VPL];
 #pragma unroll
   for (int j = 0; j < VPL; ++j) acc[j] = 0.f;
-  // A warp folds partials k = warp, warp + 8, ... in batches of 4 whose loads
-  // are all issued before any is used.  Empty ranges (two 64-bit divisions
-  // to detect) exist only when a CTA's share of the cost is below that of a
-  // segment's first stage; the starts of CTAs c0 < c <= c1 + 1 are found
-  // from the segment's own cost offsets.
+  // Empty ranges (two 64-bit divisions to detect) exist only when a CTA's
+  // share of the cost is below that of a segment's first stage; the starts
+  // of CTAs c0 < c <= c1 + 1 are found from the segment's own cost offsets.
   const bool may_be_empty = Wc < (kUnit + sc) * ctas;
   auto start_in = [&](int64_t c) { return first + stage_at(cost_target(c, Wc, ctas) - cf, sc); };
-  for (int k0 = warp; k0 < np; k0 += 4 * kMergeWarps) {
-    float lv[4], x[4][VPL];
+  const int r = r0 + rl;
+  if (rl < nr) {
+    for (int k0 = sub; k0 < np; k0 += KB * wpr) {
+      float lv[KB], x[KB][VPL];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int k = k0 + i * kMergeWarps;
-      const int64_t c = c0 + k;
-      const bool ok = k < np && (k == 0 || !may_be_empty || start_in(c) != start_in(c + 1));
-      const int64_t slot = k == 0 ? 2 * c0 + 1 : 2 * c;
-      lv[i] = ok ? pl[slot * rows + r] : -INFINITY;
-      const float *src = po + (slot * rows + r) * D + lane * VPL;
-      if constexpr (VPL == 4) {
-        const float4 v = ok ? __ldg(reinterpret_cast<const float4 *>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        x[i][0] = v.x, x[i][1] = v.y, x[i][2] = v.z, x[i][3] = v.w;
-      } else {
-        const float2 v = ok ? __ldg(reinterpret_cast<const float2 *>(src)) : make_float2(0.f, 0.f);
-        x[i][0] = v.x, x[i][1] = v.y;
+      for (int i = 0; i < KB; ++i) {
+        const int k = k0 + i * wpr;
+        const int64_t c = c0 + k;
+        const bool ok = k < np && (k == 0 || !may_be_empty || start_in(c) != start_in(c + 1));
+        const int64_t slot = k == 0 ? 2 * c0 + 1 : 2 * c;
+        lv[i] = ok ? pl[slot * rows + r] : -INFINITY;
+        const float *src = po + (slot * rows + r) * D + lane * VPL;
+        if constexpr (VPL == 4) {
+          const float4 v = ok ? __ldg(reinterpret_cast<const float4 *>(src)) : make_float4(0.f, 0.f, 0.f, 0.f);
+          x[i][0] = v.x, x[i][1] = v.y, x[i][2] = v.z, x[i][3] = v.w;
+        } else {
+          const float2 v = ok ? __ldg(reinterpret_cast<const float2 *>(src)) : make_float2(0.f, 0.f);
+          x[i][0] = v.x, x[i][1] = v.y;
+        }
       }
-    }
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (lv[i] == -INFINITY) continue;  // absent, or that split saw no key (its O is never used)
-      const float mn = fmaxf(m, lv[i]);
-      const float sc = expf(m - mn), e = expf(lv[i] - mn);
-      z = z * sc + e;
+      for (int i = 0; i < KB; ++i) {
+        if (lv[i] == -INFINITY) continue;  // absent, or that split saw no key (its O is never used)
+        const float mn = fmaxf(m, lv[i]);
+        const float sc2 = expf(m - mn), e = expf(lv[i] - mn);
+        z = z * sc2 + e;
 #pragma unroll
-      for (int j = 0; j < VPL; ++j) acc[j] = acc[j] * sc + e * x[i][j];
-      m = mn;
+        for (int j = 0; j < VPL; ++j) acc[j] = acc[j] * sc2 + e * x[i][j];
+        m = mn;
+      }
     }
   }
 #pragma unroll
   for (int j = 0; j < VPL; ++j) accs[warp][lane * VPL + j] = acc[j];
   if (lane == 0) wm[warp] = m, wz[warp] = z;
   __syncthreads();
-  float M = wm[0];
-  for (int w = 1; w < kMergeWarps; ++w) M = fmaxf(M, wm[w]);
-  float Z = 0.f;
-  for (int w = 0; w < kMergeWarps; ++w) Z += wm[w] == -INFINITY ? 0.f : wz[w] * expf(wm[w] - M);
-  const float inv = M == -INFINITY ? 0.f : 1.f / Z;
-  for (int d = threadIdx.x; d < D; d += kMergeWarps * 32) {
-    float o = 0.f;
-#pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w)
-      if (wm[w] != -INFINITY) o += accs[w][d] * expf(wm[w] - M);
+  for (int i = threadIdx.x; i < nr * D; i += kWarps * 32) {
+    const int rr = i / D, d = i - rr * D, w0 = rr * wpr;
+    float M = wm[w0];
+    for (int w = 1; w < wpr; ++w) M = fmaxf(M, wm[w0 + w]);
+    float Z = 0.f, o = 0.f;
+    for (int w = 0; w < wpr; ++w) {
+      if (wm[w0 + w] == -INFINITY) continue;
+      const float e = expf(wm[w0 + w] - M);
+      Z += wz[w0 + w] * e, o += accs[w0 + w][d] * e;
+    }
+    const int64_t row = out_row(r0 + rr);
+    if (row < 0) continue;
+    const float inv = M == -INFINITY ? 0.f : 1.f / Z;
     out[row * D + d] = __half_as_ushort(__float2half_rn(o * inv));
+    if (d == 0 && lse) lse[row] = M == -INFINITY ? -INFINITY : M + logf(Z);
   }
-  if (threadIdx.x == 0 && lse) lse[row] = M == -INFINITY ? -INFINITY : M + logf(Z);
 }
 
 cudaLaunchAttribute pdl_attr() {
@@ -1379,13 +1396,18 @@ cudaError_t launch_d(const DecodeArgs &a0, const KvView &cache, const DecodeMaps
     e = cudaLaunchKernelEx(&cfg, decode_kernel<D, W, BITS>, a, cache, maps, err);
   if (e != cudaSuccess || a.cluster > 0) return e;
   const int64_t limit = cache.page_table ? static_cast<int64_t>(cache.max_pages) * kPage : cache.capacity;
+  // one merge CTA per segment when segments are many (about two ranges or
+  // fewer each), else one per row of a segment (rows = hb * G <= 32)
+  const int64_t segments = static_cast<int64_t>(a.batch) * geo.groups;
+  const bool per_segment = 2 * segments >= a.ctas;
   cudaLaunchConfig_t mc = {};
-  mc.gridDim = dim3(a.batch * geo.groups, geo.hb * G);
-  mc.blockDim = dim3(kMergeWarps * 32);
+  mc.gridDim = dim3(static_cast<unsigned>(segments), per_segment ? 1 : geo.hb * G);
+  mc.blockDim = dim3(per_segment ? 1024 : 256);
   mc.stream = stream;
   mc.attrs = attr;
   mc.numAttrs = 1;
-  return cudaLaunchKernelEx(&mc, decode_merge_kernel<D, W>, a.seq_lens, a.batch, cache.hkv, G, a.ctas, limit,
+  return cudaLaunchKernelEx(&mc, per_segment ? decode_merge_kernel<D, W, 32> : decode_merge_kernel<D, W, 8>,
+                            a.seq_lens, a.batch, cache.hkv, G, a.ctas, limit,
                             static_cast<int>(paged), cache.head_map, static_cast<int>(cache.model_hkv),
                             static_cast<const float *>(a.partial_o), static_cast<const float *>(a.partial_lse),
                             a.out, a.lse);
